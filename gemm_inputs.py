@@ -1,0 +1,155 @@
+"""Seeded synthetic inputs for the GEMM workloads.
+
+This module only draws and encodes operands; it holds none of the GEMM's
+arithmetic.  Both the CUDA path (through tests and ``bench.py``) and the CPU
+oracle receive the operands it produces, so parity never depends on random
+number stability across versions: every run regenerates the same tensors for
+both sides.
+
+Recipe (one torch CPU generator per workload, A drawn before B, row-major):
+
+===================== ===================================== ==================
+workload               shape / distribution                  seed
+===================== ===================================== ==================
+single_tile            M=N=128, K=64, uniform[-1,1) -> bf16   0
+square_4096            M=N=K=4096, N(0,1) -> bf16              1
+ragged_k1040           M=4099, N=2053, K=1040, N(0,1) -> bf16  2
+ragged_k8              M=4099, N=2053, K=8,    N(0,1) -> bf16  2
+square_8192            M=N=K=8192, 0.5*N(0,1) -> bf16          3
+mxfp8_8192             M=N=K=8192, N(0,1) -> MXFP8             4
+===================== ===================================== ==================
+
+bf16 rounding is torch's float32 -> bfloat16 cast (round-to-nearest-even).
+MXFP8 encoding of a float32 row: for each block of 32 consecutive k (the
+last block may be partial) take amax = max |x|, the scale exponent e is the
+smallest integer with amax <= 448 * 2^e (clamped to [-127, 127]; amax = 0
+gives e = -127), the scale byte is e + 127 (UE8M0) and each element is
+x * 2^-e rounded to E4M3 (round-to-nearest-even; |x * 2^-e| <= 448 by
+construction, so no saturation is needed).  Scale rows are padded with zero
+bytes to a multiple of 16, the row pitch the library requires.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    M: int
+    N: int
+    K: int
+    seed: int
+    dist: str            # "uniform" | "normal"
+    scale: float = 1.0
+    kind: str = "bf16"   # "bf16" | "mxfp8"
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+
+WORKLOADS = {
+    w.name: w for w in [
+        Workload("single_tile", 128, 128, 64, 0, "uniform"),
+        Workload("square_4096", 4096, 4096, 4096, 1, "normal"),
+        Workload("ragged_k1040", 4099, 2053, 1040, 2, "normal"),
+        Workload("ragged_k8", 4099, 2053, 8, 2, "normal"),
+        Workload("square_8192", 8192, 8192, 8192, 3, "normal", 0.5),
+        Workload("mxfp8_8192", 8192, 8192, 8192, 4, "normal", 1.0, "mxfp8"),
+    ]
+}
+
+
+def _draw(g: torch.Generator, rows: int, cols: int, dist: str, scale: float) -> torch.Tensor:
+    if dist == "uniform":
+        x = torch.rand(rows, cols, generator=g, dtype=torch.float32) * 2 - 1
+    elif dist == "normal":
+        x = torch.randn(rows, cols, generator=g, dtype=torch.float32)
+    else:
+        raise ValueError(dist)
+    if scale != 1.0:
+        x = x * scale
+    return x
+
+
+def float_operands(M: int, N: int, K: int, seed: int, dist: str = "normal",
+                   scale: float = 1.0):
+    """float32 A [M,K] and B [N,K], A drawn first."""
+    g = torch.Generator().manual_seed(seed)
+    A = _draw(g, M, K, dist, scale)
+    B = _draw(g, N, K, dist, scale)
+    return A, B
+
+
+def bf16_operands(M: int, N: int, K: int, seed: int, dist: str = "normal",
+                  scale: float = 1.0):
+    """bf16 A [M,K] and B [N,K] (CPU tensors, contiguous)."""
+    A, B = float_operands(M, N, K, seed, dist, scale)
+    return A.to(torch.bfloat16), B.to(torch.bfloat16)
+
+
+def sf_pitch(K: int) -> int:
+    """Row pitch, in bytes, of a scale-factor matrix for reduction length K."""
+    nblk = (K + 31) // 32
+    return max(16, (nblk + 15) // 16 * 16)
+
+
+def mxfp8_quantize(x: torch.Tensor):
+    """Encode float32 rows [R, K] as (E4M3 codes uint8 [R, K], UE8M0 scale
+    bytes uint8 [R, sf_pitch(K)]), one scale per 32 consecutive k."""
+    if x.dtype != torch.float32 or x.dim() != 2:
+        raise TypeError("expected a 2-D float32 tensor")
+    R, K = x.shape
+    nblk = (K + 31) // 32
+    pad = nblk * 32 - K
+    xp = torch.nn.functional.pad(x, (0, pad)) if pad else x
+    blocks = xp.reshape(R, nblk, 32).double()
+    amax = blocks.abs().amax(dim=2)                                  # [R, nblk]
+    # smallest integer e with amax <= 448 * 2^e: a float guess, then exact fix-ups
+    safe = torch.where(amax > 0, amax, torch.ones_like(amax))
+    e = torch.ceil(torch.log2(safe / 448.0))
+    four48 = torch.full_like(e, 448.0)
+    for _ in range(2):
+        e = torch.where(amax > torch.ldexp(four48, e), e + 1, e)
+        e = torch.where(amax <= torch.ldexp(four48, e - 1), e - 1, e)
+    e = torch.where(amax > 0, e, torch.full_like(e, -127.0)).clamp(-127, 127)
+    scaled = torch.ldexp(blocks, -e.unsqueeze(2))                    # exact
+    q = scaled.float().to(torch.float8_e4m3fn).view(torch.uint8)
+    q = q.reshape(R, nblk * 32)[:, :K].contiguous()
+    sf = torch.zeros(R, sf_pitch(K), dtype=torch.uint8)
+    sf[:, :nblk] = (e + 127).to(torch.uint8)
+    return q, sf
+
+
+def mxfp8_operands(M: int, N: int, K: int, seed: int, dist: str = "normal",
+                   scale: float = 1.0):
+    """(A codes [M,K], SFA [M,pitch], B codes [N,K], SFB [N,pitch]), uint8."""
+    A, B = float_operands(M, N, K, seed, dist, scale)
+    qa, sfa = mxfp8_quantize(A)
+    qb, sfb = mxfp8_quantize(B)
+    return qa, sfa, qb, sfb
+
+
+def workload_operands(name: str):
+    """Operands of a named workload: (A, B) for bf16, (A, SFA, B, SFB) for MXFP8."""
+    w = WORKLOADS[name]
+    if w.kind == "bf16":
+        return bf16_operands(w.M, w.N, w.K, w.seed, w.dist, w.scale)
+    return mxfp8_operands(w.M, w.N, w.K, w.seed, w.dist, w.scale)
+
+
+def bf16_codes(t: torch.Tensor) -> np.ndarray:
+    """uint16 bit patterns of a CPU bf16 tensor (a view, no arithmetic)."""
+    if t.dtype != torch.bfloat16:
+        raise TypeError("expected bfloat16")
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def u8_codes(t: torch.Tensor) -> np.ndarray:
+    if t.dtype != torch.uint8:
+        raise TypeError("expected uint8")
+    return t.contiguous().numpy()

@@ -1,0 +1,282 @@
+"""Pins for the CPU oracle: checks against facts that do not come from it.
+
+Each ``pin_*`` takes an ``oracle.Oracle`` and raises AssertionError when the
+oracle disagrees with a value fixed by a number-format definition (checked
+through torch's own conversions of every bit pattern), by exact rational
+arithmetic on tiny inputs, or by a closed form (all-ones, identity, K=1 outer
+product, small-integer products, NaN/Inf propagation).  The shapes are
+asymmetric (M != N != K, leading dimensions wider than K) so that a
+transposed operand, a swapped index or an ignored stride changes the result.
+
+``test_oracle.py`` runs every pin on the real oracle; ``test_oracle_mutants.py``
+runs them on deliberately broken copies of it and requires each copy to fail
+at least one pin.
+"""
+from __future__ import annotations
+
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+BF16_ONE = 0x3F80
+
+
+# ------------------------------------------------------------------ helpers
+
+def torch_bf16_f64(codes: np.ndarray) -> np.ndarray:
+    """bf16 codes -> float64 through torch's own conversion."""
+    t = torch.from_numpy(np.ascontiguousarray(codes).view(np.int16)).view(torch.bfloat16)
+    return t.double().numpy()
+
+
+def torch_e4m3_f64(codes: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn)
+    return t.float().double().numpy()
+
+
+def random_bf16_codes(rng: np.random.Generator, shape, scale=1.0) -> np.ndarray:
+    x = torch.from_numpy(rng.standard_normal(shape).astype(np.float32) * np.float32(scale))
+    return x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def random_e4m3_codes(rng: np.random.Generator, shape) -> np.ndarray:
+    c = rng.integers(0, 256, size=shape, dtype=np.uint8)
+    c[(c & 0x7F) == 0x7F] = 0x3F          # no NaN codes
+    return c
+
+
+def same(a: np.ndarray, b: np.ndarray) -> bool:
+    """Equal as values, NaN equal to NaN."""
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    return a.shape == b.shape and bool(np.all((a == b) | (np.isnan(a) & np.isnan(b))))
+
+
+def exact_dot(avals, bvals) -> tuple[Fraction, Fraction]:
+    s = Fraction(0)
+    sa = Fraction(0)
+    for a, b in zip(avals, bvals):
+        p = a * b
+        s += p
+        sa += abs(p)
+    return s, sa
+
+
+# --------------------------------------------------------- number formats
+
+def pin_bf16_decode_all(o):
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    assert same(o.bf16_to_f64(codes), torch_bf16_f64(codes)), "bf16 decode"
+
+
+def pin_e4m3_decode_all(o):
+    codes = np.arange(256, dtype=np.uint16).astype(np.uint8)
+    got = o.e4m3_to_f64(codes)
+    assert same(got, torch_e4m3_f64(codes)), "E4M3 decode"
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x08] == 2.0 ** -6
+    assert np.isnan(got[0x7F]) and np.isnan(got[0xFF])
+
+
+def pin_ue8m0_decode_all(o):
+    codes = np.arange(256, dtype=np.uint16).astype(np.uint8)
+    got = o.ue8m0_to_f64(codes)
+    if hasattr(torch, "float8_e8m0fnu"):
+        ref = torch.from_numpy(codes).view(torch.float8_e8m0fnu).float().double().numpy()
+        assert same(got, ref), "UE8M0 decode"
+    assert got[127] == 1.0 and got[128] == 2.0 and got[126] == 0.5
+    assert np.isnan(got[255])
+
+
+def pin_bf16_rne(o):
+    rng = np.random.default_rng(11)
+    vals = [rng.standard_normal(4000).astype(np.float32),
+            (rng.standard_normal(1000) * 1e-38).astype(np.float32),       # bf16 subnormals
+            (rng.standard_normal(1000) * 1e38).astype(np.float32)]
+    # exact midpoints between neighbouring bf16 values (ties): 9 significant bits
+    mids = []
+    for code in rng.integers(0x0080, 0x7F00, size=2000):
+        lo = np.array([code], np.uint32) << 16
+        mids.append((lo + (1 << 15)).view(np.float32)[0])
+    vals.append(np.array(mids, np.float32))
+    vals.append(-np.array(mids, np.float32))
+    vals.append(np.array([0.0, -0.0, np.inf, -np.inf, 3.3895314e38, 3.4e38], np.float32))
+    v = np.concatenate(vals)
+    got = o.f64_to_bf16_rne(v.astype(np.float64))
+    ref = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, ref), "bf16 RNE"
+    assert o.f64_to_bf16_rne(np.array([np.nan]))[0] & 0x7FFF > 0x7F80
+
+
+# ------------------------------------------------------------- bf16 GEMM
+
+def pin_bruteforce_bf16(o):
+    rng = np.random.default_rng(1)
+    for (M, N, K, lda, ldb) in [(3, 5, 7, 9, 8), (5, 2, 40, 40, 48), (1, 4, 33, 36, 33),
+                                (4, 3, 1, 3, 1)]:
+        A = random_bf16_codes(rng, (M, lda), 4.0)
+        B = random_bf16_codes(rng, (N, ldb), 0.25)
+        D, S = o.gemm_bf16(A, B, K)
+        Af = torch_bf16_f64(A)
+        Bf = torch_bf16_f64(B)
+        for i in range(M):
+            for j in range(N):
+                s, sa = exact_dot([Fraction(x) for x in Af[i, :K]],
+                                  [Fraction(x) for x in Bf[j, :K]])
+                tol = K * 2.0 ** -52 * float(sa)
+                assert abs(Fraction(D[i, j]) - s) <= Fraction(tol), ("bf16 brute", M, N, K, i, j)
+                assert abs(Fraction(S[i, j]) - sa) <= Fraction(tol), ("abs sum", i, j)
+
+
+def pin_all_ones(o):
+    for K in (1, 8, 64, 1040, 4096):
+        A = np.full((3, K + 8), BF16_ONE, np.uint16)
+        B = np.full((5, K), BF16_ONE, np.uint16)
+        D, S = o.gemm_bf16(A, B, K)
+        assert np.all(D == K) and np.all(S == K), ("all ones", K)
+
+
+def pin_identity(o):
+    rng = np.random.default_rng(2)
+    for K, N in ((128, 37), (256, 5), (16, 300)):
+        A = np.zeros((K, K), np.uint16)
+        A[np.arange(K), np.arange(K)] = BF16_ONE
+        B = random_bf16_codes(rng, (N, K))
+        D, _ = o.gemm_bf16(A, B)
+        assert same(D, torch_bf16_f64(B).T), ("identity", K, N)
+
+
+def pin_k1_outer(o):
+    rng = np.random.default_rng(3)
+    A = random_bf16_codes(rng, (6, 1), 3.0)
+    B = random_bf16_codes(rng, (9, 1), 0.5)
+    D, _ = o.gemm_bf16(A, B)
+    assert same(D, np.outer(torch_bf16_f64(A)[:, 0], torch_bf16_f64(B)[:, 0])), "K=1"
+
+
+def pin_small_int_bf16(o):
+    rng = np.random.default_rng(4)
+    M, N, K = 13, 7, 70
+    Ai = rng.integers(-2, 3, size=(M, K))
+    Bi = rng.integers(-2, 3, size=(N, K))
+    A = torch.from_numpy(Ai.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    B = torch.from_numpy(Bi.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    D, S = o.gemm_bf16(A, B)
+    assert np.array_equal(D, (Ai @ Bi.T).astype(np.float64)), "small integers"
+    assert np.array_equal(S, (np.abs(Ai) @ np.abs(Bi).T).astype(np.float64)), "small integer |.|"
+
+
+def pin_entries_bf16(o):
+    rng = np.random.default_rng(5)
+    A = random_bf16_codes(rng, (17, 50))
+    B = random_bf16_codes(rng, (11, 50))
+    D, S = o.gemm_bf16(A, B, 45)
+    rows = rng.integers(0, 17, 40)
+    cols = rng.integers(0, 11, 40)
+    De, Se = o.gemm_bf16_entries(A, B, rows, cols, 45)
+    assert np.array_equal(De, D[rows, cols]) and np.array_equal(Se, S[rows, cols]), "entries"
+
+
+def pin_nonfinite(o):
+    A = np.full((4, 6), BF16_ONE, np.uint16)
+    B = np.full((3, 6), BF16_ONE, np.uint16)
+    A[2, 3] = 0x7FC0                  # NaN in row 2
+    A[1, 0] = 0x7F80                  # +Inf in row 1 ...
+    B[2, 0] = 0x0000                  # ... meets a zero in column 2: Inf * 0 = NaN
+    D, _ = o.gemm_bf16(A, B)
+    assert np.all(np.isnan(D[2])), "NaN row"
+    assert np.isposinf(D[1, 0]) and np.isposinf(D[1, 1]) and np.isnan(D[1, 2]), "Inf row"
+    assert np.all(np.isfinite(D[[0, 3]])), "finite rows"
+
+
+# ------------------------------------------------------------ MXFP8 GEMM
+
+def _mx_exact_values(codes, sf, K):
+    dec = torch_e4m3_f64(codes)
+    rows = []
+    for r in range(codes.shape[0]):
+        rows.append([Fraction(dec[r, k]) * Fraction(2) ** (int(sf[r, k // 32]) - 127)
+                     for k in range(K)])
+    return rows
+
+
+def pin_bruteforce_mxfp8(o):
+    rng = np.random.default_rng(6)
+    for (M, N, K) in [(3, 4, 40), (2, 5, 97), (4, 1, 64)]:
+        nblk = (K + 31) // 32
+        A = random_e4m3_codes(rng, (M, K + 16))
+        B = random_e4m3_codes(rng, (N, K))
+        SFA = rng.integers(112, 142, size=(M, nblk + 3), dtype=np.uint8)
+        SFB = rng.integers(112, 142, size=(N, nblk), dtype=np.uint8)
+        D, S = o.gemm_mxfp8(A, B, SFA, SFB, K)
+        av = _mx_exact_values(A, SFA, K)
+        bv = _mx_exact_values(B, SFB, K)
+        for i in range(M):
+            for j in range(N):
+                s, sa = exact_dot(av[i], bv[j])
+                tol = Fraction(K * 2.0 ** -52) * sa
+                assert abs(Fraction(D[i, j]) - s) <= tol, ("mxfp8 brute", M, N, K, i, j)
+                assert abs(Fraction(S[i, j]) - sa) <= tol, ("mxfp8 abs sum", i, j)
+
+
+def pin_small_int_mxfp8(o):
+    """Integer E4M3 values with per-(row, block) power-of-two scales: every
+    partial sum is exact, so D equals an integer product rescaled exactly."""
+    rng = np.random.default_rng(7)
+    M, N, K = 9, 6, 160
+    nblk = K // 32
+    Ai = rng.integers(-4, 5, size=(M, K))
+    Bi = rng.integers(-4, 5, size=(N, K))
+    ea = rng.integers(120, 135, size=(M, nblk))
+    eb = rng.integers(120, 135, size=(N, nblk))
+    A = torch.from_numpy(Ai.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    B = torch.from_numpy(Bi.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    D, _ = o.gemm_mxfp8(A, B, ea.astype(np.uint8), eb.astype(np.uint8))
+    for i in range(M):
+        for j in range(N):
+            ref = Fraction(0)
+            for b in range(nblk):
+                blk = int(Ai[i, 32 * b:32 * b + 32] @ Bi[j, 32 * b:32 * b + 32])
+                ref += blk * Fraction(2) ** (int(ea[i, b]) + int(eb[j, b]) - 254)
+            assert Fraction(D[i, j]) == ref, ("mxfp8 integers", i, j)
+
+
+def pin_identity_mxfp8(o):
+    rng = np.random.default_rng(8)
+    K, N = 96, 7
+    A = np.zeros((K, K), np.uint8)
+    A[np.arange(K), np.arange(K)] = 0x38          # E4M3 1.0
+    SFA = np.full((K, 3), 127, np.uint8)          # scale 1
+    B = random_e4m3_codes(rng, (N, K))
+    SFB = rng.integers(120, 135, size=(N, 3), dtype=np.uint8)
+    D, _ = o.gemm_mxfp8(A, B, SFA, SFB)
+    ref = np.array([[float(v) for v in row] for row in _mx_exact_values(B, SFB, K)]).T
+    assert same(D, ref), "mxfp8 identity"
+
+
+def pin_entries_mxfp8(o):
+    rng = np.random.default_rng(9)
+    A = random_e4m3_codes(rng, (8, 80))
+    B = random_e4m3_codes(rng, (6, 80))
+    SFA = rng.integers(120, 135, size=(8, 3), dtype=np.uint8)
+    SFB = rng.integers(120, 135, size=(6, 3), dtype=np.uint8)
+    D, S = o.gemm_mxfp8(A, B, SFA, SFB, 70)
+    rows = rng.integers(0, 8, 30)
+    cols = rng.integers(0, 6, 30)
+    De, Se = o.gemm_mxfp8_entries(A, B, SFA, SFB, rows, cols, 70)
+    assert np.array_equal(De, D[rows, cols]) and np.array_equal(Se, S[rows, cols]), "mx entries"
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
+
+
+def failing_pins(o) -> list[str]:
+    """Names of the pins that the given oracle fails (or crashes in)."""
+    bad = []
+    for pin in ALL_PINS:
+        try:
+            pin(o)
+        except Exception:          # an assertion or a crash both count
+            bad.append(pin.__name__)
+    return bad
+
