@@ -1,0 +1,202 @@
+"""Python binding of the GB300 tcgen05 GEMM library (``include/gemm_gb300.h``).
+
+Argument marshalling only: every step of the GEMM runs in the CUDA library's
+own kernels.  The entry points keep the C names and arguments (raw device
+pointers as integers, sizes, leading dimensions in elements, a CUDA stream
+handle); ``matmul_bf16`` / ``matmul_mxfp8`` are conveniences that take torch
+CUDA tensors, call the same entry points on the current stream and raise on
+a non-zero status.  There is no CPU or library fallback: when the CUDA
+library cannot be built or loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+from . import _build
+
+__all__ = [
+    "GEMM_OK", "GEMM_ERR_INVALID_ARG", "GEMM_ERR_ALIGNMENT", "GEMM_ERR_UNSUPPORTED_DEVICE",
+    "GEMM_ERR_LAUNCH", "GEMM_ERR_TIMEOUT", "GEMM_ERR_DEVICE_FAULT",
+    "VARIANT_AUTO", "VARIANT_1CTA", "VARIANT_2CTA", "VARIANT_SYNC", "VARIANT_DIRECT_STORE",
+    "GemmError", "load", "library_path", "EXPORTED_SYMBOLS",
+    "gemm_bf16", "gemm_bf16_variant", "gemm_mxfp8", "gemm_mxfp8_variant",
+    "gemm_last_status", "gemm_last_status_word", "gemm_status_string", "gemm_set_watchdog_ms",
+    "gemm_kernel_plan", "matmul_bf16", "matmul_mxfp8",
+]
+
+GEMM_OK = 0
+GEMM_ERR_INVALID_ARG = -1
+GEMM_ERR_ALIGNMENT = -2
+GEMM_ERR_UNSUPPORTED_DEVICE = -3
+GEMM_ERR_LAUNCH = -4
+GEMM_ERR_TIMEOUT = -5
+GEMM_ERR_DEVICE_FAULT = -6
+
+VARIANT_AUTO = 0
+VARIANT_1CTA = 1
+VARIANT_2CTA = 2
+VARIANT_SYNC = 3
+VARIANT_DIRECT_STORE = 0x100
+
+# Every function include/gemm_gb300.h declares.
+EXPORTED_SYMBOLS = (
+    "gemm_bf16", "gemm_bf16_variant", "gemm_mxfp8", "gemm_mxfp8_variant", "gemm_last_status",
+    "gemm_last_status_word", "gemm_status_string", "gemm_set_watchdog_ms", "gemm_kernel_plan",
+)
+
+_lock = threading.Lock()
+_lib = None
+_i64 = ctypes.c_int64
+_vp = ctypes.c_void_p
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {gemm_status_string(status)} ({status})" if what
+                         else f"{gemm_status_string(status)} ({status})")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load the CUDA library, building it in-tree first if it is missing or
+    older than its sources.  Raises if it cannot be built or loaded."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            L = ctypes.CDLL(path)
+            L.gemm_bf16.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _i64, _vp]
+            L.gemm_bf16_variant.argtypes = [ctypes.c_int, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
+                                            _i64, _i64, _vp]
+            L.gemm_mxfp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _i64,
+                                     _i64, _i64, _vp]
+            L.gemm_mxfp8_variant.argtypes = [ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _i64, _i64,
+                                             _i64, _i64, _i64, _i64, _i64, _i64, _vp]
+            for name in ("gemm_bf16", "gemm_bf16_variant", "gemm_mxfp8", "gemm_mxfp8_variant"):
+                getattr(L, name).restype = ctypes.c_int
+            L.gemm_last_status.argtypes = [_vp]
+            L.gemm_last_status.restype = ctypes.c_int
+            L.gemm_last_status_word.argtypes = [_vp]
+            L.gemm_last_status_word.restype = ctypes.c_uint64
+            L.gemm_status_string.argtypes = [ctypes.c_int]
+            L.gemm_status_string.restype = ctypes.c_char_p
+            L.gemm_set_watchdog_ms.argtypes = [_i64]
+            L.gemm_set_watchdog_ms.restype = _i64
+            P = ctypes.POINTER(ctypes.c_int32)
+            L.gemm_kernel_plan.argtypes = [ctypes.c_int, ctypes.c_int, P, P, P, P, P, P, P]
+            L.gemm_kernel_plan.restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+# ------------------------------------------------------------- C entry points
+
+def gemm_bf16(A: int, B: int, D: int, M: int, N: int, K: int, lda: int, ldb: int, ldd: int,
+              stream: int = 0) -> int:
+    return load().gemm_bf16(A, B, D, M, N, K, lda, ldb, ldd, stream)
+
+
+def gemm_bf16_variant(variant: int, A: int, B: int, D: int, M: int, N: int, K: int, lda: int,
+                      ldb: int, ldd: int, stream: int = 0) -> int:
+    return load().gemm_bf16_variant(variant, A, B, D, M, N, K, lda, ldb, ldd, stream)
+
+
+def gemm_mxfp8(A: int, B: int, SFA: int, SFB: int, D: int, M: int, N: int, K: int, lda: int,
+               ldb: int, ldsfa: int, ldsfb: int, ldd: int, stream: int = 0) -> int:
+    return load().gemm_mxfp8(A, B, SFA, SFB, D, M, N, K, lda, ldb, ldsfa, ldsfb, ldd, stream)
+
+
+def gemm_mxfp8_variant(variant: int, A: int, B: int, SFA: int, SFB: int, D: int, M: int, N: int,
+                       K: int, lda: int, ldb: int, ldsfa: int, ldsfb: int, ldd: int,
+                       stream: int = 0) -> int:
+    return load().gemm_mxfp8_variant(variant, A, B, SFA, SFB, D, M, N, K, lda, ldb, ldsfa, ldsfb,
+                                     ldd, stream)
+
+
+def gemm_last_status(stream: int = 0) -> int:
+    return load().gemm_last_status(stream)
+
+
+def gemm_last_status_word(stream: int = 0) -> int:
+    return int(load().gemm_last_status_word(stream))
+
+
+def gemm_status_string(status: int) -> str:
+    return load().gemm_status_string(status).decode()
+
+
+def gemm_set_watchdog_ms(ms: int) -> int:
+    return int(load().gemm_set_watchdog_ms(ms))
+
+
+def gemm_kernel_plan(mxfp8: bool, variant: int) -> dict:
+    vals = [ctypes.c_int32() for _ in range(7)]
+    rc = load().gemm_kernel_plan(int(bool(mxfp8)), variant, *[ctypes.byref(v) for v in vals])
+    if rc != GEMM_OK:
+        raise GemmError(rc, "gemm_kernel_plan")
+    keys = ("stages", "smem_bytes", "tmem_cols", "threads", "cluster", "tile_m", "tile_n")
+    return {k: v.value for k, v in zip(keys, vals)}
+
+
+# ------------------------------------------------------- torch conveniences
+
+def _stream_handle(stream) -> int:
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _check_2d(t, name):
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be a 2-D tensor with unit column stride")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def matmul_bf16(A, B, out=None, variant: int = VARIANT_AUTO, stream=None):
+    """D = A @ B.T for bf16 CUDA tensors A [M,K], B [N,K]; returns D [M,N] bf16."""
+    import torch
+    _check_2d(A, "A")
+    _check_2d(B, "B")
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
+        raise TypeError("A and B must be bfloat16")
+    M, K = A.shape
+    N = B.shape[0]
+    if B.shape[1] != K:
+        raise ValueError("A and B disagree on K")
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=A.device)
+    _check_2d(out, "out")
+    rc = gemm_bf16_variant(variant, A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K,
+                           A.stride(0), B.stride(0), out.stride(0), _stream_handle(stream))
+    if rc != GEMM_OK:
+        raise GemmError(rc, "gemm_bf16")
+    return out
+
+
+def matmul_mxfp8(A, SFA, B, SFB, out=None, variant: int = VARIANT_AUTO, stream=None):
+    """Block-scaled D = A @ B.T: A [M,K], B [N,K] E4M3 codes (uint8 or
+    float8_e4m3fn), SFA [M,>=ceil(K/32)], SFB [N,>=ceil(K/32)] UE8M0 bytes."""
+    import torch
+    for t, n in ((A, "A"), (B, "B"), (SFA, "SFA"), (SFB, "SFB")):
+        _check_2d(t, n)
+        if t.element_size() != 1:
+            raise TypeError(f"{n} must hold one byte per element")
+    M, K = A.shape
+    N = B.shape[0]
+    if B.shape[1] != K:
+        raise ValueError("A and B disagree on K")
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=A.device)
+    _check_2d(out, "out")
+    rc = gemm_mxfp8_variant(variant, A.data_ptr(), B.data_ptr(), SFA.data_ptr(), SFB.data_ptr(),
+                            out.data_ptr(), M, N, K, A.stride(0), B.stride(0), SFA.stride(0),
+                            SFB.stride(0), out.stride(0), _stream_handle(stream))
+    if rc != GEMM_OK:
+        raise GemmError(rc, "gemm_mxfp8")
+    return out

@@ -1,0 +1,335 @@
+// The C ABI (include/gemm_gb300.h): argument validation, per-device set-up,
+// tensor-map encoding, kernel choice and the device status word.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "gemm_gb300.h"
+#include "gemm_host.h"
+#include "kernel_common.cuh"
+
+// The library's only device state: the watchdog status word (first error
+// wins; cleared by gemm_last_status).
+static __device__ unsigned long long g_status_word = 0ull;
+
+namespace gb300 {
+namespace {
+
+constexpr int kMaxDevices = 128;
+
+struct DeviceState {
+  int state = 0;  // 0 = not yet set up, 1 = ready, < 0 = gemm_status_t failure
+  int num_sms = 0;
+  unsigned long long* status = nullptr;
+};
+
+std::mutex g_mu;
+DeviceState g_devices[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::atomic<int64_t> g_watchdog_ms{-1};
+
+int64_t watchdog_ms() {
+  int64_t v = g_watchdog_ms.load();
+  if (v < 0) {
+    int64_t def = 2000;
+    if (const char* e = std::getenv("GEMM_WATCHDOG_MS")) {
+      const long long x = std::atoll(e);
+      if (x > 0) def = x;
+    }
+    int64_t expected = -1;
+    g_watchdog_ms.compare_exchange_strong(expected, def);
+    v = g_watchdog_ms.load();
+  }
+  return v;
+}
+
+// Current device: compute capability 10.3 required; SM count, the status
+// word's device address and the tensor-map encoder are looked up once.
+int current_device(LaunchCtx* ctx) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return GEMM_ERR_UNSUPPORTED_DEVICE;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& d = g_devices[dev];
+  if (d.state == 0) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      d.state = GEMM_ERR_UNSUPPORTED_DEVICE;
+    } else if (major != 10 || minor != 3) {
+      d.state = GEMM_ERR_UNSUPPORTED_DEVICE;
+    } else {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) {
+        cudaGetLastError();
+        d.state = GEMM_ERR_LAUNCH;
+      } else {
+        d.status = static_cast<unsigned long long*>(p);
+        d.num_sms = sms;
+        d.state = 1;
+      }
+    }
+    if (d.state == 1 && g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr) {
+        cudaGetLastError();
+        d.state = GEMM_ERR_LAUNCH;
+      } else {
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+      }
+    }
+  }
+  if (d.state != 1) return d.state;
+  ctx->device = dev;
+  ctx->num_sms = d.num_sms;
+  ctx->status = d.status;
+  return GEMM_OK;
+}
+
+// True when `p` is memory the current device can address (device or managed).
+bool is_device_pointer(const void* p, int dev) {
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (attr.type == cudaMemoryTypeManaged) return true;
+  return attr.type == cudaMemoryTypeDevice && attr.device == dev;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+// Shape and pitch checks shared by both element types (esize: operand bytes).
+int check_shape(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+                int64_t lda, int64_t ldb, int64_t ldd, int64_t esize) {
+  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return GEMM_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return GEMM_OK;
+  if (D == nullptr || ldd < N || ldd > (int64_t(1) << 36)) return GEMM_ERR_INVALID_ARG;
+  if (K == 0) return GEMM_OK;
+  if (A == nullptr || B == nullptr || lda < K || ldb < K || lda > (int64_t(1) << 36) ||
+      ldb > (int64_t(1) << 36))
+    return GEMM_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || (lda * esize) % 16 != 0 || (ldb * esize) % 16 != 0)
+    return GEMM_ERR_ALIGNMENT;
+  return GEMM_OK;
+}
+
+int64_t timeout_ns_for(int64_t K) {
+  // The longest legitimate wait is about one tile's main loop; allow 64 ns per
+  // k on top of the fixed limit (eight times a pessimistic per-SM rate).
+  return watchdog_ms() * 1000000ll + K * 64ll;
+}
+
+}  // namespace
+
+bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
+                   uint64_t rows, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_rows,
+                   CUtensorMapSwizzle swizzle) {
+  if (g_encode == nullptr) return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {pitch_bytes};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace gb300
+
+using namespace gb300;
+
+extern "C" {
+
+int gemm_bf16_variant(int variant, const void* A, const void* B, void* D, int64_t M, int64_t N,
+                      int64_t K, int64_t lda, int64_t ldb, int64_t ldd, cudaStream_t stream) {
+  const int base = variant & 0xFF;
+  const bool direct = (variant & GEMM_VARIANT_DIRECT_STORE) != 0;
+  if ((variant & ~(0xFF | GEMM_VARIANT_DIRECT_STORE)) != 0 || base > GEMM_VARIANT_SYNC)
+    return GEMM_ERR_INVALID_ARG;
+  int rc = check_shape(A, B, D, M, N, K, lda, ldb, ldd, 2);
+  if (rc != GEMM_OK || M == 0 || N == 0) return rc;
+  LaunchCtx ctx;
+  if ((rc = current_device(&ctx)) != GEMM_OK) return rc;
+  if (!is_device_pointer(D, ctx.device)) return GEMM_ERR_INVALID_ARG;
+  Problem p = {};
+  p.M = static_cast<uint32_t>(M);
+  p.N = static_cast<uint32_t>(N);
+  p.K = static_cast<uint32_t>(K);
+  p.lda = static_cast<uint64_t>(lda);
+  p.ldb = static_cast<uint64_t>(ldb);
+  p.ldd = static_cast<uint64_t>(ldd);
+  p.A = A;
+  p.B = B;
+  p.D = D;
+  if (K == 0) return launch_zero_fill(p, stream);
+  if (!is_device_pointer(A, ctx.device) || !is_device_pointer(B, ctx.device))
+    return GEMM_ERR_INVALID_ARG;
+  ctx.timeout_ns = static_cast<unsigned long long>(timeout_ns_for(K));
+  const bool tma_store = !direct && aligned16(D) && (ldd * 2) % 16 == 0;
+  switch (base) {
+    case GEMM_VARIANT_SYNC:
+      return launch_bf16_sync(p, ctx, stream);
+    case GEMM_VARIANT_2CTA:
+      return launch_bf16_ws(2, tma_store, p, ctx, stream);
+    case GEMM_VARIANT_1CTA:
+    case GEMM_VARIANT_AUTO:
+    default:
+      return launch_bf16_ws(1, tma_store, p, ctx, stream);
+  }
+}
+
+int gemm_bf16(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+              int64_t lda, int64_t ldb, int64_t ldd, cudaStream_t stream) {
+  return gemm_bf16_variant(GEMM_VARIANT_AUTO, A, B, D, M, N, K, lda, ldb, ldd, stream);
+}
+
+int gemm_mxfp8_variant(int variant, const void* A, const void* B, const void* SFA,
+                       const void* SFB, void* D, int64_t M, int64_t N, int64_t K, int64_t lda,
+                       int64_t ldb, int64_t ldsfa, int64_t ldsfb, int64_t ldd,
+                       cudaStream_t stream) {
+  const int base = variant & 0xFF;
+  const bool direct = (variant & GEMM_VARIANT_DIRECT_STORE) != 0;
+  if ((variant & ~(0xFF | GEMM_VARIANT_DIRECT_STORE)) != 0 ||
+      (base != GEMM_VARIANT_AUTO && base != GEMM_VARIANT_1CTA))
+    return GEMM_ERR_INVALID_ARG;
+  int rc = check_shape(A, B, D, M, N, K, lda, ldb, ldd, 1);
+  if (rc != GEMM_OK || M == 0 || N == 0) return rc;
+  if (K > 0) {
+    const int64_t nblk = (K + 31) / 32;
+    if (SFA == nullptr || SFB == nullptr || ldsfa < nblk || ldsfb < nblk ||
+        ldsfa > (int64_t(1) << 36) || ldsfb > (int64_t(1) << 36))
+      return GEMM_ERR_INVALID_ARG;
+    if (!aligned16(SFA) || !aligned16(SFB) || ldsfa % 16 != 0 || ldsfb % 16 != 0)
+      return GEMM_ERR_ALIGNMENT;
+  }
+  LaunchCtx ctx;
+  if ((rc = current_device(&ctx)) != GEMM_OK) return rc;
+  if (!is_device_pointer(D, ctx.device)) return GEMM_ERR_INVALID_ARG;
+  Problem p = {};
+  p.M = static_cast<uint32_t>(M);
+  p.N = static_cast<uint32_t>(N);
+  p.K = static_cast<uint32_t>(K);
+  p.lda = static_cast<uint64_t>(lda);
+  p.ldb = static_cast<uint64_t>(ldb);
+  p.ldd = static_cast<uint64_t>(ldd);
+  p.ldsfa = static_cast<uint64_t>(ldsfa);
+  p.ldsfb = static_cast<uint64_t>(ldsfb);
+  p.A = A;
+  p.B = B;
+  p.SFA = SFA;
+  p.SFB = SFB;
+  p.D = D;
+  if (K == 0) return launch_zero_fill(p, stream);
+  if (!is_device_pointer(A, ctx.device) || !is_device_pointer(B, ctx.device) ||
+      !is_device_pointer(SFA, ctx.device) || !is_device_pointer(SFB, ctx.device))
+    return GEMM_ERR_INVALID_ARG;
+  ctx.timeout_ns = static_cast<unsigned long long>(timeout_ns_for(K));
+  const bool tma_store = !direct && aligned16(D) && (ldd * 2) % 16 == 0;
+  return launch_mxf8_ws(tma_store, p, ctx, stream);
+}
+
+int gemm_mxfp8(const void* A, const void* B, const void* SFA, const void* SFB, void* D,
+               int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldsfa,
+               int64_t ldsfb, int64_t ldd, cudaStream_t stream) {
+  return gemm_mxfp8_variant(GEMM_VARIANT_AUTO, A, B, SFA, SFB, D, M, N, K, lda, ldb, ldsfa, ldsfb,
+                            ldd, stream);
+}
+
+uint64_t gemm_last_status_word(cudaStream_t stream) {
+  LaunchCtx ctx;
+  if (current_device(&ctx) != GEMM_OK) return 0;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  unsigned long long w = 0;
+  if (cudaMemcpyFromSymbol(&w, g_status_word, sizeof w) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return w;
+}
+
+int gemm_last_status(cudaStream_t stream) {
+  LaunchCtx ctx;
+  int rc = current_device(&ctx);
+  if (rc != GEMM_OK) return rc;
+  const cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_DEVICE_FAULT;
+  }
+  unsigned long long w = 0;
+  if (cudaMemcpyFromSymbol(&w, g_status_word, sizeof w) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_DEVICE_FAULT;
+  }
+  if (w == 0) return GEMM_OK;
+  const unsigned long long zero = 0;
+  if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_DEVICE_FAULT;
+  }
+  return (w >> 56) == kDevTimeout ? GEMM_ERR_TIMEOUT : GEMM_ERR_DEVICE_FAULT;
+}
+
+const char* gemm_status_string(int status) {
+  switch (status) {
+    case GEMM_OK: return "ok";
+    case GEMM_ERR_INVALID_ARG: return "invalid argument";
+    case GEMM_ERR_ALIGNMENT: return "operand alignment or pitch not supported by TMA";
+    case GEMM_ERR_UNSUPPORTED_DEVICE: return "device is not sm_103 (GB300)";
+    case GEMM_ERR_LAUNCH: return "kernel launch or tensor-map encoding failed";
+    case GEMM_ERR_TIMEOUT: return "device watchdog: a barrier wait timed out";
+    case GEMM_ERR_DEVICE_FAULT: return "device fault reported by the stream";
+    default: return "unknown status";
+  }
+}
+
+int64_t gemm_set_watchdog_ms(int64_t ms) {
+  const int64_t old = watchdog_ms();
+  if (ms > 0) g_watchdog_ms.store(ms);
+  return old;
+}
+
+int gemm_kernel_plan(int mxfp8, int variant, int32_t* stages, int32_t* smem_bytes,
+                     int32_t* tmem_cols, int32_t* threads, int32_t* cluster, int32_t* tile_m,
+                     int32_t* tile_n) {
+  const int base = variant & 0xFF;
+  const bool tma_store = (variant & GEMM_VARIANT_DIRECT_STORE) == 0;
+  KernelPlan k;
+  bool ok;
+  if (mxfp8)
+    ok = (base == GEMM_VARIANT_AUTO || base == GEMM_VARIANT_1CTA) && plan_mxf8(tma_store, &k);
+  else
+    ok = plan_bf16(base == GEMM_VARIANT_AUTO ? 1 : base, tma_store, &k);
+  if (!ok) return GEMM_ERR_INVALID_ARG;
+  if (stages) *stages = k.stages;
+  if (smem_bytes) *smem_bytes = k.smem_bytes;
+  if (tmem_cols) *tmem_cols = k.tmem_cols;
+  if (threads) *threads = k.threads;
+  if (cluster) *cluster = k.cluster;
+  if (tile_m) *tile_m = k.tile_m;
+  if (tile_n) *tile_n = k.tile_n;
+  return GEMM_OK;
+}
+
+}  // extern "C"

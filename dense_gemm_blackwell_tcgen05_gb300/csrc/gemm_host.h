@@ -1,0 +1,57 @@
+// Host-side plumbing shared by the translation units of the library (not
+// part of the public ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace gb300 {
+
+struct Problem {
+  uint32_t M, N, K;
+  uint64_t lda, ldb, ldd, ldsfa, ldsfb;
+  const void* A;
+  const void* B;
+  const void* SFA;
+  const void* SFB;
+  void* D;
+};
+
+struct LaunchCtx {
+  int device;
+  int num_sms;
+  unsigned long long* status;      // device address of the status word
+  unsigned long long timeout_ns;
+};
+
+struct Maps {
+  CUtensorMap A;
+  CUtensorMap B;
+  CUtensorMap D;
+  CUtensorMap SFA;
+  CUtensorMap SFB;
+};
+
+// Encodes a 2-D tiled tensor map (rows of `inner` elements, pitch in bytes).
+// Returns false when the driver rejects it.
+bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
+                   uint64_t rows, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_rows,
+                   CUtensorMapSwizzle swizzle);
+
+// Kernel launchers; each returns a gemm_status_t value.
+int launch_bf16_ws(int cg, bool tma_store, const Problem& p, const LaunchCtx& ctx,
+                   cudaStream_t stream);
+int launch_bf16_sync(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream);
+int launch_mxf8_ws(bool tma_store, const Problem& p, const LaunchCtx& ctx, cudaStream_t stream);
+int launch_zero_fill(const Problem& p, cudaStream_t stream);
+
+// Compile-time plans for gemm_kernel_plan().
+struct KernelPlan {
+  int stages, smem_bytes, tmem_cols, threads, cluster, tile_m, tile_n;
+};
+bool plan_bf16(int cg, bool tma_store, KernelPlan* out);
+bool plan_mxf8(bool tma_store, KernelPlan* out);
+
+}  // namespace gb300

@@ -1,0 +1,454 @@
+// The tcgen05 GEMM kernels: D[M,N] = A[M,K] * B[N,K]^T, fp32 accumulation in
+// TMEM, bf16 output.
+//
+//  * gemm_ws_kernel   -- persistent, warp-specialised kernel (TMA producer
+//                        warp, single-thread MMA issuer, four epilogue warps),
+//                        one CTA (cta_group::1, 128x256 tiles) or a CTA pair
+//                        (cta_group::2, 256x256 cluster tiles); bf16 operands
+//                        or block-scaled MXFP8 operands.
+//  * gemm_sync_kernel -- (gemm_sync.cuh) one 128x128 tile per CTA with synchronous thread
+//                        copies into shared memory and one MMA batch per
+//                        K-tile: the first rungs of the optimisation ladder,
+//                        kept as a bisection reference.
+//  * zero_fill_kernel -- (gemm_sync.cuh) D = 0 for an empty reduction (K = 0).
+//
+// Method: b200-gemm-optimization-ladder ("A1 -- The nine-level route",
+// levels 1-8), b200-tma-pipeline-designer ("E -- Executable steps": tensor-map
+// descriptor, single issuer, ready/free barriers, store drain, three-phase
+// timeline) and b200-tmem-lifecycle-planner ("E -- Executable steps": column
+// budget, TLane/TCol map, write/read paths and the lifecycle).
+#pragma once
+
+#include <cstdint>
+
+#include "kernel_common.cuh"
+
+namespace gb300 {
+
+enum class Kind { BF16, MXF8 };
+
+struct GemmArgs {
+  uint32_t M, N, K;
+  uint32_t num_m_blocks;      // tiles along M (UMMA_M rows each)
+  uint32_t num_n_blocks;      // tiles along N (UMMA_N columns each)
+  uint32_t num_k_tiles;       // ceil(K / BK)
+  uint32_t group_m;           // raster group (M-blocks swept together)
+  void* D;                    // D base (direct-store epilogue)
+  uint64_t ldd;               // D row pitch in elements
+  unsigned long long* status; // device status word
+  unsigned long long timeout_ns;
+};
+
+__host__ __device__ constexpr uint32_t align_up_u32(uint32_t x, uint32_t a) {
+  return (x + a - 1) / a * a;
+}
+
+// Compile-time plan of one kernel configuration: tile shape, stage ring,
+// TMEM column budget and shared-memory map.
+template <int CG, Kind KIND, bool TMA_STORE>
+struct GemmCfg {
+  static_assert(CG == 1 || CG == 2, "cta_group is 1 or 2");
+  static constexpr bool MX = KIND == Kind::MXF8;
+  static_assert(!(MX && CG == 2), "MXFP8 runs on the single-CTA kernel");
+
+  static constexpr uint32_t kThreads = 192;   // w0 TMA, w1 MMA/TMEM, w2..5 epilogue
+  static constexpr uint32_t BLOCK_M = 128;    // D rows owned by one CTA (= TMEM lanes)
+  static constexpr uint32_t UMMA_M = 128 * CG;
+  static constexpr uint32_t UMMA_N = 256;     // D columns per tile (= TMEM columns)
+  static constexpr uint32_t B_ROWS = UMMA_N / CG;  // B rows staged by one CTA
+  static constexpr uint32_t ELEM = MX ? 1 : 2;
+  static constexpr uint32_t BK = 128 / ELEM;  // K elements per stage: one 128-byte row
+  static constexpr uint32_t UMMA_K = 32 / ELEM;
+  static constexpr uint32_t K_STEPS = BK / UMMA_K;
+  static constexpr uint32_t A_BYTES = BLOCK_M * 128;
+  static constexpr uint32_t B_BYTES = B_ROWS * 128;
+  // MXFP8 scale factors: a TMA box of 16 bytes (4 K-tiles' scales) per row,
+  // then the MMA warp re-tiles one K-tile's bytes into the 32x16-byte chunk
+  // that tcgen05.cp copies into TMEM.
+  static constexpr uint32_t SFB_ROWS = MX ? UMMA_N : 0;
+  static constexpr uint32_t SFA_RAW = MX ? BLOCK_M * 16 : 0;
+  static constexpr uint32_t SFB_RAW = SFB_ROWS * 16;
+  static constexpr uint32_t SFA_T = MX ? BLOCK_M * 4 : 0;
+  static constexpr uint32_t SFB_T = SFB_ROWS * 4;
+  static constexpr uint32_t OFF_B = A_BYTES;
+  static constexpr uint32_t OFF_SFA_RAW = OFF_B + B_BYTES;
+  static constexpr uint32_t OFF_SFB_RAW = OFF_SFA_RAW + SFA_RAW;
+  static constexpr uint32_t OFF_SFA_T = OFF_SFB_RAW + SFB_RAW;
+  static constexpr uint32_t OFF_SFB_T = OFF_SFA_T + SFA_T;
+  static constexpr uint32_t STAGE_BYTES = align_up_u32(OFF_SFB_T + SFB_T, 1024);
+  static constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES + SFA_RAW + SFB_RAW;  // per CTA
+
+  // TMEM: ACC_STAGES accumulators of UMMA_N fp32 columns, then the scale
+  // factors (MXFP8: 4 columns for A, 8 for B).  512 = whole TMEM.
+  static constexpr uint32_t ACC_STAGES = MX ? 1 : 2;
+  static constexpr uint32_t SF_TMEM_COL = ACC_STAGES * UMMA_N;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static_assert(SF_TMEM_COL + (MX ? 12 : 0) <= TMEM_COLS, "TMEM column budget");
+
+  // Epilogue staging for TMA stores: per epilogue warp, two 32x64 bf16
+  // buffers (32 rows of 128 bytes, 128-byte swizzled).
+  static constexpr uint32_t EPI_BUF_BYTES = 32 * 128;
+  static constexpr uint32_t EPI_BUFS = 2;
+  static constexpr uint32_t EPI_BYTES = TMA_STORE ? 4 * EPI_BUFS * EPI_BUF_BYTES : 0;
+
+  static constexpr uint32_t SMEM_LIMIT = 232448;  // 227 KB opt-in per CTA
+  static constexpr uint32_t BAR_BYTES = 256;
+  static constexpr uint32_t ALIGN_SLACK = 1024;
+  static constexpr uint32_t STAGES_FIT =
+      (SMEM_LIMIT - ALIGN_SLACK - BAR_BYTES - EPI_BYTES) / STAGE_BYTES;
+  static constexpr uint32_t STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static_assert(STAGES >= 2, "stage ring needs two slots");
+  static constexpr uint32_t SMEM_BYTES = ALIGN_SLACK + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
+  static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
+  static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
+};
+
+template <int CG>
+__device__ __forceinline__ void commit_to(uint32_t bar) {
+  if constexpr (CG == 1)
+    tc_commit(bar);
+  else
+    tc_commit_pair_multicast(bar, 0x3);  // the same barrier in both CTAs of the pair
+}
+
+// Bounded wait by lane 0, result broadcast to the warp; on success the other
+// lanes also observe the completed phase (acquire) before touching its data.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Watchdog& wd,
+                                          uint32_t site, uint32_t lane) {
+  bool ok = true;
+  if (lane == 0) ok = wait_bounded(bar, parity, wd, site);
+  ok = __shfl_sync(0xffffffffu, ok ? 1u : 0u, 0) != 0;
+  if (ok && lane != 0) ok = wait_bounded(bar, parity, wd, site);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Exit-path wait that ignores the abort flag (used to let this CTA's own
+// asynchronous operations finish before shared memory / TMEM are released).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const Watchdog& wd,
+                                           uint32_t site) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t n = 0;; ++n) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((n & 31u) == 31u && global_timer_ns() - t0 > wd.timeout_ns) {
+      report_error(wd.status, kDevTimeout, site);
+      return;
+    }
+  }
+}
+
+// Direct epilogue store of one thread's 32 consecutive outputs of row `row`
+// starting at column `col0`, masked against M/N; any pitch and alignment.
+__device__ __forceinline__ void store_row32(uint16_t* D, uint64_t ldd, uint32_t M, uint32_t N,
+                                            uint32_t row, uint32_t col0, const uint32_t (&v)[32]) {
+  if (row >= M || col0 >= N) return;
+  uint32_t p[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) p[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+  uint16_t* dst = D + static_cast<uint64_t>(row) * ldd + col0;
+  const uint32_t n = min(32u, N - col0);
+  const uintptr_t a = reinterpret_cast<uintptr_t>(dst);
+  if (n == 32 && (a & 15) == 0) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d4[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+  } else if ((a & 3) == 0) {
+    uint32_t* d2 = reinterpret_cast<uint32_t*>(dst);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (2 * i + 1 < n) d2[i] = p[i];
+      else if (2 * i < n) dst[2 * i] = static_cast<uint16_t>(p[i] & 0xFFFFu);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (2 * i < n) dst[2 * i] = static_cast<uint16_t>(p[i] & 0xFFFFu);
+      if (2 * i + 1 < n) dst[2 * i + 1] = static_cast<uint16_t>(p[i] >> 16);
+    }
+  }
+}
+
+template <int CG, Kind KIND, bool TMA_STORE>
+__global__ void __launch_bounds__(192, 1)
+    gemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmD,
+                   const __grid_constant__ CUtensorMap tmSFA,
+                   const __grid_constant__ CUtensorMap tmSFB, const GemmArgs args) {
+  using C = GemmCfg<CG, KIND, TMA_STORE>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const base_ptr = smem_raw + (base - raw);
+  const uint32_t stage0 = base;
+  const uint32_t epi0 = base + C::STAGES * C::STAGE_BYTES;
+  const uint32_t bar0 = epi0 + C::EPI_BYTES;
+  const auto full_bar = [&](uint32_t s) { return bar0 + 8 * s; };
+  const auto empty_bar = [&](uint32_t s) { return bar0 + 8 * (C::STAGES + s); };
+  const auto accf_bar = [&](uint32_t b) { return bar0 + 8 * (2 * C::STAGES + b); };
+  const auto acce_bar = [&](uint32_t b) { return bar0 + 8 * (2 * C::STAGES + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8 * (2 * C::STAGES + 4);
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + (bar0 - base) + 8 * (2 * C::STAGES + 5));
+  volatile uint32_t* const abort_flag = tmem_slot + 1;
+
+  const uint32_t warp = warp_idx_sync();
+  const uint32_t lane = lane_idx();
+  const uint32_t rank = (CG == 2) ? cluster_cta_rank() : 0u;
+  const bool leader = rank == 0;
+  const uint32_t cluster_id = blockIdx.x / CG;
+  const uint32_t num_clusters = gridDim.x / CG;
+  const Watchdog wd{args.status, args.timeout_ns, abort_flag};
+
+  // ---- set-up: barriers (one thread), TMEM allocation (one warp) ----------
+  if (warp == 0 && lane == 0) {
+    for (uint32_t s = 0; s < C::STAGES; ++s) {
+      mbar_init(full_bar(s), 1);    // producer's expect_tx arrival (+ TMA bytes)
+      mbar_init(empty_bar(s), 1);   // MMA issuer's commit
+    }
+    for (uint32_t b = 0; b < 2; ++b) {
+      mbar_init(accf_bar(b), 1);        // MMA issuer's commit after the last K-tile
+      mbar_init(acce_bar(b), 4 * CG);   // every epilogue warp of the pair
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    if constexpr (TMA_STORE) tma_prefetch_desc(&tmD);
+    if constexpr (C::MX) {
+      tma_prefetch_desc(&tmSFA);
+      tma_prefetch_desc(&tmSFB);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc<CG>(smem_addr(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish<CG>();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if constexpr (CG == 2) cluster_sync();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  const uint32_t num_tiles = args.num_m_blocks * args.num_n_blocks;
+  const uint32_t KT = args.num_k_tiles;
+
+  if (warp == 0) {
+    // ==================== TMA producer: one elected thread ====================
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_last();
+      uint32_t it = 0;
+      bool ok = true;
+      for (uint32_t t = cluster_id; t < num_tiles && ok; t += num_clusters) {
+        uint32_t mb, nb;
+        tile_coords(t, args.num_m_blocks, args.num_n_blocks, args.group_m, mb, nb);
+        const int32_t a_row = static_cast<int32_t>(mb * C::UMMA_M + rank * C::BLOCK_M);
+        const int32_t b_row = static_cast<int32_t>(nb * C::UMMA_N + rank * C::B_ROWS);
+        for (uint32_t kt = 0; kt < KT; ++kt, ++it) {
+          const uint32_t s = it % C::STAGES;
+          const uint32_t round = it / C::STAGES;
+          // free barrier: the MMA that last read this slot has completed
+          if (!wait_bounded(empty_bar(s), (round & 1u) ^ 1u, wd, kSiteProducerEmpty)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sb = stage0 + s * C::STAGE_BYTES;
+          const int32_t kx = static_cast<int32_t>(kt * C::BK);
+          if constexpr (CG == 1) {
+            mbar_arrive_expect_tx(full_bar(s), C::TX_BYTES);
+            tma_load_2d(sb, &tmA, full_bar(s), kx, a_row, pol);
+            tma_load_2d(sb + C::OFF_B, &tmB, full_bar(s), kx, b_row, pol);
+            if constexpr (C::MX) {
+              const int32_t sx = static_cast<int32_t>((kt / 4) * 16);
+              tma_load_2d(sb + C::OFF_SFA_RAW, &tmSFA, full_bar(s), sx, a_row, pol);
+              tma_load_2d(sb + C::OFF_SFB_RAW, &tmSFB, full_bar(s), sx, b_row, pol);
+            }
+          } else {
+            // both CTAs' bytes land on the leader's ready barrier
+            const uint32_t leader_full = mapa_shared(full_bar(s), 0);
+            if (leader) mbar_arrive_expect_tx(full_bar(s), CG * C::TX_BYTES);
+            tma_load_2d_pair(sb, &tmA, leader_full, kx, a_row, pol);
+            tma_load_2d_pair(sb + C::OFF_B, &tmB, leader_full, kx, b_row, pol);
+          }
+        }
+      }
+      // Exit path after a give-up: let this CTA's issued loads land first.
+      if (*abort_flag && leader) {
+        const uint32_t first = it > C::STAGES ? it - C::STAGES : 0u;
+        for (uint32_t i = first; i < it; ++i)
+          drain_wait(full_bar(i % C::STAGES), (i / C::STAGES) & 1u, wd, kSiteProducerDrain);
+      }
+    }
+  } else if (warp == 1) {
+    // ==================== MMA issuer (leader CTA of the pair) ===================
+    if (leader) {
+      uint32_t it = 0, j = 0;
+      bool issued = false;
+      for (uint32_t t = cluster_id; t < num_tiles; t += num_clusters, ++j) {
+        const uint32_t b = j % C::ACC_STAGES;
+        const uint32_t around = j / C::ACC_STAGES;
+        // accumulator b must have been drained by every epilogue warp
+        if (!warp_wait(acce_bar(b), (around & 1u) ^ 1u, wd, kSiteMmaAccEmpty, lane)) break;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + b * C::UMMA_N;
+        bool ok = true;
+        for (uint32_t kt = 0; kt < KT; ++kt, ++it) {
+          const uint32_t s = it % C::STAGES;
+          const uint32_t round = it / C::STAGES;
+          if (!warp_wait(full_bar(s), round & 1u, wd, kSiteMmaFull, lane)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sb = stage0 + s * C::STAGE_BYTES;
+          if constexpr (C::MX) {
+            // Re-tile this K-tile's scale bytes: row r's 4-byte word (one
+            // UE8M0 per 32 k) moves to byte 16*(r%32) + 4*(r/32) of its
+            // 128-row chunk, the layout tcgen05.cp ... 32x128b.warpx4 expects.
+            const uint32_t w = kt & 3u;
+            const uint32_t* rawA = reinterpret_cast<const uint32_t*>(base_ptr + (sb - base) + C::OFF_SFA_RAW);
+            const uint32_t* rawB = reinterpret_cast<const uint32_t*>(base_ptr + (sb - base) + C::OFF_SFB_RAW);
+            uint4* tA = reinterpret_cast<uint4*>(base_ptr + (sb - base) + C::OFF_SFA_T);
+            uint4* tB = reinterpret_cast<uint4*>(base_ptr + (sb - base) + C::OFF_SFB_T);
+            tA[lane] = make_uint4(rawA[(lane + 0) * 4 + w], rawA[(lane + 32) * 4 + w],
+                                  rawA[(lane + 64) * 4 + w], rawA[(lane + 96) * 4 + w]);
+#pragma unroll
+            for (uint32_t h = 0; h < C::SFB_ROWS / 128; ++h) {
+              const uint32_t r = h * 128 + lane;
+              tB[h * 32 + lane] = make_uint4(rawB[(r + 0) * 4 + w], rawB[(r + 32) * 4 + w],
+                                             rawB[(r + 64) * 4 + w], rawB[(r + 96) * 4 + w]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+          if (lane == 0) {
+            tc_fence_after_sync();
+            const uint64_t adesc = smem_desc_sw128(sb);
+            const uint64_t bdesc = smem_desc_sw128(sb + C::OFF_B);
+            if constexpr (C::MX) {
+              const uint32_t sfa_t = tmem_base + C::SF_TMEM_COL;
+              const uint32_t sfb_t = sfa_t + 4;
+              tmem_cp_32x128b_warpx4<CG>(sfa_t, smem_desc_rows16(sb + C::OFF_SFA_T));
+#pragma unroll
+              for (uint32_t h = 0; h < C::SFB_ROWS / 128; ++h)
+                tmem_cp_32x128b_warpx4<CG>(sfb_t + 4 * h, smem_desc_rows16(sb + C::OFF_SFB_T + 512 * h));
+#pragma unroll
+              for (uint32_t k = 0; k < C::K_STEPS; ++k)
+                mma_mxf8<CG>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc_mxf8(C::UMMA_M, C::UMMA_N, k, k),
+                             sfa_t, sfb_t, (kt | k) != 0u);
+            } else {
+              constexpr uint32_t idesc = idesc_bf16(C::UMMA_M, C::UMMA_N);
+#pragma unroll
+              for (uint32_t k = 0; k < C::K_STEPS; ++k)
+                mma_bf16<CG>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kt | k) != 0u);
+            }
+            commit_to<CG>(empty_bar(s));   // frees the slot once these MMAs finish
+          }
+          issued = true;
+          __syncwarp();
+        }
+        if (!ok) break;
+        if (lane == 0) commit_to<CG>(accf_bar(b));   // accumulator b complete
+        __syncwarp();
+      }
+      // Exit path: every tcgen05 op this thread issued completes before TMEM
+      // is released.
+      if (lane == 0 && issued) {
+        if constexpr (CG == 1)
+          tc_commit(drain_bar);
+        else
+          tc_commit_pair_multicast(drain_bar, 0x1);
+        drain_wait(drain_bar, 0, wd, kSiteMmaDrain);
+      }
+      __syncwarp();
+    }
+  } else {
+    // ==================== epilogue: four warps, one TMEM lane quarter each =========
+    const uint32_t q = warp & 3u;            // TMEM lanes 32q .. 32q+31
+    const uint32_t ew = warp - 2u;           // staging slot owner
+    uint32_t j = 0, chunk_ctr = 0;
+    for (uint32_t t = cluster_id; t < num_tiles; t += num_clusters, ++j) {
+      const uint32_t b = j % C::ACC_STAGES;
+      const uint32_t around = j / C::ACC_STAGES;
+      if (!warp_wait(accf_bar(b), around & 1u, wd, kSiteEpiAccFull, lane)) break;
+      tc_fence_after_sync();
+      uint32_t mb, nb;
+      tile_coords(t, args.num_m_blocks, args.num_n_blocks, args.group_m, mb, nb);
+      const uint32_t row0 = mb * C::UMMA_M + rank * C::BLOCK_M + q * 32;
+      const uint32_t col_base = nb * C::UMMA_N;
+      const uint32_t t_addr = tmem_base + ((q * 32u) << 16) + b * C::UMMA_N;
+      if (row0 < args.M) {
+        if constexpr (TMA_STORE) {
+#pragma unroll 1
+          for (uint32_t c = 0; c < C::UMMA_N / 64; ++c) {
+            if (col_base + c * 64 >= args.N) break;
+            uint32_t v0[32], v1[32];
+            tmem_ld_32x32b_x32(t_addr + c * 64, v0);
+            tmem_ld_32x32b_x32(t_addr + c * 64 + 32, v1);
+            tmem_wait_ld();
+            const uint32_t buf = epi0 + (ew * C::EPI_BUFS + (chunk_ctr % C::EPI_BUFS)) * C::EPI_BUF_BYTES;
+            if (lane == 0) bulk_wait_group_read<C::EPI_BUFS - 1>();   // this buffer's last store has read it
+            __syncwarp();
+            uint8_t* rowp = base_ptr + (buf - base) + lane * 128;
+#pragma unroll
+            for (uint32_t i = 0; i < 8; ++i) {
+              uint4 val;
+              if (i < 4) {
+                val = make_uint4(pack_bf16x2(__uint_as_float(v0[8 * i + 0]), __uint_as_float(v0[8 * i + 1])),
+                                 pack_bf16x2(__uint_as_float(v0[8 * i + 2]), __uint_as_float(v0[8 * i + 3])),
+                                 pack_bf16x2(__uint_as_float(v0[8 * i + 4]), __uint_as_float(v0[8 * i + 5])),
+                                 pack_bf16x2(__uint_as_float(v0[8 * i + 6]), __uint_as_float(v0[8 * i + 7])));
+              } else {
+                const uint32_t o = 8 * (i - 4);
+                val = make_uint4(pack_bf16x2(__uint_as_float(v1[o + 0]), __uint_as_float(v1[o + 1])),
+                                 pack_bf16x2(__uint_as_float(v1[o + 2]), __uint_as_float(v1[o + 3])),
+                                 pack_bf16x2(__uint_as_float(v1[o + 4]), __uint_as_float(v1[o + 5])),
+                                 pack_bf16x2(__uint_as_float(v1[o + 6]), __uint_as_float(v1[o + 7])));
+              }
+              // 128-byte swizzle: 16-byte chunk i of row r sits at chunk i ^ (r % 8)
+              *reinterpret_cast<uint4*>(rowp + ((i ^ (lane & 7u)) << 4)) = val;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmD, buf, static_cast<int32_t>(col_base + c * 64), static_cast<int32_t>(row0));
+              bulk_commit_group();
+            }
+            ++chunk_ctr;
+          }
+        } else {
+#pragma unroll 1
+          for (uint32_t c = 0; c < C::UMMA_N / 32; ++c) {
+            if (col_base + c * 32 >= args.N) break;
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(t_addr + c * 32, v);
+            tmem_wait_ld();
+            store_row32(static_cast<uint16_t*>(args.D), args.ldd, args.M, args.N, row0 + lane,
+                        col_base + c * 32, v);
+          }
+        }
+      }
+      // all TMEM reads of accumulator b by this warp are complete
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (CG == 1)
+          mbar_arrive(acce_bar(b));
+        else
+          mbar_arrive_cluster(mapa_shared(acce_bar(b), 0));
+      }
+    }
+    if constexpr (TMA_STORE) {
+      if (lane == 0) bulk_wait_group<0>();
+      __syncwarp();
+    }
+  }
+
+  // ---- teardown: every role is done with TMEM and with the peer's barriers ----
+  tc_fence_before_sync();
+  __syncthreads();
+  if constexpr (CG == 2) cluster_sync();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc<CG>(tmem_base, C::TMEM_COLS);
+  }
+}
+
+}  // namespace gb300

@@ -1,0 +1,139 @@
+// Host-side launcher of gemm_ws_kernel: encodes the tensor maps, sizes the
+// persistent grid from the SM count (or the number of co-resident clusters)
+// and launches with the cluster dimension of the configuration.
+#pragma once
+
+#include <atomic>
+#include <cstring>
+#include <mutex>
+
+#include "gemm_gb300.h"
+#include "gemm_host.h"
+#include "gemm_kernels.cuh"
+
+namespace gb300 {
+
+template <int CG, Kind KIND, bool TMA_STORE>
+int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) {
+  using C = GemmCfg<CG, KIND, TMA_STORE>;
+  auto kern = gemm_ws_kernel<CG, KIND, TMA_STORE>;
+
+  // Per-device, one-time: opt into the large shared-memory carve-out and
+  // (pairs) find how many clusters can be resident at once.
+  static std::mutex mu;
+  static int prepared[128] = {0};
+  static int max_clusters[128] = {0};
+  if (ctx.device < 0 || ctx.device >= 128) return GEMM_ERR_UNSUPPORTED_DEVICE;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (!prepared[ctx.device]) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(C::SMEM_BYTES)) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+      }
+      if constexpr (CG == 2) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) !=
+            cudaSuccess)
+          cudaGetLastError();
+        cudaLaunchConfig_t q = {};
+        q.gridDim = dim3(2 * ctx.num_sms);
+        q.blockDim = dim3(C::kThreads);
+        q.dynamicSmemBytes = C::SMEM_BYTES;
+        cudaLaunchAttribute qa[1];
+        qa[0].id = cudaLaunchAttributeClusterDimension;
+        qa[0].val.clusterDim.x = CG;
+        qa[0].val.clusterDim.y = 1;
+        qa[0].val.clusterDim.z = 1;
+        q.attrs = qa;
+        q.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess || n <= 0) {
+          cudaGetLastError();
+          n = ctx.num_sms / 2;
+        }
+        max_clusters[ctx.device] = n;
+      }
+      prepared[ctx.device] = 1;
+    }
+  }
+
+  Maps maps;
+  std::memset(&maps, 0, sizeof maps);
+  const CUtensorMapDataType dt =
+      C::MX ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!encode_map_2d(&maps.A, dt, p.A, p.K, p.M, p.lda * C::ELEM, C::BK, C::BLOCK_M,
+                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_map_2d(&maps.B, dt, p.B, p.K, p.N, p.ldb * C::ELEM, C::BK, C::B_ROWS,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+    return GEMM_ERR_LAUNCH;
+  if constexpr (TMA_STORE) {
+    if (!encode_map_2d(&maps.D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.D, p.N, p.M, p.ldd * 2, 64, 32,
+                       CU_TENSOR_MAP_SWIZZLE_128B))
+      return GEMM_ERR_LAUNCH;
+  }
+  if constexpr (C::MX) {
+    const uint64_t nblk = (p.K + 31) / 32;
+    if (!encode_map_2d(&maps.SFA, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.SFA, nblk, p.M, p.ldsfa, 16,
+                       C::BLOCK_M, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_map_2d(&maps.SFB, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.SFB, nblk, p.N, p.ldsfb, 16,
+                       C::SFB_ROWS, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return GEMM_ERR_LAUNCH;
+  }
+
+  GemmArgs a;
+  a.M = p.M;
+  a.N = p.N;
+  a.K = p.K;
+  a.num_m_blocks = (p.M + C::UMMA_M - 1) / C::UMMA_M;
+  a.num_n_blocks = (p.N + C::UMMA_N - 1) / C::UMMA_N;
+  a.num_k_tiles = (p.K + C::BK - 1) / C::BK;
+  a.group_m = CG == 2 ? 8u : 16u;
+  a.D = p.D;
+  a.ldd = p.ldd;
+  a.status = ctx.status;
+  a.timeout_ns = ctx.timeout_ns;
+
+  const uint64_t tiles = static_cast<uint64_t>(a.num_m_blocks) * a.num_n_blocks;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if constexpr (CG == 2) {
+    const uint64_t clusters = tiles < static_cast<uint64_t>(max_clusters[ctx.device])
+                                  ? tiles
+                                  : static_cast<uint64_t>(max_clusters[ctx.device]);
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  } else {
+    const uint64_t ctas = tiles < static_cast<uint64_t>(ctx.num_sms) ? tiles
+                                                                     : static_cast<uint64_t>(ctx.num_sms);
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+  }
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, kern, maps.A, maps.B, maps.D, maps.SFA, maps.SFB, a);
+  if (err != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_LAUNCH;
+  }
+  return GEMM_OK;
+}
+
+template <int CG, Kind KIND, bool TMA_STORE>
+void fill_plan(KernelPlan* out) {
+  using C = GemmCfg<CG, KIND, TMA_STORE>;
+  out->stages = C::STAGES;
+  out->smem_bytes = C::SMEM_BYTES;
+  out->tmem_cols = C::TMEM_COLS;
+  out->threads = C::kThreads;
+  out->cluster = CG;
+  out->tile_m = C::UMMA_M;
+  out->tile_n = C::UMMA_N;
+}
+
+}  // namespace gb300

@@ -1,0 +1,139 @@
+/*
+ * gemm_gb300.h -- C ABI of the GB300 (sm_103a) tcgen05 dense GEMM library.
+ *
+ *     D[M,N] = A[M,K] * B[N,K]^T      fp32 accumulation, bf16 output
+ *
+ * The operation is the dense GEMM of b200-gemm-optimization-ladder ("E --
+ * Executable steps", step 1: fix the math definition, layout and dtype; "A1 --
+ * The nine-level route": data path GMEM -> SMEM -> tcgen05 -> TMEM ->
+ * registers/SMEM -> GMEM), with the block-scaled variant whose scale factors
+ * are staged SMEM -> TMEM by tcgen05.cp (b200-tmem-lifecycle-planner, "A1 --
+ * Case 2: block-scaled MMA").
+ *
+ * Layout (all matrices row-major, leading dimensions in ELEMENTS):
+ *   A  [M, K] with row pitch lda >= K          (K contiguous)
+ *   B  [N, K] with row pitch ldb >= K          (K contiguous, "K-major")
+ *   D  [M, N] with row pitch ldd >= N          (bf16, round-to-nearest-even)
+ *
+ * Ownership: every pointer is a caller-owned DEVICE pointer (e.g. a torch CUDA
+ * tensor).  The library never allocates or frees device memory; its only
+ * device state is one status word per device, read by gemm_last_status().
+ * A, B, SFA, SFB must not overlap D.
+ *
+ * Ordering: calls are asynchronous on `stream` (0 = the legacy default
+ * stream), like cuBLAS.  Argument errors are returned synchronously; a
+ * device-side watchdog timeout is reported by gemm_last_status().
+ *
+ * Errors: every entry point returns a gemm_status_t:
+ *   GEMM_ERR_INVALID_ARG  M, N or K negative or >= 2^31, a NULL pointer,
+ *                         lda < K, ldb < K, ldd < N, a pointer that is not
+ *                         device memory, an unknown variant
+ *   GEMM_ERR_ALIGNMENT    A or B (or SFA/SFB) not 16-byte aligned, or a row
+ *                         pitch whose byte size is not a multiple of 16
+ *                         (the TMA engine's rule): bf16 needs lda, ldb
+ *                         multiples of 8, E4M3 multiples of 16
+ *   GEMM_ERR_UNSUPPORTED_DEVICE  the current device is not compute
+ *                         capability 10.3 (sm_103); there is no fallback
+ *   GEMM_ERR_LAUNCH       the CUDA launch (or tensor-map encoding) failed
+ * M == 0 or N == 0 is a no-op that returns GEMM_OK.  K == 0 writes D = 0
+ * (the empty sum).  D may have any pitch and alignment: when its rows are not
+ * 16-byte aligned the epilogue uses masked stores instead of TMA stores.
+ */
+#ifndef GEMM_GB300_H
+#define GEMM_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#ifndef __DRIVER_TYPES_H__
+typedef struct CUstream_st* cudaStream_t;
+#endif
+
+typedef enum {
+  GEMM_OK = 0,
+  GEMM_ERR_INVALID_ARG = -1,
+  GEMM_ERR_ALIGNMENT = -2,
+  GEMM_ERR_UNSUPPORTED_DEVICE = -3,
+  GEMM_ERR_LAUNCH = -4,
+  GEMM_ERR_TIMEOUT = -5,
+  GEMM_ERR_DEVICE_FAULT = -6
+} gemm_status_t;
+
+/* Kernel choice for gemm_bf16_variant / gemm_mxfp8_variant. */
+typedef enum {
+  GEMM_VARIANT_AUTO = 0,        /* the fastest path for the arguments              */
+  GEMM_VARIANT_1CTA = 1,        /* persistent warp-specialised, cta_group::1,
+                                   128x256 tiles (ladder levels 4-7)               */
+  GEMM_VARIANT_2CTA = 2,        /* persistent warp-specialised CTA pair,
+                                   cta_group::2, 256x256 tiles (ladder level 8)    */
+  GEMM_VARIANT_SYNC = 3,        /* one 128x128 tile per CTA, synchronous copies
+                                   (ladder levels 1-3; bf16 only, reference rung)  */
+  GEMM_VARIANT_DIRECT_STORE = 0x100  /* flag: masked st.global epilogue instead of
+                                        TMA stores, even when D is aligned         */
+} gemm_variant_t;
+
+/*
+ * bf16 GEMM: D = A * B^T with A, B, D bf16 (IEEE bfloat16 bit patterns).
+ * Runs the persistent tcgen05 kernel chosen for the shape (GEMM_VARIANT_AUTO).
+ */
+int gemm_bf16(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+              int64_t lda, int64_t ldb, int64_t ldd, cudaStream_t stream);
+
+/* bf16 GEMM on an explicitly chosen kernel (a gemm_variant_t value, optionally
+ * OR-ed with GEMM_VARIANT_DIRECT_STORE).  Same arguments and errors. */
+int gemm_bf16_variant(int variant, const void* A, const void* B, void* D, int64_t M, int64_t N,
+                      int64_t K, int64_t lda, int64_t ldb, int64_t ldd, cudaStream_t stream);
+
+/*
+ * Block-scaled MXFP8 GEMM:  D[i,j] = sum_k a(i,k) * b(j,k),
+ *   a(i,k) = 2^(SFA[i*ldsfa + k/32] - 127) * e4m3(A[i*lda + k])
+ *   b(j,k) = 2^(SFB[j*ldsfb + k/32] - 127) * e4m3(B[j*ldb + k])
+ * A [M, K], B [N, K]: E4M3 ("e4m3fn") bytes, lda/ldb multiples of 16.
+ * SFA [M, ldsfa], SFB [N, ldsfb]: UE8M0 scale bytes (2^(e-127), 255 = NaN), one
+ * per 32 consecutive k (the last block may be partial); ldsfa, ldsfb are
+ * row pitches in bytes, >= ceil(K/32) and multiples of 16; SFA/SFB 16-byte
+ * aligned.  D bf16 as above.
+ */
+int gemm_mxfp8(const void* A, const void* B, const void* SFA, const void* SFB, void* D,
+               int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldsfa,
+               int64_t ldsfb, int64_t ldd, cudaStream_t stream);
+
+int gemm_mxfp8_variant(int variant, const void* A, const void* B, const void* SFA,
+                       const void* SFB, void* D, int64_t M, int64_t N, int64_t K, int64_t lda,
+                       int64_t ldb, int64_t ldsfa, int64_t ldsfb, int64_t ldd,
+                       cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's status
+ * word: GEMM_OK, GEMM_ERR_TIMEOUT when a kernel's bounded barrier wait gave up
+ * (the kernel released its TMEM and returned; D is undefined), or
+ * GEMM_ERR_DEVICE_FAULT when the stream reports a CUDA error.
+ */
+int gemm_last_status(cudaStream_t stream);
+
+/* Raw status word of the last watchdog event (0 if none) without clearing it:
+ * bits 56-63 code, 48-55 wait site, 0-31 CTA index.  Synchronises `stream`. */
+uint64_t gemm_last_status_word(cudaStream_t stream);
+
+/* Static text for a gemm_status_t value. */
+const char* gemm_status_string(int status);
+
+/* Per-wait watchdog limit in milliseconds for later launches on this process
+ * (default 2000, also read once from GEMM_WATCHDOG_MS); returns the old one. */
+int64_t gemm_set_watchdog_ms(int64_t ms);
+
+/* Compile-time plan of a kernel variant, for reports: pipeline stages,
+ * dynamic shared memory bytes, TMEM columns, threads per CTA, CTAs per
+ * cluster, tile M and N.  Returns GEMM_OK or GEMM_ERR_INVALID_ARG. */
+int gemm_kernel_plan(int mxfp8, int variant, int32_t* stages, int32_t* smem_bytes,
+                     int32_t* tmem_cols, int32_t* threads, int32_t* cluster, int32_t* tile_m,
+                     int32_t* tile_n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_GB300_H */

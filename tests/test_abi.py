@@ -1,0 +1,108 @@
+"""The C-ABI library on a CPU-only machine: it builds for sm_103a, loads,
+exports every function include/gemm_gb300.h declares, and rejects bad
+arguments before any device work.  No compute call is made here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import dense_gemm_blackwell_tcgen05_gb300 as g
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gemm_gb300.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(gemm_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_expected():
+    assert declared_functions() == sorted(g.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol():
+    L = g.load()
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_library_is_sm103a_only_and_needs_no_driver_at_load():
+    path = g.library_path()
+    assert os.path.exists(path)
+    # statically linked runtime: loading works here without libcuda
+    ctypes.CDLL(path)
+
+
+def test_status_strings():
+    for code in range(-6, 1):
+        s = g.gemm_status_string(code)
+        assert s and s != "unknown status"
+    assert g.gemm_status_string(7) == "unknown status"
+
+
+NULL = 0
+FAKE = 0x7F0000000000   # never dereferenced: every case below fails validation first
+
+
+@pytest.mark.parametrize("args, want", [
+    (dict(M=-1, N=4, K=4, lda=8, ldb=8, ldd=4), g.GEMM_ERR_INVALID_ARG),
+    (dict(M=4, N=4, K=-4, lda=8, ldb=8, ldd=4), g.GEMM_ERR_INVALID_ARG),
+    (dict(M=1 << 31, N=4, K=4, lda=8, ldb=8, ldd=4), g.GEMM_ERR_INVALID_ARG),
+    (dict(M=4, N=4, K=16, lda=8, ldb=16, ldd=4), g.GEMM_ERR_INVALID_ARG),    # lda < K
+    (dict(M=4, N=4, K=16, lda=16, ldb=8, ldd=4), g.GEMM_ERR_INVALID_ARG),    # ldb < K
+    (dict(M=4, N=8, K=16, lda=16, ldb=16, ldd=4), g.GEMM_ERR_INVALID_ARG),   # ldd < N
+    (dict(M=4, N=4, K=12, lda=12, ldb=16, ldd=4), g.GEMM_ERR_ALIGNMENT),     # 24-byte pitch
+    (dict(M=4, N=4, K=16, lda=16, ldb=20, ldd=4), g.GEMM_ERR_ALIGNMENT),
+    (dict(M=0, N=4, K=16, lda=16, ldb=16, ldd=4), g.GEMM_OK),               # empty: no-op
+    (dict(M=4, N=0, K=16, lda=16, ldb=16, ldd=4), g.GEMM_OK),
+])
+def test_bf16_validation(args, want):
+    rc = g.gemm_bf16(FAKE, FAKE, FAKE, args["M"], args["N"], args["K"], args["lda"], args["ldb"],
+                     args["ldd"], 0)
+    assert rc == want
+
+
+def test_bf16_null_and_misaligned_pointers():
+    assert g.gemm_bf16(NULL, FAKE, FAKE, 4, 4, 16, 16, 16, 4, 0) == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_bf16(FAKE, FAKE, NULL, 4, 4, 16, 16, 16, 4, 0) == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_bf16(FAKE + 8, FAKE, FAKE, 4, 4, 16, 16, 16, 4, 0) == g.GEMM_ERR_ALIGNMENT
+
+
+def test_variant_validation():
+    assert g.gemm_bf16_variant(9, FAKE, FAKE, FAKE, 4, 4, 16, 16, 16, 4, 0) == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_bf16_variant(0x200, FAKE, FAKE, FAKE, 4, 4, 16, 16, 16, 4, 0) == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_mxfp8_variant(g.VARIANT_2CTA, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 4, 32, 32, 32, 16,
+                                16, 4, 0) == g.GEMM_ERR_INVALID_ARG
+
+
+def test_mxfp8_validation():
+    f = lambda **k: g.gemm_mxfp8(k.get("A", FAKE), FAKE, k.get("SFA", FAKE), FAKE, FAKE, 4, 4,
+                                 k.get("K", 64), k.get("lda", 64), 64, k.get("ldsfa", 16), 16, 4, 0)
+    assert f(lda=40, K=40) == g.GEMM_ERR_ALIGNMENT          # E4M3 pitch must be 16-byte multiple
+    assert f(ldsfa=8) == g.GEMM_ERR_ALIGNMENT               # scale pitch multiple of 16
+    assert f(K=1024, lda=1024, ldsfa=16) == g.GEMM_ERR_INVALID_ARG   # ldsfa < ceil(K/32)
+    assert f(SFA=NULL) == g.GEMM_ERR_INVALID_ARG
+    assert f(SFA=FAKE + 4) == g.GEMM_ERR_ALIGNMENT
+
+
+def test_no_device_is_reported_not_crashed():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    # valid-looking arguments reach the device check, which fails cleanly
+    assert g.gemm_bf16(FAKE, FAKE, FAKE, 4, 4, 16, 16, 16, 4, 0) == g.GEMM_ERR_UNSUPPORTED_DEVICE
+
+
+@pytest.mark.parametrize("mx, variant", [(0, 1), (0, 2), (0, 3), (0, 0x101), (0, 0x102), (1, 1), (1, 0x101)])
+def test_kernel_plans_fit_the_sm(mx, variant):
+    p = g.gemm_kernel_plan(bool(mx), variant)
+    assert 0 <= p["smem_bytes"] <= 232448
+    assert p["tmem_cols"] in (128, 256, 512)
+    assert p["stages"] >= 1
+    if (variant & 0xFF) == 2:
+        assert p["cluster"] == 2 and p["tile_m"] == 256 and p["tile_n"] == 256
+    if (variant & 0xFF) in (1, 2):
+        assert p["stages"] >= 3

@@ -1,0 +1,239 @@
+"""bf16 GEMM on the GPU through the C ABI, element by element against the
+oracle.  Bitwise where every partial sum is exact in fp32 (all-ones,
+identity, K=1, small integers); within the bound
+|D - D_ref| <= 2^-7 |D_ref| + 1e-3 sum_k |a_ik b_jk| otherwise."""
+import numpy as np
+import pytest
+import torch
+
+import dense_gemm_blackwell_tcgen05_gb300 as g
+import gemm_inputs as gi
+import oracle
+from tests import parity as P
+
+pytestmark = pytest.mark.gpu
+
+VARIANTS = {
+    "1cta": g.VARIANT_1CTA,
+    "2cta": g.VARIANT_2CTA,
+    "sync": g.VARIANT_SYNC,
+    "1cta_direct": g.VARIANT_1CTA | g.VARIANT_DIRECT_STORE,
+    "2cta_direct": g.VARIANT_2CTA | g.VARIANT_DIRECT_STORE,
+    "auto": g.VARIANT_AUTO,
+}
+FAST = ["1cta", "2cta", "auto"]
+
+
+def run(A_cpu, B_cpu, variant, K=None, ldd=None, stream=None):
+    """D = A B^T on the GPU (A [M, lda], B [N, ldb] bf16 CPU tensors)."""
+    A = A_cpu.cuda()
+    B = B_cpu.cuda()
+    M, lda = A.shape
+    N, ldb = B.shape
+    K = lda if K is None else K
+    ldd = N if ldd is None else ldd
+    Dfull = torch.full((M, ldd), float("nan"), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.current_stream() if stream is None else stream
+    rc = g.gemm_bf16_variant(variant, A.data_ptr(), B.data_ptr(), Dfull.data_ptr(), M, N, K, lda,
+                             ldb, ldd, s.cuda_stream)
+    assert rc == g.GEMM_OK, g.gemm_status_string(rc)
+    st = g.gemm_last_status(s.cuda_stream)
+    assert st == g.GEMM_OK, g.gemm_status_string(st)
+    return Dfull[:, :N].cpu()
+
+
+def ref(A_cpu, B_cpu, K=None):
+    return oracle.gemm_bf16(gi.bf16_codes(A_cpu), gi.bf16_codes(B_cpu), K)
+
+
+def assert_bitwise(D_gpu, D_ref):
+    want = oracle.f64_to_bf16_rne(D_ref)
+    got = gi.bf16_codes(D_gpu)
+    if not np.array_equal(got, want):
+        bad = np.argwhere(got != want)
+        i, j = bad[0]
+        raise AssertionError(f"{len(bad)} mismatches; first at {(i, j)}: got {D_gpu[i, j].item()} "
+                             f"want {D_ref[i, j]}")
+
+
+# ------------------------------------------------------------ exact pins
+
+@pytest.mark.parametrize("v", list(VARIANTS))
+def test_single_tile_workload(v):
+    w = gi.WORKLOADS["single_tile"]
+    A, B = gi.workload_operands("single_tile")
+    D = run(A, B, VARIANTS[v])
+    D_ref, S = ref(A, B)
+    P.check_within_bound(P.bf16_to_f64(D), D_ref, S, f"single_tile/{v}")
+    assert D.shape == (w.M, w.N)
+
+
+@pytest.mark.parametrize("v", list(VARIANTS))
+@pytest.mark.parametrize("K", [8, 64, 1040])
+def test_all_ones(v, K):
+    M, N = 300, 520
+    A = torch.ones(M, K, dtype=torch.bfloat16)
+    B = torch.ones(N, K, dtype=torch.bfloat16)
+    D = run(A, B, VARIANTS[v])
+    assert torch.all(D.float() == K), (D.float().min().item(), D.float().max().item())
+
+
+@pytest.mark.parametrize("v", list(VARIANTS))
+def test_identity(v):
+    K, N = 256, 300
+    A = torch.eye(K, dtype=torch.bfloat16)
+    B = torch.randn(N, K, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16)
+    D = run(A, B, VARIANTS[v])
+    assert torch.equal(D, B.t().contiguous())
+
+
+@pytest.mark.parametrize("v", list(VARIANTS))
+def test_k1_outer_product(v):
+    g_ = torch.Generator().manual_seed(6)
+    M, N = 200, 300
+    A = torch.zeros(M, 8, dtype=torch.bfloat16)
+    B = torch.zeros(N, 8, dtype=torch.bfloat16)
+    A[:, 0] = (torch.randn(M, generator=g_) * 3).to(torch.bfloat16)
+    B[:, 0] = (torch.randn(N, generator=g_) * 0.5).to(torch.bfloat16)
+    D = run(A, B, VARIANTS[v], K=1)
+    D_ref, _ = ref(A, B, 1)
+    assert_bitwise(D, D_ref)
+
+
+@pytest.mark.parametrize("v", list(VARIANTS))
+@pytest.mark.parametrize("shape", [(300, 520, 64), (129, 257, 40), (257, 300, 1040), (4099, 513, 200)])
+def test_small_integers(v, shape):
+    M, N, K = shape
+    rng = np.random.default_rng(M + N + K)
+    A = P.bf16_from_ints(rng.integers(-2, 3, size=(M, K)))
+    B = P.bf16_from_ints(rng.integers(-2, 3, size=(N, K)))
+    D = run(A, B, VARIANTS[v])
+    D_ref, _ = ref(A, B)
+    assert_bitwise(D, D_ref)
+
+
+# ------------------------------------------------------- seeded, tolerance
+
+@pytest.mark.parametrize("v", list(VARIANTS))
+@pytest.mark.parametrize("shape", [(300, 520, 200), (128, 256, 4096), (513, 1031, 264), (1, 1, 8)])
+def test_random_full(v, shape):
+    M, N, K = shape
+    A, B = gi.bf16_operands(M, N, K, seed=M * 7 + N)
+    D = run(A, B, VARIANTS[v])
+    D_ref, S = ref(A, B)
+    P.check_within_bound(P.bf16_to_f64(D), D_ref, S, f"{shape}/{v}")
+
+
+@pytest.mark.parametrize("v", ["1cta", "2cta", "sync"])
+def test_pitches_and_guard_bands(v):
+    """lda > K, ldb > K, ldd > N (aligned and unaligned): rows read at the
+    pitch, and nothing outside D[:, :N] is written."""
+    M, N, K = 261, 300, 136
+    A_wide, B_wide = gi.bf16_operands(M, N, K + 24, seed=9)    # lda = K + 24
+    B_wide = B_wide[:, :K + 8].contiguous()                      # ldb = K + 8
+    for ldd in (N + 12, N + 13):                                 # 16-byte rows / odd pitch
+        sentinel = torch.tensor(-1234.0).to(torch.bfloat16)
+        Dbuf = torch.full((M + 2, ldd), sentinel.item(), dtype=torch.bfloat16, device="cuda")
+        D = Dbuf[1:M + 1]
+        A = A_wide.cuda()
+        B = B_wide.cuda()
+        s = torch.cuda.current_stream().cuda_stream
+        rc = g.gemm_bf16_variant(VARIANTS[v], A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K,
+                                 A.stride(0), B.stride(0), ldd, s)
+        assert rc == g.GEMM_OK
+        assert g.gemm_last_status(s) == g.GEMM_OK
+        host = Dbuf.cpu()
+        assert torch.all(host[0] == sentinel) and torch.all(host[M + 1] == sentinel)
+        assert torch.all(host[1:M + 1, N:] == sentinel), "write outside D[:, :N]"
+        D_ref, S = oracle.gemm_bf16(gi.bf16_codes(A_wide), gi.bf16_codes(B_wide), K)
+        P.check_within_bound(P.bf16_to_f64(host[1:M + 1, :N]), D_ref, S, f"ldd={ldd}/{v}")
+
+
+@pytest.mark.parametrize("v", FAST)
+def test_k_zero_writes_zeros(v):
+    D = torch.full((37, 45), 7.0, dtype=torch.bfloat16, device="cuda")
+    A = torch.zeros(37, 8, dtype=torch.bfloat16, device="cuda")
+    rc = g.gemm_bf16_variant(VARIANTS[v], A.data_ptr(), A.data_ptr(), D.data_ptr(), 37, 45, 0, 8, 8,
+                             45, 0)
+    assert rc == g.GEMM_OK and g.gemm_last_status(0) == g.GEMM_OK
+    assert torch.all(D == 0)
+
+
+def test_empty_m_or_n_is_noop():
+    D = torch.full((4, 4), 7.0, dtype=torch.bfloat16, device="cuda")
+    assert g.gemm_bf16(0, 0, D.data_ptr(), 0, 4, 16, 16, 16, 4, 0) == g.GEMM_OK
+    assert g.gemm_bf16(0, 0, D.data_ptr(), 4, 0, 16, 16, 16, 4, 0) == g.GEMM_OK
+    torch.cuda.synchronize()
+    assert torch.all(D == 7.0)
+
+
+def test_host_pointer_rejected():
+    A = torch.zeros(4, 16, dtype=torch.bfloat16)            # host memory
+    D = torch.zeros(4, 4, dtype=torch.bfloat16, device="cuda")
+    Ad = A.cuda()
+    assert g.gemm_bf16(A.data_ptr(), Ad.data_ptr(), D.data_ptr(), 4, 4, 16, 16, 16, 4, 0) \
+        == g.GEMM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("v", FAST)
+def test_nonfinite_propagation(v):
+    M, N, K = 130, 260, 72
+    A = torch.ones(M, K, dtype=torch.bfloat16)
+    B = torch.ones(N, K, dtype=torch.bfloat16)
+    A[5, 3] = float("nan")
+    A[129, 0] = float("inf")
+    B[257, 0] = 0.0                                          # inf * 0 -> NaN at (129, 257)
+    D = run(A, B, VARIANTS[v]).float()
+    assert torch.all(torch.isnan(D[5]))
+    assert torch.isnan(D[129, 257]) and torch.isinf(D[129, 0]) and D[129, 0] > 0
+    mask = torch.ones_like(D, dtype=torch.bool)
+    mask[5] = False
+    mask[129] = False
+    assert torch.all(D[mask] == K)
+
+
+def test_deterministic_and_streams():
+    A, B = gi.bf16_operands(700, 900, 520, seed=11)
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        D1 = run(A, B, g.VARIANT_AUTO, stream=side)
+    D2 = run(A, B, g.VARIANT_AUTO)
+    assert torch.equal(D1, D2)
+
+
+# ----------------------------------------------- the named workloads, full size
+
+def _sampled(name, variant, n_random=3000):
+    w = gi.WORKLOADS[name]
+    A, B = gi.workload_operands(name)
+    D = run(A, B, variant)
+    rows, cols = P.sample_positions(w.M, w.N, n_random, seed=w.seed)
+    D_ref, S = oracle.gemm_bf16_entries(gi.bf16_codes(A), gi.bf16_codes(B), rows, cols)
+    got = P.bf16_to_f64(D)[rows, cols]
+    P.check_within_bound(got, D_ref, S, name)
+    return A, B, D
+
+
+def test_workload_ragged_k8_full():
+    A, B = gi.workload_operands("ragged_k8")
+    for v in (g.VARIANT_AUTO, g.VARIANT_1CTA, g.VARIANT_2CTA):
+        D = run(A, B, v)
+        D_ref, S = ref(A, B)
+        P.check_within_bound(P.bf16_to_f64(D), D_ref, S, f"ragged_k8/{v}")
+
+
+def test_workload_ragged_k1040():
+    A, B, D = _sampled("ragged_k1040", g.VARIANT_AUTO)
+    # the last M-block (ragged rows) in full
+    r0 = (A.shape[0] // 256) * 256
+    D_ref, S = oracle.gemm_bf16(gi.bf16_codes(A[r0:]), gi.bf16_codes(B))
+    P.check_within_bound(P.bf16_to_f64(D[r0:]), D_ref, S, "ragged_k1040 tail rows")
+
+
+def test_workload_square_4096():
+    _sampled("square_4096", g.VARIANT_AUTO)
+
+
+@pytest.mark.slow
+def test_workload_square_8192():
+    _sampled("square_8192", g.VARIANT_AUTO)
