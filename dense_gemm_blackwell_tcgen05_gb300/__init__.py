@@ -22,7 +22,7 @@ __all__ = [
     "GemmError", "load", "library_path", "EXPORTED_SYMBOLS",
     "gemm_bf16", "gemm_bf16_variant", "gemm_mxfp8", "gemm_mxfp8_variant",
     "gemm_last_status", "gemm_last_status_word", "gemm_status_string", "gemm_set_watchdog_ms",
-    "gemm_kernel_plan", "matmul_bf16", "matmul_mxfp8",
+    "gemm_kernel_plan", "gemm_last_cuda_error", "matmul_bf16", "matmul_mxfp8",
 ]
 
 GEMM_OK = 0
@@ -43,6 +43,7 @@ VARIANT_DIRECT_STORE = 0x100
 EXPORTED_SYMBOLS = (
     "gemm_bf16", "gemm_bf16_variant", "gemm_mxfp8", "gemm_mxfp8_variant", "gemm_last_status",
     "gemm_last_status_word", "gemm_status_string", "gemm_set_watchdog_ms", "gemm_kernel_plan",
+    "gemm_last_cuda_error",
 )
 
 _lock = threading.Lock()
@@ -54,6 +55,8 @@ _vp = ctypes.c_void_p
 class GemmError(RuntimeError):
     def __init__(self, status: int, what: str = ""):
         self.status = status
+        if status == GEMM_ERR_LAUNCH:
+            what = f"{what} (cuda error {gemm_last_cuda_error()})"
         super().__init__(f"{what}: {gemm_status_string(status)} ({status})" if what
                          else f"{gemm_status_string(status)} ({status})")
 
@@ -85,6 +88,8 @@ def load() -> ctypes.CDLL:
             L.gemm_last_status_word.restype = ctypes.c_uint64
             L.gemm_status_string.argtypes = [ctypes.c_int]
             L.gemm_status_string.restype = ctypes.c_char_p
+            L.gemm_last_cuda_error.argtypes = []
+            L.gemm_last_cuda_error.restype = ctypes.c_int
             L.gemm_set_watchdog_ms.argtypes = [_i64]
             L.gemm_set_watchdog_ms.restype = _i64
             P = ctypes.POINTER(ctypes.c_int32)
@@ -128,6 +133,10 @@ def gemm_last_status_word(stream: int = 0) -> int:
 
 def gemm_status_string(status: int) -> str:
     return load().gemm_status_string(status).decode()
+
+
+def gemm_last_cuda_error() -> int:
+    return int(load().gemm_last_cuda_error())
 
 
 def gemm_set_watchdog_ms(ms: int) -> int:

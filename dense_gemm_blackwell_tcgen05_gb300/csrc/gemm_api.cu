@@ -33,6 +33,7 @@ std::mutex g_mu;
 DeviceState g_devices[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::atomic<int64_t> g_watchdog_ms{-1};
+thread_local int t_last_cuda_error = 0;
 
 int64_t watchdog_ms() {
   int64_t v = g_watchdog_ms.load();
@@ -138,6 +139,8 @@ int64_t timeout_ns_for(int64_t K) {
 
 }  // namespace
 
+void note_cuda_error(cudaError_t e) { t_last_cuda_error = static_cast<int>(e); }
+
 bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
                    uint64_t rows, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_rows,
                    CUtensorMapSwizzle swizzle) {
@@ -149,6 +152,7 @@ bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base
   const CUresult r = g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
                               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) t_last_cuda_error = 100000 + static_cast<int>(r);
   return r == CUDA_SUCCESS;
 }
 
@@ -187,12 +191,12 @@ int gemm_bf16_variant(int variant, const void* A, const void* B, void* D, int64_
   switch (base) {
     case GEMM_VARIANT_SYNC:
       return launch_bf16_sync(p, ctx, stream);
-    case GEMM_VARIANT_2CTA:
-      return launch_bf16_ws(2, tma_store, p, ctx, stream);
     case GEMM_VARIANT_1CTA:
+      return launch_bf16_ws(1, tma_store, p, ctx, stream);
+    case GEMM_VARIANT_2CTA:
     case GEMM_VARIANT_AUTO:
     default:
-      return launch_bf16_ws(1, tma_store, p, ctx, stream);
+      return launch_bf16_ws(2, tma_store, p, ctx, stream);
   }
 }
 
@@ -304,6 +308,8 @@ const char* gemm_status_string(int status) {
   }
 }
 
+int gemm_last_cuda_error(void) { return t_last_cuda_error; }
+
 int64_t gemm_set_watchdog_ms(int64_t ms) {
   const int64_t old = watchdog_ms();
   if (ms > 0) g_watchdog_ms.store(ms);
@@ -320,7 +326,7 @@ int gemm_kernel_plan(int mxfp8, int variant, int32_t* stages, int32_t* smem_byte
   if (mxfp8)
     ok = (base == GEMM_VARIANT_AUTO || base == GEMM_VARIANT_1CTA) && plan_mxf8(tma_store, &k);
   else
-    ok = plan_bf16(base == GEMM_VARIANT_AUTO ? 1 : base, tma_store, &k);
+    ok = plan_bf16(base == GEMM_VARIANT_AUTO ? 2 : base, tma_store, &k);
   if (!ok) return GEMM_ERR_INVALID_ARG;
   if (stages) *stages = k.stages;
   if (smem_bytes) *smem_bytes = k.smem_bytes;

@@ -48,16 +48,23 @@ int launch_bf16_sync(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream
   a.timeout_ns = ctx.timeout_ns;
   const dim3 grid((p.N + 127) / 128, (p.M + 127) / 128);
   if (grid.y > 65535u) return GEMM_ERR_INVALID_ARG;
-  // 32 KB static + 24 KB unused dynamic shared memory: at most four CTAs per
-  // SM, so their 128-column TMEM allocations (4 x 128 = 512) never contend.
-  gemm_sync_kernel<<<grid, 128, 24 * 1024, stream>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
+  // ~32 KB static + 15 KB unused dynamic shared memory (+1 KB reserved per
+  // CTA, under the 48 KB no-opt-in limit): at most four CTAs per SM, so their
+  // 128-column TMEM allocations (4 x 128 = 512 columns) never contend.
+  gemm_sync_kernel<<<grid, 128, 15 * 1024, stream>>>(a);
+  if (const cudaError_t e = cudaGetLastError(); e != cudaSuccess) {
+    note_cuda_error(e);
+    return GEMM_ERR_LAUNCH;
+  }
   return GEMM_OK;
 }
 
 int launch_zero_fill(const Problem& p, cudaStream_t stream) {
   zero_fill_kernel<<<1024, 256, 0, stream>>>(static_cast<uint16_t*>(p.D), p.M, p.N, p.ldd);
-  if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
+  if (const cudaError_t e = cudaGetLastError(); e != cudaSuccess) {
+    note_cuda_error(e);
+    return GEMM_ERR_LAUNCH;
+  }
   return GEMM_OK;
 }
 

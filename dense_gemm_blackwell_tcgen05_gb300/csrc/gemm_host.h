@@ -34,6 +34,9 @@ struct Maps {
   CUtensorMap SFB;
 };
 
+// Records the CUDA error behind a GEMM_ERR_LAUNCH for gemm_last_cuda_error().
+void note_cuda_error(cudaError_t e);
+
 // Encodes a 2-D tiled tensor map (rows of `inner` elements, pitch in bytes).
 // Returns false when the driver rejects it.
 bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,

@@ -27,8 +27,10 @@ int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) 
   {
     std::lock_guard<std::mutex> lk(mu);
     if (!prepared[ctx.device]) {
-      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(C::SMEM_BYTES)) != cudaSuccess) {
+      if (const cudaError_t e = cudaFuncSetAttribute(
+              kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM_BYTES));
+          e != cudaSuccess) {
+        note_cuda_error(e);
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
       }
@@ -118,6 +120,7 @@ int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) 
   }
   const cudaError_t err = cudaLaunchKernelEx(&cfg, kern, maps.A, maps.B, maps.D, maps.SFA, maps.SFB, a);
   if (err != cudaSuccess) {
+    note_cuda_error(err);
     cudaGetLastError();
     return GEMM_ERR_LAUNCH;
   }

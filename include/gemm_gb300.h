@@ -118,6 +118,11 @@ int gemm_last_status(cudaStream_t stream);
  * bits 56-63 code, 48-55 wait site, 0-31 CTA index.  Synchronises `stream`. */
 uint64_t gemm_last_status_word(cudaStream_t stream);
 
+/* The CUDA runtime error (cudaError_t value) behind the calling thread's most
+ * recent GEMM_ERR_LAUNCH, or 100000 + CUresult when the driver rejected a
+ * tensor map; 0 if none.  Diagnostic only. */
+int gemm_last_cuda_error(void);
+
 /* Static text for a gemm_status_t value. */
 const char* gemm_status_string(int status);
 
