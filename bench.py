@@ -1,0 +1,470 @@
+#!/usr/bin/env python
+"""Throughput of the tcgen05 GEMM library on one or more GB300s.
+
+One step = one pass of the whole GEMM path over the headline workload:
+D = A B^T for bf16 8192^3 and for block-scaled MXFP8 8192^3 (the two halves
+of the headline metric; the MXFP8 GEMM also exercises the scale-factor path).
+``value`` is the whole job's algorithmic TFLOP/s (2 M N K per GEMM, summed
+over the step and over all ranks) with inputs already resident in HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the CPU oracle, as it stands
+
+Timing: W untimed warm-up steps, then K steps bracketed by a barrier and a
+device synchronise on both sides, CUDA events on the launching stream, max
+over ranks.  The operands (256 MiB of bf16, 128 MiB of E4M3) are larger
+than the 129 MB L2, so no flush is needed between steps.  Multi-GPU runs are
+weak-scaled replicas: every rank multiplies its own copy of the workload and
+no data-path collective exists (the barrier and the max-reduction of the
+elapsed time are the only inter-rank traffic).
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s and % of dense tensor peak (bf16 & MXFP8, 8192³) on 1 GB300"
+HEADLINE = ("square_8192", "mxfp8_8192")
+FP8_OVER_BF16 = 2.0   # nominal dense FP8 / BF16 tensor ratio (4.5 vs 2.25 PFLOP/s)
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# --------------------------------------------------------------- utilities
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="headline",
+                    help="headline (bf16 8192^3 + MXFP8 8192^3) or one named workload")
+    ap.add_argument("--variant", type=int, default=0, help="kernel variant (0 = auto)")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="CPU work budget of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    """Hash of the CUDA sources, to tell whether stored ncu counters still
+    describe the kernels being timed."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dense_gemm_blackwell_tcgen05_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(kernel_key: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        t = json.load(f)
+    if t.get("source_hash") != kernel_source_hash():
+        return None
+    ent = t.get("kernels", {}).get(kernel_key)
+    return None if ent is None else ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.buf = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r for r in csv.reader(io.StringIO(out)) if len(r) >= 9]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        power = [float(r[3]) for r in rows if r[3].strip().replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+def dist_setup(want_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ the workload
+
+def workload_list(name: str):
+    import gemm_inputs as gi
+    names = HEADLINE if name == "headline" else (name,)
+    for n in names:
+        if n not in gi.WORKLOADS:
+            raise SystemExit(f"unknown workload {n}; known: headline, {', '.join(gi.WORKLOADS)}")
+    return [gi.WORKLOADS[n] for n in names]
+
+
+def host_operands(w, pinned: bool = True):
+    """Seeded operands on the host (page-locked when a GPU will copy them)."""
+    import gemm_inputs as gi
+    ops = gi.workload_operands(w.name)
+    return tuple(t.pin_memory() for t in ops) if pinned else ops
+
+
+def alg_bytes(w) -> int:
+    if w.kind == "bf16":
+        return 2 * (w.M * w.K + w.N * w.K + w.M * w.N)
+    nblk = (w.K + 31) // 32
+    return w.M * w.K + w.N * w.K + (w.M + w.N) * nblk + 2 * w.M * w.N
+
+
+class Problem:
+    """Device buffers of one workload plus the call that runs it."""
+
+    def __init__(self, w, host, variant, device):
+        import torch
+        self.w = w
+        self.host = host
+        self.dev = tuple(t.to(device, non_blocking=False) for t in host)
+        self.D = torch.empty(w.M, w.N, dtype=torch.bfloat16, device=device)
+        self.D_host = torch.empty(w.M, w.N, dtype=torch.bfloat16).pin_memory()
+        self.variant = variant
+
+    def launch(self, stream_handle: int, bufs=None) -> int:
+        import dense_gemm_blackwell_tcgen05_gb300 as g
+        w = self.w
+        b = self.dev if bufs is None else bufs
+        if w.kind == "bf16":
+            A, B = b
+            return g.gemm_bf16_variant(self.variant, A.data_ptr(), B.data_ptr(), self.D.data_ptr(),
+                                       w.M, w.N, w.K, A.stride(0), B.stride(0), self.D.stride(0),
+                                       stream_handle)
+        A, SFA, B, SFB = b
+        return g.gemm_mxfp8_variant(self.variant, A.data_ptr(), B.data_ptr(), SFA.data_ptr(),
+                                    SFB.data_ptr(), self.D.data_ptr(), w.M, w.N, w.K, A.stride(0),
+                                    B.stride(0), SFA.stride(0), SFB.stride(0), self.D.stride(0),
+                                    stream_handle)
+
+    def h2d_bytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in self.host)
+
+    def d2h_bytes(self) -> int:
+        return self.D.numel() * self.D.element_size()
+
+
+# ------------------------------------------------------------ CPU oracle leg
+
+def oracle_entries(w, host, n: int) -> float:
+    """Run the oracle on the first `n` entries of D in row-major order; seconds."""
+    import numpy as np
+
+    import gemm_inputs as gi
+    import oracle
+    t = np.arange(n, dtype=np.int64)
+    r, c = t // w.N, t % w.N
+    rows = int(r[-1]) + 1
+    t0 = time.perf_counter()
+    if w.kind == "bf16":
+        A, B = host
+        oracle.gemm_bf16_entries(gi.bf16_codes(A[:rows]), gi.bf16_codes(B), r, c)
+    else:
+        A, SFA, B, SFB = host
+        oracle.gemm_mxfp8_entries(A[:rows].numpy(), B.numpy(), SFA[:rows].numpy(), SFB.numpy(), r, c)
+    return time.perf_counter() - t0
+
+
+def plan_oracle_sample(works, hosts, seconds: float):
+    """Entries per workload so that one pass of the sample takes about `seconds`."""
+    plan = []
+    for w, h in zip(works, hosts):
+        probe = min(w.M * w.N, 4096)
+        t1 = max(oracle_entries(w, h, probe) / probe, 1e-9)
+        n = int(max(1, min(w.M * w.N, (seconds / len(works)) / t1)))
+        plan.append(n)
+    return plan
+
+
+def oracle_pass(works, hosts, plan):
+    secs = 0.0
+    flops = 0
+    for w, h, n in zip(works, hosts, plan):
+        secs += oracle_entries(w, h, n)
+        flops += 2 * n * w.K
+    return flops, secs
+
+
+def sample_text(works, plan) -> str:
+    return "; ".join(f"first {n} of {w.M * w.N} outputs (row-major) of {w.name} "
+                     f"({w.M}x{w.N}x{w.K} {w.kind})" for w, n in zip(works, plan))
+
+
+# --------------------------------------------------------------- the arms
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    import oracle
+    works = workload_list(args.workload)
+    hosts = [host_operands(w, pinned=False) for w in works]
+    oracle.default()
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    plan = plan_oracle_sample(works, hosts, budget)
+    for _ in range(args.warmup):
+        oracle_pass(works, hosts, plan)
+    flops = 0
+    secs = 0.0
+    for _ in range(args.steps):
+        f, s = oracle_pass(works, hosts, plan)
+        flops += f
+        secs += s
+    value = flops / secs / 1e12
+    cores = oracle.num_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": " + ".join(w.name for w in works), "parallelism": "none (CPU)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample_text(works, plan) + " per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    import dense_gemm_blackwell_tcgen05_gb300 as g
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    g.load()
+    works = workload_list(args.workload)
+    hosts = [host_operands(w) for w in works]
+    probs = [Problem(w, h, args.variant, device) for w, h in zip(works, hosts)]
+    stream = torch.cuda.current_stream(device)
+    sh = stream.cuda_stream
+    step_flops = sum(w.flops for w in works)
+
+    def step():
+        for p in probs:
+            rc = p.launch(sh)
+            if rc != g.GEMM_OK:
+                raise g.GemmError(rc, p.w.name)
+
+    # ---- warm-up (also the correctness gate of the watchdog status) ----
+    for _ in range(max(3, args.warmup)):
+        step()
+    st = g.gemm_last_status(sh)
+    if st != g.GEMM_OK:
+        raise g.GemmError(st, "warm-up")
+
+    # ---- device-resident timed region ----
+    starts = [[torch.cuda.Event(enable_timing=True) for _ in range(args.steps)] for _ in probs]
+    ends = [[torch.cuda.Event(enable_timing=True) for _ in range(args.steps)] for _ in probs]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize(device)
+    clocks.start()
+    time.sleep(0.3)   # let the sampler attach before the first timed kernel
+    t0.record(stream)
+    for i in range(args.steps):
+        for j, p in enumerate(probs):
+            starts[j][i].record(stream)
+            rc = p.launch(sh)
+            ends[j][i].record(stream)
+            if rc != g.GEMM_OK:
+                raise g.GemmError(rc, p.w.name)
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world)
+    clk = clocks.stop()
+    st = g.gemm_last_status(sh)
+    if st != g.GEMM_OK:
+        raise g.GemmError(st, "timed region")
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world)
+    value = world * args.steps * step_flops / (elapsed_ms / 1e3) / 1e12
+    kern_ms = [statistics.fmean(s.elapsed_time(e) for s, e in zip(starts[j], ends[j]))
+               for j in range(len(probs))]
+
+    # ---- end to end through the C ABI from pinned host buffers ----
+    e2e_steps = max(1, args.e2e_steps)
+    h2d = sum(p.h2d_bytes() for p in probs)
+    d2h = sum(p.d2h_bytes() for p in probs)
+    staging = [tuple(torch.empty_like(t, device=device) for t in p.host) for p in probs]
+
+    def e2e_step():
+        for p, buf in zip(probs, staging):
+            for dst, src in zip(buf, p.host):
+                dst.copy_(src, non_blocking=True)
+            rc = p.launch(sh, buf)
+            if rc != g.GEMM_OK:
+                raise g.GemmError(rc, p.w.name)
+            p.D_host.copy_(p.D, non_blocking=True)
+
+    e2e_step()
+    barrier(world)
+    torch.cuda.synchronize(device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    e2e_value = world * e2e_steps * step_flops / (e2e_ms / 1e3) / 1e12
+
+    # ---- roofline of each kernel (the first workload's kernel dominates) ----
+    peaks, peak_src = load_peaks()
+    bf16_peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    kernels = {}
+    for p, ms in zip(probs, kern_ms):
+        w = p.w
+        tflops = w.flops / (ms / 1e3) / 1e12
+        gbs = alg_bytes(w) / (ms / 1e3) / 1e9
+        if w.kind == "bf16" and w.K >= 256:
+            bound, ach, pk, unit = "tensor", tflops, bf16_peak, "TFLOP/s"
+        elif w.kind == "mxfp8":
+            bound, ach, pk, unit = "tensor", tflops, bf16_peak * FP8_OVER_BF16, "TFLOP/s"
+        else:
+            bound, ach, pk, unit = "hbm", gbs, peaks["hbm_gbs"], "GB/s"
+        key = f"{w.name}/variant{args.variant}"
+        kernels[w.name] = {"bound": bound, "achieved": ach, "peak": pk, "unit": unit,
+                           "frac": ach / pk, "traffic": stored_traffic(key),
+                           "ms_per_launch": ms, "tflops": tflops, "alg_bytes": alg_bytes(w)}
+    dom = max(range(len(probs)), key=lambda j: kern_ms[j])
+    roof = {k: kernels[works[dom].name][k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
+    roof["kernel"] = works[dom].name
+    roof["peak_source"] = f"{peak_src} ({'bf16_tflops_sustained' if peak_src == 'measured' else 'fallback sustained'}" \
+                          f"{' x2 for FP8' if works[dom].kind == 'mxfp8' else ''})"
+
+    # ---- CPU baseline: the oracle as it stands, bounded sample, rank 0 at N=1 ----
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.default()
+        plan = plan_oracle_sample(works, hosts, args.cpu_seconds)
+        f, s = oracle_pass(works, hosts, plan)
+        cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+               "kind": "oracle", "sample": sample_text(works, plan), "seconds": s}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "+".join(sorted({"bf16" if w.kind == "bf16" else "e4m3" for w in works})) + "->f32",
+            "data": "synthetic (seeded; bf16 N(0,1)*0.5, MXFP8 quantised from N(0,1))",
+            "config": {"workload": " + ".join(f"{w.name} {w.M}x{w.N}x{w.K} {w.kind}" for w in works),
+                       "variant": args.variant, "l2": "operands larger than L2, no flush",
+                       "parallelism": f"replicas x{world} (no data-path collective)"},
+            "roofline": roof,
+            "kernels": kernels,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+            "gpu_launches": args.steps * len(probs),
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_setup(args.gpus)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, rank, world)
+        return run_ours(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

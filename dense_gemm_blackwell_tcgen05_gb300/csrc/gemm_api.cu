@@ -131,6 +131,14 @@ int check_shape(const void* A, const void* B, void* D, int64_t M, int64_t N, int
   return GEMM_OK;
 }
 
+// The TMA-store epilogue needs a 16-byte aligned D with a 16-byte multiple
+// pitch, and N * 2 bytes a multiple of 16 as well: a tensor store clips its
+// box against the row end only to 16-byte granularity, so a ragged N would
+// also write the padding columns up to the next 16-byte boundary.
+bool tma_store_ok(const void* D, int64_t N, int64_t ldd, bool direct) {
+  return !direct && aligned16(D) && (ldd * 2) % 16 == 0 && (N * 2) % 16 == 0;
+}
+
 int64_t timeout_ns_for(int64_t K) {
   // The longest legitimate wait is about one tile's main loop; allow 64 ns per
   // k on top of the fixed limit (eight times a pessimistic per-SM rate).
@@ -187,7 +195,7 @@ int gemm_bf16_variant(int variant, const void* A, const void* B, void* D, int64_
   if (!is_device_pointer(A, ctx.device) || !is_device_pointer(B, ctx.device))
     return GEMM_ERR_INVALID_ARG;
   ctx.timeout_ns = static_cast<unsigned long long>(timeout_ns_for(K));
-  const bool tma_store = !direct && aligned16(D) && (ldd * 2) % 16 == 0;
+  const bool tma_store = tma_store_ok(D, N, ldd, direct);
   switch (base) {
     case GEMM_VARIANT_SYNC:
       return launch_bf16_sync(p, ctx, stream);
@@ -246,7 +254,7 @@ int gemm_mxfp8_variant(int variant, const void* A, const void* B, const void* SF
       !is_device_pointer(SFA, ctx.device) || !is_device_pointer(SFB, ctx.device))
     return GEMM_ERR_INVALID_ARG;
   ctx.timeout_ns = static_cast<unsigned long long>(timeout_ns_for(K));
-  const bool tma_store = !direct && aligned16(D) && (ldd * 2) % 16 == 0;
+  const bool tma_store = tma_store_ok(D, N, ldd, direct);
   return launch_mxf8_ws(tma_store, p, ctx, stream);
 }
 

@@ -189,7 +189,10 @@ def test_nonfinite_propagation(v):
     mask = torch.ones_like(D, dtype=torch.bool)
     mask[5] = False
     mask[129] = False
+    mask[:, 257] = False
     assert torch.all(D[mask] == K)
+    rows = [i for i in range(M) if i not in (5, 129)]
+    assert torch.all(D[rows, 257] == K - 1)            # the one zero term of column 257
 
 
 def test_deterministic_and_streams():
@@ -237,3 +240,37 @@ def test_workload_square_4096():
 @pytest.mark.slow
 def test_workload_square_8192():
     _sampled("square_8192", g.VARIANT_AUTO)
+
+
+@pytest.mark.parametrize("v", list(VARIANTS))
+@pytest.mark.parametrize("K, lda", [(1, 8), (3, 8), (100, 104), (70, 72), (1043, 1048)])
+def test_k_tail_reads_nothing_past_k(v, K, lda):
+    """The pitch padding [K, lda) holds large values; none may enter the sum."""
+    M, N = 256, 512
+    A = torch.ones(M, lda, dtype=torch.bfloat16)
+    B = torch.ones(N, lda, dtype=torch.bfloat16)
+    A[:, K:] = 1000.0
+    B[:, K:] = 1000.0
+    D = run(A, B, VARIANTS[v], K=K)
+    D_ref, _ = ref(A, B, K)
+    assert_bitwise(D, D_ref)
+
+
+@pytest.mark.parametrize("v", ["1cta", "2cta", "auto"])
+@pytest.mark.parametrize("N, ldd", [(300, 304), (300, 320), (260, 264), (1000, 1024)])
+def test_ragged_n_never_writes_padding(v, N, ldd):
+    """D as a column slice of a wider matrix: columns [N, ldd) belong to
+    someone else and must keep their contents."""
+    M, K = 261, 136
+    A, B = gi.bf16_operands(M, N, K, seed=N)
+    big = torch.full((M, ldd), -1234.0, dtype=torch.bfloat16, device="cuda")
+    D = big[:, :N]
+    Ad, Bd = A.cuda(), B.cuda()
+    s = torch.cuda.current_stream().cuda_stream
+    assert g.gemm_bf16_variant(VARIANTS[v], Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), M, N, K, K,
+                               K, ldd, s) == g.GEMM_OK
+    assert g.gemm_last_status(s) == g.GEMM_OK
+    host = big.cpu()
+    assert torch.all(host[:, N:] == torch.tensor(-1234.0).to(torch.bfloat16))
+    D_ref, S = ref(A, B)
+    P.check_within_bound(P.bf16_to_f64(host[:, :N]), D_ref, S, f"N={N} ldd={ldd}/{v}")

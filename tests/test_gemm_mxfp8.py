@@ -42,19 +42,27 @@ def ref(A, SFA, B, SFB, K=None):
     return oracle.gemm_mxfp8(A.numpy(), B.numpy(), SFA.numpy(), SFB.numpy(), K)
 
 
-def int_operands(M, N, K, seed, lda=None):
+def int_operands(M, N, K, seed, lda=None, imax=None, sf_lo=None, sf_hi=None):
+    """Integer E4M3 values in [-imax, imax] and scale bytes in [sf_lo, sf_hi],
+    chosen so that every partial sum is exact in fp32: the sum is a multiple
+    of 2^(2 sf_lo - 254) and at most imax^2 K 2^(2 sf_hi - 254) in size, so it
+    needs fewer than 24 significant bits whatever the summation order."""
     rng = np.random.default_rng(seed)
     lda = K if lda is None else lda
+    if imax is None:
+        imax, sf_lo, sf_hi = (4, 124, 130) if K <= 256 else (1, 126, 129)
+    span = np.log2(imax * imax * K) + 2 * (sf_hi - sf_lo)
+    assert span <= 24, "operand ranges would not keep fp32 partial sums exact"
     nblk = (K + 31) // 32
     pitch = gi.sf_pitch(K)
     A = torch.zeros(M, lda, dtype=torch.uint8)
-    A[:, :K] = P.e4m3_from_ints(rng.integers(-4, 5, size=(M, K)))
+    A[:, :K] = P.e4m3_from_ints(rng.integers(-imax, imax + 1, size=(M, K)))
     B = torch.zeros(N, lda, dtype=torch.uint8)
-    B[:, :K] = P.e4m3_from_ints(rng.integers(-4, 5, size=(N, K)))
+    B[:, :K] = P.e4m3_from_ints(rng.integers(-imax, imax + 1, size=(N, K)))
     SFA = torch.zeros(M, pitch, dtype=torch.uint8)
     SFB = torch.zeros(N, pitch, dtype=torch.uint8)
-    SFA[:, :nblk] = torch.from_numpy(rng.integers(120, 135, size=(M, nblk)).astype(np.uint8))
-    SFB[:, :nblk] = torch.from_numpy(rng.integers(120, 135, size=(N, nblk)).astype(np.uint8))
+    SFA[:, :nblk] = torch.from_numpy(rng.integers(sf_lo, sf_hi + 1, size=(M, nblk)).astype(np.uint8))
+    SFB[:, :nblk] = torch.from_numpy(rng.integers(sf_lo, sf_hi + 1, size=(N, nblk)).astype(np.uint8))
     return A, SFA, B, SFB
 
 
@@ -116,3 +124,23 @@ def test_workload_mxfp8_8192():
     rows, cols = P.sample_positions(w.M, w.N, 3000, seed=w.seed)
     D_ref, S = oracle.gemm_mxfp8_entries(A.numpy(), B.numpy(), SFA.numpy(), SFB.numpy(), rows, cols)
     P.check_within_bound(P.bf16_to_f64(D)[rows, cols], D_ref, S, "mxfp8_8192")
+
+
+@pytest.mark.parametrize("v", list(VARIANTS))
+@pytest.mark.parametrize("K, lda", [(100, 112), (40, 48), (1000, 1008)])
+def test_k_tail_reads_nothing_past_k(v, K, lda):
+    """Operand padding holds 448 and scale padding holds the NaN scale 0xFF;
+    neither may reach the result."""
+    M, N = 256, 512
+    A = torch.full((M, lda), 0x38, dtype=torch.uint8)          # E4M3 1.0
+    B = torch.full((N, lda), 0x38, dtype=torch.uint8)
+    A[:, K:] = 0x7E
+    B[:, K:] = 0x7E
+    nblk = (K + 31) // 32
+    SFA = torch.full((M, 48), 0xFF, dtype=torch.uint8)
+    SFB = torch.full((N, 48), 0xFF, dtype=torch.uint8)
+    SFA[:, :nblk] = 127
+    SFB[:, :nblk] = 127
+    D = run(A, SFA, B, SFB, VARIANTS[v], K=K)
+    D_ref, _ = ref(A, SFA, B, SFB, K)
+    assert np.array_equal(gi.bf16_codes(D), oracle.f64_to_bf16_rne(D_ref))
