@@ -219,8 +219,7 @@ int gemm_mxfp8_variant(int variant, const void* A, const void* B, const void* SF
                        cudaStream_t stream) {
   const int base = variant & 0xFF;
   const bool direct = (variant & GEMM_VARIANT_DIRECT_STORE) != 0;
-  if ((variant & ~(0xFF | GEMM_VARIANT_DIRECT_STORE)) != 0 ||
-      (base != GEMM_VARIANT_AUTO && base != GEMM_VARIANT_1CTA))
+  if ((variant & ~(0xFF | GEMM_VARIANT_DIRECT_STORE)) != 0 || base > GEMM_VARIANT_2CTA)
     return GEMM_ERR_INVALID_ARG;
   int rc = check_shape(A, B, D, M, N, K, lda, ldb, ldd, 1);
   if (rc != GEMM_OK || M == 0 || N == 0) return rc;
@@ -255,7 +254,7 @@ int gemm_mxfp8_variant(int variant, const void* A, const void* B, const void* SF
     return GEMM_ERR_INVALID_ARG;
   ctx.timeout_ns = static_cast<unsigned long long>(timeout_ns_for(K));
   const bool tma_store = tma_store_ok(D, N, ldd, direct);
-  return launch_mxf8_ws(tma_store, p, ctx, stream);
+  return launch_mxf8_ws(base == GEMM_VARIANT_2CTA ? 2 : 1, tma_store, p, ctx, stream);
 }
 
 int gemm_mxfp8(const void* A, const void* B, const void* SFA, const void* SFB, void* D,
@@ -332,7 +331,7 @@ int gemm_kernel_plan(int mxfp8, int variant, int32_t* stages, int32_t* smem_byte
   KernelPlan k;
   bool ok;
   if (mxfp8)
-    ok = (base == GEMM_VARIANT_AUTO || base == GEMM_VARIANT_1CTA) && plan_mxf8(tma_store, &k);
+    ok = base <= GEMM_VARIANT_2CTA && plan_mxf8(base == GEMM_VARIANT_2CTA ? 2 : 1, tma_store, &k);
   else
     ok = plan_bf16(base == GEMM_VARIANT_AUTO ? 2 : base, tma_store, &k);
   if (!ok) return GEMM_ERR_INVALID_ARG;

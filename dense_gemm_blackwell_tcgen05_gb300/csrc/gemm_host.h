@@ -47,7 +47,8 @@ bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base
 int launch_bf16_ws(int cg, bool tma_store, const Problem& p, const LaunchCtx& ctx,
                    cudaStream_t stream);
 int launch_bf16_sync(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream);
-int launch_mxf8_ws(bool tma_store, const Problem& p, const LaunchCtx& ctx, cudaStream_t stream);
+int launch_mxf8_ws(int cg, bool tma_store, const Problem& p, const LaunchCtx& ctx,
+                   cudaStream_t stream);
 int launch_zero_fill(const Problem& p, cudaStream_t stream);
 
 // Compile-time plans for gemm_kernel_plan().
@@ -55,6 +56,6 @@ struct KernelPlan {
   int stages, smem_bytes, tmem_cols, threads, cluster, tile_m, tile_n;
 };
 bool plan_bf16(int cg, bool tma_store, KernelPlan* out);
-bool plan_mxf8(bool tma_store, KernelPlan* out);
+bool plan_mxf8(int cg, bool tma_store, KernelPlan* out);
 
 }  // namespace gb300

@@ -45,16 +45,26 @@ __host__ __device__ constexpr uint32_t align_up_u32(uint32_t x, uint32_t a) {
 
 // Compile-time plan of one kernel configuration: tile shape, stage ring,
 // TMEM column budget and shared-memory map.
+//
+//   bf16,  1 CTA : 128 x 256 tiles, two 256-column accumulators
+//   bf16,  pair  : 256 x 256 cluster tiles, two 256-column accumulators
+//   MXFP8, 1 CTA : 128 x 256 tiles, one accumulator + scale columns
+//   MXFP8, pair  : 256 x 224 cluster tiles, two 224-column accumulators +
+//                  scale columns (2 x 224 + 12 <= 512)
 template <int CG, Kind KIND, bool TMA_STORE>
 struct GemmCfg {
   static_assert(CG == 1 || CG == 2, "cta_group is 1 or 2");
   static constexpr bool MX = KIND == Kind::MXF8;
-  static_assert(!(MX && CG == 2), "MXFP8 runs on the single-CTA kernel");
 
-  static constexpr uint32_t kThreads = 192;   // w0 TMA, w1 MMA/TMEM, w2..5 epilogue
+  // w0 TMA producer, w1 MMA issuer / TMEM owner, w2..5 epilogue and, for
+  // MXFP8, w6: the scale-factor warp.  It re-tiles each stage's scale bytes as
+  // soon as they land (their own barrier) and then arrives on the leader's
+  // ready barrier, which keeps that work off the MMA issuer's path.
+  static constexpr uint32_t kThreads = MX ? 224 : 192;
+  static constexpr uint32_t kSfWarp = 6;
   static constexpr uint32_t BLOCK_M = 128;    // D rows owned by one CTA (= TMEM lanes)
   static constexpr uint32_t UMMA_M = 128 * CG;
-  static constexpr uint32_t UMMA_N = 256;     // D columns per tile (= TMEM columns)
+  static constexpr uint32_t UMMA_N = (MX && CG == 2) ? 224 : 256;   // D columns per tile
   static constexpr uint32_t B_ROWS = UMMA_N / CG;  // B rows staged by one CTA
   static constexpr uint32_t ELEM = MX ? 1 : 2;
   static constexpr uint32_t BK = 128 / ELEM;  // K elements per stage: one 128-byte row
@@ -63,30 +73,35 @@ struct GemmCfg {
   static constexpr uint32_t A_BYTES = BLOCK_M * 128;
   static constexpr uint32_t B_BYTES = B_ROWS * 128;
   // MXFP8 scale factors: a TMA box of 16 bytes (4 K-tiles' scales) per row,
-  // then the MMA warp re-tiles one K-tile's bytes into the 32x16-byte chunk
-  // that tcgen05.cp copies into TMEM.
+  // then the scale-factor warp re-tiles one K-tile's bytes into the 32x16-byte
+  // chunks that tcgen05.cp copies into TMEM.  Every CTA holds the scales of
+  // all UMMA_N B rows of the tile (its tensor core multiplies by all of them).
   static constexpr uint32_t SFB_ROWS = MX ? UMMA_N : 0;
+  static constexpr uint32_t SFB_CHUNKS = (SFB_ROWS + 127) / 128;
   static constexpr uint32_t SFA_RAW = MX ? BLOCK_M * 16 : 0;
   static constexpr uint32_t SFB_RAW = SFB_ROWS * 16;
-  static constexpr uint32_t SFA_T = MX ? BLOCK_M * 4 : 0;
-  static constexpr uint32_t SFB_T = SFB_ROWS * 4;
+  static constexpr uint32_t SFA_T = MX ? 512 : 0;
+  static constexpr uint32_t SFB_T = SFB_CHUNKS * 512;
   static constexpr uint32_t OFF_B = A_BYTES;
-  static constexpr uint32_t OFF_SFA_RAW = OFF_B + B_BYTES;
+  static constexpr uint32_t OFF_SFA_RAW = align_up_u32(OFF_B + B_BYTES, 128);
   static constexpr uint32_t OFF_SFB_RAW = OFF_SFA_RAW + SFA_RAW;
-  static constexpr uint32_t OFF_SFA_T = OFF_SFB_RAW + SFB_RAW;
+  static constexpr uint32_t OFF_SFA_T = align_up_u32(OFF_SFB_RAW + SFB_RAW, 128);
   static constexpr uint32_t OFF_SFB_T = OFF_SFA_T + SFA_T;
   static constexpr uint32_t STAGE_BYTES = align_up_u32(OFF_SFB_T + SFB_T, 1024);
-  static constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES + SFA_RAW + SFB_RAW;  // per CTA
+  static constexpr uint32_t AB_TX = A_BYTES + B_BYTES;            // per CTA
+  static constexpr uint32_t SF_TX = SFA_RAW + SFB_RAW;            // per CTA
+  static constexpr uint32_t FULL_ARRIVALS = MX ? 1 + CG : 1;      // producer (+ SF warps)
 
   // TMEM: ACC_STAGES accumulators of UMMA_N fp32 columns, then the scale
-  // factors (MXFP8: 4 columns for A, 8 for B).  512 = whole TMEM.
-  static constexpr uint32_t ACC_STAGES = MX ? 1 : 2;
+  // factors (MXFP8: 4 columns for A, 4 per 128 B rows).  512 = whole TMEM.
+  static constexpr uint32_t ACC_STAGES = (MX && CG == 1) ? 1 : 2;
   static constexpr uint32_t SF_TMEM_COL = ACC_STAGES * UMMA_N;
   static constexpr uint32_t TMEM_COLS = 512;
-  static_assert(SF_TMEM_COL + (MX ? 12 : 0) <= TMEM_COLS, "TMEM column budget");
+  static_assert(SF_TMEM_COL + (MX ? 4 + 4 * SFB_CHUNKS : 0) <= TMEM_COLS, "TMEM column budget");
 
   // Epilogue staging for TMA stores: per epilogue warp, two 32x64 bf16
   // buffers (32 rows of 128 bytes, 128-byte swizzled).
+  static_assert(!TMA_STORE || UMMA_N % 64 == 0, "TMA-store epilogue works in 64-column chunks");
   static constexpr uint32_t EPI_BUF_BYTES = 32 * 128;
   static constexpr uint32_t EPI_BUFS = 2;
   static constexpr uint32_t EPI_BYTES = TMA_STORE ? 4 * EPI_BUFS * EPI_BUF_BYTES : 0;
@@ -100,8 +115,27 @@ struct GemmCfg {
   static_assert(STAGES >= 2, "stage ring needs two slots");
   static constexpr uint32_t SMEM_BYTES = ALIGN_SLACK + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
-  static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
+  static_assert((3 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
 };
+
+// Re-tile one K-tile's scale bytes for tcgen05.cp ... 32x128b.warpx4: the
+// 4-byte word of row r (one UE8M0 per 32 k, K-tile word w of the 16-byte
+// TMA row) moves to byte 16*(r%32) + 4*(r/32) of its 128-row chunk.  Rows
+// past `rows` (a tile narrower than the last chunk) are written as zero.
+template <uint32_t CHUNKS>
+__device__ __forceinline__ void retile_scales(const uint8_t* raw, uint8_t* dst, uint32_t rows,
+                                              uint32_t w, uint32_t lane) {
+  const uint32_t* rw = reinterpret_cast<const uint32_t*>(raw);
+  uint4* dt = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (uint32_t h = 0; h < CHUNKS; ++h) {
+    const uint32_t r = h * 128 + lane;
+    uint32_t v[4];
+#pragma unroll
+    for (uint32_t q = 0; q < 4; ++q) v[q] = (r + 32 * q < rows) ? rw[(r + 32 * q) * 4 + w] : 0u;
+    dt[h * 32 + lane] = make_uint4(v[0], v[1], v[2], v[3]);
+  }
+}
 
 template <int CG>
 __device__ __forceinline__ void commit_to(uint32_t bar) {
@@ -168,7 +202,7 @@ __device__ __forceinline__ void store_row32(uint16_t* D, uint64_t ldd, uint32_t 
 }
 
 template <int CG, Kind KIND, bool TMA_STORE>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
     gemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD,
                    const __grid_constant__ CUtensorMap tmSFA,
@@ -183,10 +217,11 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t bar0 = epi0 + C::EPI_BYTES;
   const auto full_bar = [&](uint32_t s) { return bar0 + 8 * s; };
   const auto empty_bar = [&](uint32_t s) { return bar0 + 8 * (C::STAGES + s); };
-  const auto accf_bar = [&](uint32_t b) { return bar0 + 8 * (2 * C::STAGES + b); };
-  const auto acce_bar = [&](uint32_t b) { return bar0 + 8 * (2 * C::STAGES + 2 + b); };
-  const uint32_t drain_bar = bar0 + 8 * (2 * C::STAGES + 4);
-  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + (bar0 - base) + 8 * (2 * C::STAGES + 5));
+  const auto sf_full_bar = [&](uint32_t s) { return bar0 + 8 * (2 * C::STAGES + s); };
+  const auto accf_bar = [&](uint32_t b) { return bar0 + 8 * (3 * C::STAGES + b); };
+  const auto acce_bar = [&](uint32_t b) { return bar0 + 8 * (3 * C::STAGES + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8 * (3 * C::STAGES + 4);
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + (bar0 - base) + 8 * (3 * C::STAGES + 5));
   volatile uint32_t* const abort_flag = tmem_slot + 1;
 
   const uint32_t warp = warp_idx_sync();
@@ -200,8 +235,9 @@ __global__ void __launch_bounds__(192, 1)
   // ---- set-up: barriers (one thread), TMEM allocation (one warp) ----------
   if (warp == 0 && lane == 0) {
     for (uint32_t s = 0; s < C::STAGES; ++s) {
-      mbar_init(full_bar(s), 1);    // producer's expect_tx arrival (+ TMA bytes)
-      mbar_init(empty_bar(s), 1);   // MMA issuer's commit
+      mbar_init(full_bar(s), C::FULL_ARRIVALS);  // producer's expect_tx (+ SF warps) + bytes
+      mbar_init(empty_bar(s), 1);                // MMA issuer's commit
+      mbar_init(sf_full_bar(s), 1);              // this CTA's scale bytes (MXFP8)
     }
     for (uint32_t b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);        // MMA issuer's commit after the last K-tile
@@ -252,29 +288,39 @@ __global__ void __launch_bounds__(192, 1)
           }
           const uint32_t sb = stage0 + s * C::STAGE_BYTES;
           const int32_t kx = static_cast<int32_t>(kt * C::BK);
+          if constexpr (C::MX) {
+            // scale bytes (4 K-tiles per 16-byte box row) land on this CTA's own
+            // barrier, where its scale-factor warp waits
+            const int32_t sx = static_cast<int32_t>((kt / 4) * 16);
+            const int32_t sfb_row = static_cast<int32_t>(nb * C::UMMA_N);   // all B rows of the tile
+            mbar_arrive_expect_tx(sf_full_bar(s), C::SF_TX);
+            tma_load_2d(sb + C::OFF_SFA_RAW, &tmSFA, sf_full_bar(s), sx, a_row, pol);
+            tma_load_2d(sb + C::OFF_SFB_RAW, &tmSFB, sf_full_bar(s), sx, sfb_row, pol);
+          }
           if constexpr (CG == 1) {
-            mbar_arrive_expect_tx(full_bar(s), C::TX_BYTES);
+            mbar_arrive_expect_tx(full_bar(s), C::AB_TX);
             tma_load_2d(sb, &tmA, full_bar(s), kx, a_row, pol);
             tma_load_2d(sb + C::OFF_B, &tmB, full_bar(s), kx, b_row, pol);
-            if constexpr (C::MX) {
-              const int32_t sx = static_cast<int32_t>((kt / 4) * 16);
-              tma_load_2d(sb + C::OFF_SFA_RAW, &tmSFA, full_bar(s), sx, a_row, pol);
-              tma_load_2d(sb + C::OFF_SFB_RAW, &tmSFB, full_bar(s), sx, b_row, pol);
-            }
           } else {
-            // both CTAs' bytes land on the leader's ready barrier
+            // both CTAs' operand bytes land on the leader's ready barrier
             const uint32_t leader_full = mapa_shared(full_bar(s), 0);
-            if (leader) mbar_arrive_expect_tx(full_bar(s), CG * C::TX_BYTES);
+            if (leader) mbar_arrive_expect_tx(full_bar(s), CG * C::AB_TX);
             tma_load_2d_pair(sb, &tmA, leader_full, kx, a_row, pol);
             tma_load_2d_pair(sb + C::OFF_B, &tmB, leader_full, kx, b_row, pol);
           }
         }
       }
       // Exit path after a give-up: let this CTA's issued loads land first.
-      if (*abort_flag && leader) {
+      if (*abort_flag) {
         const uint32_t first = it > C::STAGES ? it - C::STAGES : 0u;
-        for (uint32_t i = first; i < it; ++i)
-          drain_wait(full_bar(i % C::STAGES), (i / C::STAGES) & 1u, wd, kSiteProducerDrain);
+        for (uint32_t i = first; i < it; ++i) {
+          // (MXFP8's ready barrier also counts SF-warp arrivals, which may never
+          // come after a give-up; its scale bytes have their own barrier)
+          if (leader && !C::MX)
+            drain_wait(full_bar(i % C::STAGES), (i / C::STAGES) & 1u, wd, kSiteProducerDrain);
+          if constexpr (C::MX)
+            drain_wait(sf_full_bar(i % C::STAGES), (i / C::STAGES) & 1u, wd, kSiteProducerDrain);
+        }
       }
     }
   } else if (warp == 1) {
@@ -298,26 +344,6 @@ __global__ void __launch_bounds__(192, 1)
             break;
           }
           const uint32_t sb = stage0 + s * C::STAGE_BYTES;
-          if constexpr (C::MX) {
-            // Re-tile this K-tile's scale bytes: row r's 4-byte word (one
-            // UE8M0 per 32 k) moves to byte 16*(r%32) + 4*(r/32) of its
-            // 128-row chunk, the layout tcgen05.cp ... 32x128b.warpx4 expects.
-            const uint32_t w = kt & 3u;
-            const uint32_t* rawA = reinterpret_cast<const uint32_t*>(base_ptr + (sb - base) + C::OFF_SFA_RAW);
-            const uint32_t* rawB = reinterpret_cast<const uint32_t*>(base_ptr + (sb - base) + C::OFF_SFB_RAW);
-            uint4* tA = reinterpret_cast<uint4*>(base_ptr + (sb - base) + C::OFF_SFA_T);
-            uint4* tB = reinterpret_cast<uint4*>(base_ptr + (sb - base) + C::OFF_SFB_T);
-            tA[lane] = make_uint4(rawA[(lane + 0) * 4 + w], rawA[(lane + 32) * 4 + w],
-                                  rawA[(lane + 64) * 4 + w], rawA[(lane + 96) * 4 + w]);
-#pragma unroll
-            for (uint32_t h = 0; h < C::SFB_ROWS / 128; ++h) {
-              const uint32_t r = h * 128 + lane;
-              tB[h * 32 + lane] = make_uint4(rawB[(r + 0) * 4 + w], rawB[(r + 32) * 4 + w],
-                                             rawB[(r + 64) * 4 + w], rawB[(r + 96) * 4 + w]);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-          }
           if (lane == 0) {
             tc_fence_after_sync();
             const uint64_t adesc = smem_desc_sw128(sb);
@@ -327,7 +353,7 @@ __global__ void __launch_bounds__(192, 1)
               const uint32_t sfb_t = sfa_t + 4;
               tmem_cp_32x128b_warpx4<CG>(sfa_t, smem_desc_rows16(sb + C::OFF_SFA_T));
 #pragma unroll
-              for (uint32_t h = 0; h < C::SFB_ROWS / 128; ++h)
+              for (uint32_t h = 0; h < C::SFB_CHUNKS; ++h)
                 tmem_cp_32x128b_warpx4<CG>(sfb_t + 4 * h, smem_desc_rows16(sb + C::OFF_SFB_T + 512 * h));
 #pragma unroll
               for (uint32_t k = 0; k < C::K_STEPS; ++k)
@@ -359,7 +385,34 @@ __global__ void __launch_bounds__(192, 1)
       }
       __syncwarp();
     }
-  } else {
+  } else if (C::MX && warp == C::kSfWarp) {
+    // ==================== scale-factor warp (every CTA) ===========================
+    // Re-tile this CTA's scale bytes of every K-tile into the tcgen05.cp layout
+    // and report to the leader's ready barrier (one arrival per CTA and stage).
+    uint32_t it = 0;
+    bool ok = true;
+    for (uint32_t t = cluster_id; t < num_tiles && ok; t += num_clusters) {
+      for (uint32_t kt = 0; kt < KT; ++kt, ++it) {
+        const uint32_t s = it % C::STAGES;
+        if (!warp_wait(sf_full_bar(s), (it / C::STAGES) & 1u, wd, kSiteSfFull, lane)) {
+          ok = false;
+          break;
+        }
+        uint8_t* const sp = base_ptr + (stage0 + s * C::STAGE_BYTES - base);
+        retile_scales<1>(sp + C::OFF_SFA_RAW, sp + C::OFF_SFA_T, C::BLOCK_M, kt & 3u, lane);
+        retile_scales<C::SFB_CHUNKS>(sp + C::OFF_SFB_RAW, sp + C::OFF_SFB_T, C::SFB_ROWS, kt & 3u,
+                                     lane);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (CG == 1)
+            mbar_arrive(full_bar(s));
+          else
+            mbar_arrive_cluster(mapa_shared(full_bar(s), 0));
+        }
+      }
+    }
+  } else if (warp >= 2 && warp < 6) {
     // ==================== epilogue: four warps, one TMEM lane quarter each =========
     const uint32_t q = warp & 3u;            // TMEM lanes 32q .. 32q+31
     const uint32_t ew = warp - 2u;           // staging slot owner

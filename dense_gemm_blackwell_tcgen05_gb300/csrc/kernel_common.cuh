@@ -20,6 +20,7 @@ enum WaitSite : uint32_t {
   kSiteMmaDrain = 5,        // MMA issuer draining its own tcgen05 ops at exit
   kSiteProducerDrain = 6,   // producer draining its own TMA loads at exit
   kSiteSyncMma = 7,         // single-tile kernel waiting for its MMA
+  kSiteSfFull = 8,          // scale-factor warp waiting for its scale bytes
 };
 
 struct Watchdog {

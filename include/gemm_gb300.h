@@ -68,7 +68,9 @@ typedef enum {
   GEMM_VARIANT_1CTA = 1,        /* persistent warp-specialised, cta_group::1,
                                    128x256 tiles (ladder levels 4-7)               */
   GEMM_VARIANT_2CTA = 2,        /* persistent warp-specialised CTA pair,
-                                   cta_group::2, 256x256 tiles (ladder level 8)    */
+                                   cta_group::2, 256x256 tiles (bf16) or 256x224
+                                   tiles (MXFP8, masked-store epilogue)
+                                   (ladder level 8)                                */
   GEMM_VARIANT_SYNC = 3,        /* one 128x128 tile per CTA, synchronous copies
                                    (ladder levels 1-3; bf16 only, reference rung)  */
   GEMM_VARIANT_DIRECT_STORE = 0x100  /* flag: masked st.global epilogue instead of

@@ -74,7 +74,7 @@ def test_bf16_null_and_misaligned_pointers():
 def test_variant_validation():
     assert g.gemm_bf16_variant(9, FAKE, FAKE, FAKE, 4, 4, 16, 16, 16, 4, 0) == g.GEMM_ERR_INVALID_ARG
     assert g.gemm_bf16_variant(0x200, FAKE, FAKE, FAKE, 4, 4, 16, 16, 16, 4, 0) == g.GEMM_ERR_INVALID_ARG
-    assert g.gemm_mxfp8_variant(g.VARIANT_2CTA, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 4, 32, 32, 32, 16,
+    assert g.gemm_mxfp8_variant(g.VARIANT_SYNC, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 4, 32, 32, 32, 16,
                                 16, 4, 0) == g.GEMM_ERR_INVALID_ARG
 
 
@@ -96,13 +96,14 @@ def test_no_device_is_reported_not_crashed():
     assert g.gemm_bf16(FAKE, FAKE, FAKE, 4, 4, 16, 16, 16, 4, 0) == g.GEMM_ERR_UNSUPPORTED_DEVICE
 
 
-@pytest.mark.parametrize("mx, variant", [(0, 1), (0, 2), (0, 3), (0, 0x101), (0, 0x102), (1, 1), (1, 0x101)])
+@pytest.mark.parametrize("mx, variant", [(0, 1), (0, 2), (0, 3), (0, 0x101), (0, 0x102), (1, 1), (1, 0x101),
+                                        (1, 2)])
 def test_kernel_plans_fit_the_sm(mx, variant):
     p = g.gemm_kernel_plan(bool(mx), variant)
     assert 0 <= p["smem_bytes"] <= 232448
     assert p["tmem_cols"] in (128, 256, 512)
     assert p["stages"] >= 1
     if (variant & 0xFF) == 2:
-        assert p["cluster"] == 2 and p["tile_m"] == 256 and p["tile_n"] == 256
+        assert p["cluster"] == 2 and p["tile_m"] == 256 and p["tile_n"] == (224 if mx else 256)
     if (variant & 0xFF) in (1, 2):
         assert p["stages"] >= 3

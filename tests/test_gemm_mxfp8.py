@@ -17,6 +17,7 @@ pytestmark = pytest.mark.gpu
 VARIANTS = {
     "1cta": g.VARIANT_1CTA,
     "1cta_direct": g.VARIANT_1CTA | g.VARIANT_DIRECT_STORE,
+    "2cta": g.VARIANT_2CTA,
     "auto": g.VARIANT_AUTO,
 }
 
