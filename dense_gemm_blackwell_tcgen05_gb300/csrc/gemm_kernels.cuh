@@ -72,25 +72,33 @@ struct GemmCfg {
   static constexpr uint32_t K_STEPS = BK / UMMA_K;
   static constexpr uint32_t A_BYTES = BLOCK_M * 128;
   static constexpr uint32_t B_BYTES = B_ROWS * 128;
-  // MXFP8 scale factors: a TMA box of 16 bytes (4 K-tiles' scales) per row,
-  // then the scale-factor warp re-tiles one K-tile's bytes into the 32x16-byte
-  // chunks that tcgen05.cp copies into TMEM.  Every CTA holds the scales of
-  // all UMMA_N B rows of the tile (its tensor core multiplies by all of them).
+  static constexpr uint32_t STAGE_BYTES = align_up_u32(A_BYTES + B_BYTES, 1024);
+  static constexpr uint32_t OFF_B = A_BYTES;
+  static constexpr uint32_t AB_TX = A_BYTES + B_BYTES;            // per CTA
+  static constexpr uint32_t FULL_ARRIVALS = 1;                    // the producer's expect_tx
+
+  // MXFP8 scale factors travel in their own ring of SF_SLOTS slots, one slot
+  // per group of SF_GROUP = 4 K-tiles: one 16-byte TMA box row carries 4
+  // K-tiles' scales (4 x 4 UE8M0 bytes).  The scale-factor warp re-tiles a
+  // landed slot into one 32x16-byte chunk per 128 rows and K-tile, the
+  // layout tcgen05.cp ... 32x128b.warpx4 copies into TMEM.  Every CTA holds
+  // the scales of all UMMA_N B rows of the tile (its tensor core multiplies
+  // by all of them) and of its own 128 A rows.
+  static constexpr uint32_t SF_GROUP = 4;
+  static constexpr uint32_t SF_SLOTS = 2;
   static constexpr uint32_t SFB_ROWS = MX ? UMMA_N : 0;
   static constexpr uint32_t SFB_CHUNKS = (SFB_ROWS + 127) / 128;
   static constexpr uint32_t SFA_RAW = MX ? BLOCK_M * 16 : 0;
   static constexpr uint32_t SFB_RAW = SFB_ROWS * 16;
-  static constexpr uint32_t SFA_T = MX ? 512 : 0;
+  static constexpr uint32_t SFA_T = MX ? 512 : 0;                 // one chunk per K-tile
   static constexpr uint32_t SFB_T = SFB_CHUNKS * 512;
-  static constexpr uint32_t OFF_B = A_BYTES;
-  static constexpr uint32_t OFF_SFA_RAW = align_up_u32(OFF_B + B_BYTES, 128);
-  static constexpr uint32_t OFF_SFB_RAW = OFF_SFA_RAW + SFA_RAW;
-  static constexpr uint32_t OFF_SFA_T = align_up_u32(OFF_SFB_RAW + SFB_RAW, 128);
-  static constexpr uint32_t OFF_SFB_T = OFF_SFA_T + SFA_T;
-  static constexpr uint32_t STAGE_BYTES = align_up_u32(OFF_SFB_T + SFB_T, 1024);
-  static constexpr uint32_t AB_TX = A_BYTES + B_BYTES;            // per CTA
-  static constexpr uint32_t SF_TX = SFA_RAW + SFB_RAW;            // per CTA
-  static constexpr uint32_t FULL_ARRIVALS = MX ? 1 + CG : 1;      // producer (+ SF warps)
+  static constexpr uint32_t T_PER_KT = SFA_T + SFB_T;
+  static constexpr uint32_t OFF_SFA_RAW = 0;                      // within a slot
+  static constexpr uint32_t OFF_SFB_RAW = SFA_RAW;
+  static constexpr uint32_t OFF_T = align_up_u32(SFA_RAW + SFB_RAW, 128);
+  static constexpr uint32_t SF_SLOT_BYTES = MX ? align_up_u32(OFF_T + SF_GROUP * T_PER_KT, 1024) : 0;
+  static constexpr uint32_t SF_BYTES = SF_SLOTS * SF_SLOT_BYTES;
+  static constexpr uint32_t SF_TX = SFA_RAW + SFB_RAW;            // per CTA and slot
 
   // TMEM: ACC_STAGES accumulators of UMMA_N fp32 columns, then the scale
   // factors (MXFP8: 4 columns for A, 4 per 128 B rows).  512 = whole TMEM.
@@ -110,30 +118,38 @@ struct GemmCfg {
   static constexpr uint32_t BAR_BYTES = 256;
   static constexpr uint32_t ALIGN_SLACK = 1024;
   static constexpr uint32_t STAGES_FIT =
-      (SMEM_LIMIT - ALIGN_SLACK - BAR_BYTES - EPI_BYTES) / STAGE_BYTES;
+      (SMEM_LIMIT - ALIGN_SLACK - BAR_BYTES - EPI_BYTES - SF_BYTES) / STAGE_BYTES;
   static constexpr uint32_t STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static_assert(STAGES >= 2, "stage ring needs two slots");
-  static constexpr uint32_t SMEM_BYTES = ALIGN_SLACK + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
+  static constexpr uint32_t SMEM_BYTES =
+      ALIGN_SLACK + STAGES * STAGE_BYTES + SF_BYTES + EPI_BYTES + BAR_BYTES;
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
-  static_assert((3 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
+  static_assert((2 * STAGES + 3 * SF_SLOTS + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
 };
 
-// Re-tile one K-tile's scale bytes for tcgen05.cp ... 32x128b.warpx4: the
-// 4-byte word of row r (one UE8M0 per 32 k, K-tile word w of the 16-byte
-// TMA row) moves to byte 16*(r%32) + 4*(r/32) of its 128-row chunk.  Rows
-// past `rows` (a tile narrower than the last chunk) are written as zero.
+// Re-tile one slot's scale bytes for tcgen05.cp ... 32x128b.warpx4.  The raw
+// TMA box holds 16 bytes per row: the 4-byte words of 4 consecutive K-tiles
+// (one UE8M0 per 32 k).  For K-tile j, row r's word moves to byte
+// 16*(r%32) + 4*(r/32) of its 128-row chunk.  Lane l reads whole 16-byte rows
+// l, l+32, l+64, l+96 and writes one 16-byte chunk row per K-tile, so both
+// sides are bank-conflict free.  Rows past `rows` are written as zero.
 template <uint32_t CHUNKS>
-__device__ __forceinline__ void retile_scales(const uint8_t* raw, uint8_t* dst, uint32_t rows,
-                                              uint32_t w, uint32_t lane) {
-  const uint32_t* rw = reinterpret_cast<const uint32_t*>(raw);
-  uint4* dt = reinterpret_cast<uint4*>(dst);
+__device__ __forceinline__ void retile_scales(const uint8_t* raw, uint8_t* t_base, uint32_t t_stride,
+                                              uint32_t t_off, uint32_t rows, uint32_t lane) {
+  const uint4* rw = reinterpret_cast<const uint4*>(raw);
 #pragma unroll
   for (uint32_t h = 0; h < CHUNKS; ++h) {
-    const uint32_t r = h * 128 + lane;
-    uint32_t v[4];
+    uint4 v[4];
 #pragma unroll
-    for (uint32_t q = 0; q < 4; ++q) v[q] = (r + 32 * q < rows) ? rw[(r + 32 * q) * 4 + w] : 0u;
-    dt[h * 32 + lane] = make_uint4(v[0], v[1], v[2], v[3]);
+    for (uint32_t q = 0; q < 4; ++q) {
+      const uint32_t r = h * 128 + 32 * q + lane;
+      v[q] = r < rows ? rw[r] : make_uint4(0, 0, 0, 0);
+    }
+    uint4* d0 = reinterpret_cast<uint4*>(t_base + t_off + h * 512) + lane;
+    *d0 = make_uint4(v[0].x, v[1].x, v[2].x, v[3].x);
+    *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(d0) + t_stride) = make_uint4(v[0].y, v[1].y, v[2].y, v[3].y);
+    *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(d0) + 2 * t_stride) = make_uint4(v[0].z, v[1].z, v[2].z, v[3].z);
+    *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(d0) + 3 * t_stride) = make_uint4(v[0].w, v[1].w, v[2].w, v[3].w);
   }
 }
 
@@ -213,15 +229,20 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const base_ptr = smem_raw + (base - raw);
   const uint32_t stage0 = base;
-  const uint32_t epi0 = base + C::STAGES * C::STAGE_BYTES;
+  const uint32_t sf0 = base + C::STAGES * C::STAGE_BYTES;
+  const uint32_t epi0 = sf0 + C::SF_BYTES;
   const uint32_t bar0 = epi0 + C::EPI_BYTES;
   const auto full_bar = [&](uint32_t s) { return bar0 + 8 * s; };
   const auto empty_bar = [&](uint32_t s) { return bar0 + 8 * (C::STAGES + s); };
-  const auto sf_full_bar = [&](uint32_t s) { return bar0 + 8 * (2 * C::STAGES + s); };
-  const auto accf_bar = [&](uint32_t b) { return bar0 + 8 * (3 * C::STAGES + b); };
-  const auto acce_bar = [&](uint32_t b) { return bar0 + 8 * (3 * C::STAGES + 2 + b); };
-  const uint32_t drain_bar = bar0 + 8 * (3 * C::STAGES + 4);
-  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + (bar0 - base) + 8 * (3 * C::STAGES + 5));
+  constexpr uint32_t kSfBar0 = 2 * C::STAGES;
+  const auto sf_full_bar = [&](uint32_t g) { return bar0 + 8 * (kSfBar0 + g); };
+  const auto sf_ready_bar = [&](uint32_t g) { return bar0 + 8 * (kSfBar0 + C::SF_SLOTS + g); };
+  const auto sf_empty_bar = [&](uint32_t g) { return bar0 + 8 * (kSfBar0 + 2 * C::SF_SLOTS + g); };
+  constexpr uint32_t kAccBar0 = kSfBar0 + 3 * C::SF_SLOTS;
+  const auto accf_bar = [&](uint32_t b) { return bar0 + 8 * (kAccBar0 + b); };
+  const auto acce_bar = [&](uint32_t b) { return bar0 + 8 * (kAccBar0 + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8 * (kAccBar0 + 4);
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + (bar0 - base) + 8 * (kAccBar0 + 5));
   volatile uint32_t* const abort_flag = tmem_slot + 1;
 
   const uint32_t warp = warp_idx_sync();
@@ -235,9 +256,13 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
   // ---- set-up: barriers (one thread), TMEM allocation (one warp) ----------
   if (warp == 0 && lane == 0) {
     for (uint32_t s = 0; s < C::STAGES; ++s) {
-      mbar_init(full_bar(s), C::FULL_ARRIVALS);  // producer's expect_tx (+ SF warps) + bytes
+      mbar_init(full_bar(s), C::FULL_ARRIVALS);  // producer's expect_tx (+ TMA bytes)
       mbar_init(empty_bar(s), 1);                // MMA issuer's commit
-      mbar_init(sf_full_bar(s), 1);              // this CTA's scale bytes (MXFP8)
+    }
+    for (uint32_t g = 0; g < C::SF_SLOTS; ++g) {
+      mbar_init(sf_full_bar(g), 1);    // this CTA's scale bytes landed (expect_tx)
+      mbar_init(sf_ready_bar(g), CG);  // leader: every CTA's SF warp re-tiled the slot
+      mbar_init(sf_empty_bar(g), 1);   // MMA issuer's commit after the slot's last K-tile
     }
     for (uint32_t b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);        // MMA issuer's commit after the last K-tile
@@ -271,7 +296,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
     // ==================== TMA producer: one elected thread ====================
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_last();
-      uint32_t it = 0;
+      uint32_t it = 0, gi = 0;
       bool ok = true;
       for (uint32_t t = cluster_id; t < num_tiles && ok; t += num_clusters) {
         uint32_t mb, nb;
@@ -279,6 +304,24 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
         const int32_t a_row = static_cast<int32_t>(mb * C::UMMA_M + rank * C::BLOCK_M);
         const int32_t b_row = static_cast<int32_t>(nb * C::UMMA_N + rank * C::B_ROWS);
         for (uint32_t kt = 0; kt < KT; ++kt, ++it) {
+          if constexpr (C::MX) {
+            if (kt % C::SF_GROUP == 0) {
+              // a new scale-factor slot: 4 K-tiles' scales of this CTA's A rows and
+              // of all the tile's B rows, landing on this CTA's own barrier
+              const uint32_t g = gi % C::SF_SLOTS;
+              if (!wait_bounded(sf_empty_bar(g), ((gi / C::SF_SLOTS) & 1u) ^ 1u, wd, kSiteProducerEmpty)) {
+                ok = false;
+                break;
+              }
+              const uint32_t slot = sf0 + g * C::SF_SLOT_BYTES;
+              const int32_t sx = static_cast<int32_t>((kt / C::SF_GROUP) * 16);
+              mbar_arrive_expect_tx(sf_full_bar(g), C::SF_TX);
+              tma_load_2d(slot + C::OFF_SFA_RAW, &tmSFA, sf_full_bar(g), sx, a_row, pol);
+              tma_load_2d(slot + C::OFF_SFB_RAW, &tmSFB, sf_full_bar(g), sx,
+                          static_cast<int32_t>(nb * C::UMMA_N), pol);
+              ++gi;
+            }
+          }
           const uint32_t s = it % C::STAGES;
           const uint32_t round = it / C::STAGES;
           // free barrier: the MMA that last read this slot has completed
@@ -288,15 +331,6 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
           }
           const uint32_t sb = stage0 + s * C::STAGE_BYTES;
           const int32_t kx = static_cast<int32_t>(kt * C::BK);
-          if constexpr (C::MX) {
-            // scale bytes (4 K-tiles per 16-byte box row) land on this CTA's own
-            // barrier, where its scale-factor warp waits
-            const int32_t sx = static_cast<int32_t>((kt / 4) * 16);
-            const int32_t sfb_row = static_cast<int32_t>(nb * C::UMMA_N);   // all B rows of the tile
-            mbar_arrive_expect_tx(sf_full_bar(s), C::SF_TX);
-            tma_load_2d(sb + C::OFF_SFA_RAW, &tmSFA, sf_full_bar(s), sx, a_row, pol);
-            tma_load_2d(sb + C::OFF_SFB_RAW, &tmSFB, sf_full_bar(s), sx, sfb_row, pol);
-          }
           if constexpr (CG == 1) {
             mbar_arrive_expect_tx(full_bar(s), C::AB_TX);
             tma_load_2d(sb, &tmA, full_bar(s), kx, a_row, pol);
@@ -313,20 +347,20 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
       // Exit path after a give-up: let this CTA's issued loads land first.
       if (*abort_flag) {
         const uint32_t first = it > C::STAGES ? it - C::STAGES : 0u;
-        for (uint32_t i = first; i < it; ++i) {
-          // (MXFP8's ready barrier also counts SF-warp arrivals, which may never
-          // come after a give-up; its scale bytes have their own barrier)
-          if (leader && !C::MX)
+        if (leader)
+          for (uint32_t i = first; i < it; ++i)
             drain_wait(full_bar(i % C::STAGES), (i / C::STAGES) & 1u, wd, kSiteProducerDrain);
-          if constexpr (C::MX)
-            drain_wait(sf_full_bar(i % C::STAGES), (i / C::STAGES) & 1u, wd, kSiteProducerDrain);
+        if constexpr (C::MX) {
+          const uint32_t gfirst = gi > C::SF_SLOTS ? gi - C::SF_SLOTS : 0u;
+          for (uint32_t i = gfirst; i < gi; ++i)
+            drain_wait(sf_full_bar(i % C::SF_SLOTS), (i / C::SF_SLOTS) & 1u, wd, kSiteProducerDrain);
         }
       }
     }
   } else if (warp == 1) {
     // ==================== MMA issuer (leader CTA of the pair) ===================
     if (leader) {
-      uint32_t it = 0, j = 0;
+      uint32_t it = 0, j = 0, gi = 0;
       bool issued = false;
       for (uint32_t t = cluster_id; t < num_tiles; t += num_clusters, ++j) {
         const uint32_t b = j % C::ACC_STAGES;
@@ -339,6 +373,15 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
         for (uint32_t kt = 0; kt < KT; ++kt, ++it) {
           const uint32_t s = it % C::STAGES;
           const uint32_t round = it / C::STAGES;
+          const uint32_t g = gi % C::SF_SLOTS;
+          if constexpr (C::MX) {
+            // first K-tile of a scale-factor group: every CTA re-tiled the slot
+            if (kt % C::SF_GROUP == 0 &&
+                !warp_wait(sf_ready_bar(g), (gi / C::SF_SLOTS) & 1u, wd, kSiteMmaFull, lane)) {
+              ok = false;
+              break;
+            }
+          }
           if (!warp_wait(full_bar(s), round & 1u, wd, kSiteMmaFull, lane)) {
             ok = false;
             break;
@@ -351,10 +394,11 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
             if constexpr (C::MX) {
               const uint32_t sfa_t = tmem_base + C::SF_TMEM_COL;
               const uint32_t sfb_t = sfa_t + 4;
-              tmem_cp_32x128b_warpx4<CG>(sfa_t, smem_desc_rows16(sb + C::OFF_SFA_T));
+              const uint32_t tsrc = sf0 + g * C::SF_SLOT_BYTES + C::OFF_T + (kt % C::SF_GROUP) * C::T_PER_KT;
+              tmem_cp_32x128b_warpx4<CG>(sfa_t, smem_desc_rows16(tsrc));
 #pragma unroll
               for (uint32_t h = 0; h < C::SFB_CHUNKS; ++h)
-                tmem_cp_32x128b_warpx4<CG>(sfb_t + 4 * h, smem_desc_rows16(sb + C::OFF_SFB_T + 512 * h));
+                tmem_cp_32x128b_warpx4<CG>(sfb_t + 4 * h, smem_desc_rows16(tsrc + C::SFA_T + 512 * h));
 #pragma unroll
               for (uint32_t k = 0; k < C::K_STEPS; ++k)
                 mma_mxf8<CG>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc_mxf8(C::UMMA_M, C::UMMA_N, k, k),
@@ -366,7 +410,10 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
                 mma_bf16<CG>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kt | k) != 0u);
             }
             commit_to<CG>(empty_bar(s));   // frees the slot once these MMAs finish
+            if (C::MX && (kt % C::SF_GROUP == C::SF_GROUP - 1 || kt + 1 == KT))
+              commit_to<CG>(sf_empty_bar(g));   // the scale-factor slot too
           }
+          if (C::MX && (kt % C::SF_GROUP == C::SF_GROUP - 1 || kt + 1 == KT)) ++gi;
           issued = true;
           __syncwarp();
         }
@@ -387,28 +434,30 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
     }
   } else if (C::MX && warp == C::kSfWarp) {
     // ==================== scale-factor warp (every CTA) ===========================
-    // Re-tile this CTA's scale bytes of every K-tile into the tcgen05.cp layout
-    // and report to the leader's ready barrier (one arrival per CTA and stage).
-    uint32_t it = 0;
+    // Re-tile every landed scale-factor slot of this CTA into the tcgen05.cp
+    // layout and report to the leader's slot-ready barrier (one arrival per
+    // CTA and slot, i.e. per 4 K-tiles).
+    const uint32_t groups = (KT + C::SF_GROUP - 1) / C::SF_GROUP;
+    uint32_t gi = 0;
     bool ok = true;
     for (uint32_t t = cluster_id; t < num_tiles && ok; t += num_clusters) {
-      for (uint32_t kt = 0; kt < KT; ++kt, ++it) {
-        const uint32_t s = it % C::STAGES;
-        if (!warp_wait(sf_full_bar(s), (it / C::STAGES) & 1u, wd, kSiteSfFull, lane)) {
+      for (uint32_t q = 0; q < groups; ++q, ++gi) {
+        const uint32_t g = gi % C::SF_SLOTS;
+        if (!warp_wait(sf_full_bar(g), (gi / C::SF_SLOTS) & 1u, wd, kSiteSfFull, lane)) {
           ok = false;
           break;
         }
-        uint8_t* const sp = base_ptr + (stage0 + s * C::STAGE_BYTES - base);
-        retile_scales<1>(sp + C::OFF_SFA_RAW, sp + C::OFF_SFA_T, C::BLOCK_M, kt & 3u, lane);
-        retile_scales<C::SFB_CHUNKS>(sp + C::OFF_SFB_RAW, sp + C::OFF_SFB_T, C::SFB_ROWS, kt & 3u,
-                                     lane);
+        uint8_t* const sp = base_ptr + (sf0 + g * C::SF_SLOT_BYTES - base);
+        retile_scales<1>(sp + C::OFF_SFA_RAW, sp + C::OFF_T, C::T_PER_KT, 0, C::BLOCK_M, lane);
+        retile_scales<C::SFB_CHUNKS>(sp + C::OFF_SFB_RAW, sp + C::OFF_T, C::T_PER_KT, C::SFA_T,
+                                     C::SFB_ROWS, lane);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
           if constexpr (CG == 1)
-            mbar_arrive(full_bar(s));
+            mbar_arrive(sf_ready_bar(g));
           else
-            mbar_arrive_cluster(mapa_shared(full_bar(s), 0));
+            mbar_arrive_cluster(mapa_shared(sf_ready_bar(g), 0));
         }
       }
     }
