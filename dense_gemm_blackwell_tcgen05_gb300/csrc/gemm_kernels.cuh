@@ -77,15 +77,21 @@ struct GemmCfg {
   static constexpr uint32_t AB_TX = A_BYTES + B_BYTES;            // per CTA
   static constexpr uint32_t FULL_ARRIVALS = 1;                    // the producer's expect_tx
 
-  // MXFP8 scale factors travel in their own ring of SF_SLOTS slots, one slot
-  // per group of SF_GROUP = 4 K-tiles: one 16-byte TMA box row carries 4
-  // K-tiles' scales (4 x 4 UE8M0 bytes).  The scale-factor warp re-tiles a
-  // landed slot into one 32x16-byte chunk per 128 rows and K-tile, the
-  // layout tcgen05.cp ... 32x128b.warpx4 copies into TMEM.  Every CTA holds
-  // the scales of all UMMA_N B rows of the tile (its tensor core multiplies
-  // by all of them) and of its own 128 A rows.
+  // MXFP8 scale factors travel in two rings of their own, one slot per group
+  // of SF_GROUP = 4 K-tiles (one 16-byte TMA box row carries 4 K-tiles'
+  // scales: 4 x 4 UE8M0 bytes):
+  //   raw ring (RAW_SLOTS): the TMA boxes of this CTA's A rows and of all the
+  //     tile's B rows; freed by the scale-factor warp as soon as it re-tiled
+  //     them, so loading never waits for the tensor core;
+  //   re-tiled ring (T_SLOTS): one 32x16-byte chunk per 128 rows and K-tile,
+  //     the layout tcgen05.cp ... 32x128b.warpx4 copies into TMEM; freed by
+  //     the MMA issuer's commit after the group's last K-tile.  Its depth is
+  //     the MMA issuer's look-ahead over scale factors.
+  // Every CTA holds the scales of all UMMA_N B rows of the tile (its tensor
+  // core multiplies by all of them) and of its own 128 A rows.
   static constexpr uint32_t SF_GROUP = 4;
-  static constexpr uint32_t SF_SLOTS = 2;
+  static constexpr uint32_t RAW_SLOTS = 2;
+  static constexpr uint32_t T_SLOTS = CG == 2 ? 4 : 3;
   static constexpr uint32_t SFB_ROWS = MX ? UMMA_N : 0;
   static constexpr uint32_t SFB_CHUNKS = (SFB_ROWS + 127) / 128;
   static constexpr uint32_t SFA_RAW = MX ? BLOCK_M * 16 : 0;
@@ -93,12 +99,12 @@ struct GemmCfg {
   static constexpr uint32_t SFA_T = MX ? 512 : 0;                 // one chunk per K-tile
   static constexpr uint32_t SFB_T = SFB_CHUNKS * 512;
   static constexpr uint32_t T_PER_KT = SFA_T + SFB_T;
-  static constexpr uint32_t OFF_SFA_RAW = 0;                      // within a slot
+  static constexpr uint32_t OFF_SFA_RAW = 0;                      // within a raw slot
   static constexpr uint32_t OFF_SFB_RAW = SFA_RAW;
-  static constexpr uint32_t OFF_T = align_up_u32(SFA_RAW + SFB_RAW, 128);
-  static constexpr uint32_t SF_SLOT_BYTES = MX ? align_up_u32(OFF_T + SF_GROUP * T_PER_KT, 1024) : 0;
-  static constexpr uint32_t SF_BYTES = SF_SLOTS * SF_SLOT_BYTES;
-  static constexpr uint32_t SF_TX = SFA_RAW + SFB_RAW;            // per CTA and slot
+  static constexpr uint32_t RAW_SLOT_BYTES = MX ? align_up_u32(SFA_RAW + SFB_RAW, 1024) : 0;
+  static constexpr uint32_t T_SLOT_BYTES = MX ? align_up_u32(SF_GROUP * T_PER_KT, 1024) : 0;
+  static constexpr uint32_t SF_BYTES = RAW_SLOTS * RAW_SLOT_BYTES + T_SLOTS * T_SLOT_BYTES;
+  static constexpr uint32_t SF_TX = SFA_RAW + SFB_RAW;            // per CTA and raw slot
 
   // TMEM: ACC_STAGES accumulators of UMMA_N fp32 columns, then the scale
   // factors (MXFP8: 4 columns for A, 4 per 128 B rows).  512 = whole TMEM.
@@ -115,7 +121,7 @@ struct GemmCfg {
   static constexpr uint32_t EPI_BYTES = TMA_STORE ? 4 * EPI_BUFS * EPI_BUF_BYTES : 0;
 
   static constexpr uint32_t SMEM_LIMIT = 232448;  // 227 KB opt-in per CTA
-  static constexpr uint32_t BAR_BYTES = 256;
+  static constexpr uint32_t BAR_BYTES = 512;
   static constexpr uint32_t ALIGN_SLACK = 1024;
   static constexpr uint32_t STAGES_FIT =
       (SMEM_LIMIT - ALIGN_SLACK - BAR_BYTES - EPI_BYTES - SF_BYTES) / STAGE_BYTES;
@@ -124,7 +130,7 @@ struct GemmCfg {
   static constexpr uint32_t SMEM_BYTES =
       ALIGN_SLACK + STAGES * STAGE_BYTES + SF_BYTES + EPI_BYTES + BAR_BYTES;
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
-  static_assert((2 * STAGES + 3 * SF_SLOTS + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
+  static_assert((2 * STAGES + 2 * RAW_SLOTS + 2 * T_SLOTS + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
 };
 
 // Re-tile one slot's scale bytes for tcgen05.cp ... 32x128b.warpx4.  The raw
@@ -235,10 +241,14 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
   const auto full_bar = [&](uint32_t s) { return bar0 + 8 * s; };
   const auto empty_bar = [&](uint32_t s) { return bar0 + 8 * (C::STAGES + s); };
   constexpr uint32_t kSfBar0 = 2 * C::STAGES;
-  const auto sf_full_bar = [&](uint32_t g) { return bar0 + 8 * (kSfBar0 + g); };
-  const auto sf_ready_bar = [&](uint32_t g) { return bar0 + 8 * (kSfBar0 + C::SF_SLOTS + g); };
-  const auto sf_empty_bar = [&](uint32_t g) { return bar0 + 8 * (kSfBar0 + 2 * C::SF_SLOTS + g); };
-  constexpr uint32_t kAccBar0 = kSfBar0 + 3 * C::SF_SLOTS;
+  const auto raw_full_bar = [&](uint32_t g) { return bar0 + 8 * (kSfBar0 + g); };
+  const auto raw_empty_bar = [&](uint32_t g) { return bar0 + 8 * (kSfBar0 + C::RAW_SLOTS + g); };
+  constexpr uint32_t kTBar0 = kSfBar0 + 2 * C::RAW_SLOTS;
+  const auto t_ready_bar = [&](uint32_t g) { return bar0 + 8 * (kTBar0 + g); };
+  const auto t_empty_bar = [&](uint32_t g) { return bar0 + 8 * (kTBar0 + C::T_SLOTS + g); };
+  constexpr uint32_t kAccBar0 = kTBar0 + 2 * C::T_SLOTS;
+  const uint32_t raw0 = sf0;                                       // raw slots, then re-tiled slots
+  const uint32_t t0 = sf0 + C::RAW_SLOTS * C::RAW_SLOT_BYTES;
   const auto accf_bar = [&](uint32_t b) { return bar0 + 8 * (kAccBar0 + b); };
   const auto acce_bar = [&](uint32_t b) { return bar0 + 8 * (kAccBar0 + 2 + b); };
   const uint32_t drain_bar = bar0 + 8 * (kAccBar0 + 4);
@@ -259,10 +269,13 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
       mbar_init(full_bar(s), C::FULL_ARRIVALS);  // producer's expect_tx (+ TMA bytes)
       mbar_init(empty_bar(s), 1);                // MMA issuer's commit
     }
-    for (uint32_t g = 0; g < C::SF_SLOTS; ++g) {
-      mbar_init(sf_full_bar(g), 1);    // this CTA's scale bytes landed (expect_tx)
-      mbar_init(sf_ready_bar(g), CG);  // leader: every CTA's SF warp re-tiled the slot
-      mbar_init(sf_empty_bar(g), 1);   // MMA issuer's commit after the slot's last K-tile
+    for (uint32_t g = 0; g < C::RAW_SLOTS; ++g) {
+      mbar_init(raw_full_bar(g), 1);   // this CTA's scale bytes landed (expect_tx)
+      mbar_init(raw_empty_bar(g), 1);  // this CTA's SF warp re-tiled them
+    }
+    for (uint32_t g = 0; g < C::T_SLOTS; ++g) {
+      mbar_init(t_ready_bar(g), CG);   // leader: every CTA's SF warp filled the slot
+      mbar_init(t_empty_bar(g), 1);    // MMA issuer's commit after the group's last K-tile
     }
     for (uint32_t b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);        // MMA issuer's commit after the last K-tile
@@ -308,16 +321,17 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
             if (kt % C::SF_GROUP == 0) {
               // a new scale-factor slot: 4 K-tiles' scales of this CTA's A rows and
               // of all the tile's B rows, landing on this CTA's own barrier
-              const uint32_t g = gi % C::SF_SLOTS;
-              if (!wait_bounded(sf_empty_bar(g), ((gi / C::SF_SLOTS) & 1u) ^ 1u, wd, kSiteProducerEmpty)) {
+              const uint32_t g = gi % C::RAW_SLOTS;
+              if (!wait_bounded(raw_empty_bar(g), ((gi / C::RAW_SLOTS) & 1u) ^ 1u, wd,
+                                kSiteProducerEmpty)) {
                 ok = false;
                 break;
               }
-              const uint32_t slot = sf0 + g * C::SF_SLOT_BYTES;
+              const uint32_t slot = raw0 + g * C::RAW_SLOT_BYTES;
               const int32_t sx = static_cast<int32_t>((kt / C::SF_GROUP) * 16);
-              mbar_arrive_expect_tx(sf_full_bar(g), C::SF_TX);
-              tma_load_2d(slot + C::OFF_SFA_RAW, &tmSFA, sf_full_bar(g), sx, a_row, pol);
-              tma_load_2d(slot + C::OFF_SFB_RAW, &tmSFB, sf_full_bar(g), sx,
+              mbar_arrive_expect_tx(raw_full_bar(g), C::SF_TX);
+              tma_load_2d(slot + C::OFF_SFA_RAW, &tmSFA, raw_full_bar(g), sx, a_row, pol);
+              tma_load_2d(slot + C::OFF_SFB_RAW, &tmSFB, raw_full_bar(g), sx,
                           static_cast<int32_t>(nb * C::UMMA_N), pol);
               ++gi;
             }
@@ -351,9 +365,9 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
           for (uint32_t i = first; i < it; ++i)
             drain_wait(full_bar(i % C::STAGES), (i / C::STAGES) & 1u, wd, kSiteProducerDrain);
         if constexpr (C::MX) {
-          const uint32_t gfirst = gi > C::SF_SLOTS ? gi - C::SF_SLOTS : 0u;
+          const uint32_t gfirst = gi > C::RAW_SLOTS ? gi - C::RAW_SLOTS : 0u;
           for (uint32_t i = gfirst; i < gi; ++i)
-            drain_wait(sf_full_bar(i % C::SF_SLOTS), (i / C::SF_SLOTS) & 1u, wd, kSiteProducerDrain);
+            drain_wait(raw_full_bar(i % C::RAW_SLOTS), (i / C::RAW_SLOTS) & 1u, wd, kSiteProducerDrain);
         }
       }
     }
@@ -373,11 +387,11 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
         for (uint32_t kt = 0; kt < KT; ++kt, ++it) {
           const uint32_t s = it % C::STAGES;
           const uint32_t round = it / C::STAGES;
-          const uint32_t g = gi % C::SF_SLOTS;
+          const uint32_t g = gi % C::T_SLOTS;
           if constexpr (C::MX) {
-            // first K-tile of a scale-factor group: every CTA re-tiled the slot
+            // first K-tile of a scale-factor group: every CTA filled the slot
             if (kt % C::SF_GROUP == 0 &&
-                !warp_wait(sf_ready_bar(g), (gi / C::SF_SLOTS) & 1u, wd, kSiteMmaFull, lane)) {
+                !warp_wait(t_ready_bar(g), (gi / C::T_SLOTS) & 1u, wd, kSiteMmaFull, lane)) {
               ok = false;
               break;
             }
@@ -394,7 +408,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
             if constexpr (C::MX) {
               const uint32_t sfa_t = tmem_base + C::SF_TMEM_COL;
               const uint32_t sfb_t = sfa_t + 4;
-              const uint32_t tsrc = sf0 + g * C::SF_SLOT_BYTES + C::OFF_T + (kt % C::SF_GROUP) * C::T_PER_KT;
+              const uint32_t tsrc = t0 + g * C::T_SLOT_BYTES + (kt % C::SF_GROUP) * C::T_PER_KT;
               tmem_cp_32x128b_warpx4<CG>(sfa_t, smem_desc_rows16(tsrc));
 #pragma unroll
               for (uint32_t h = 0; h < C::SFB_CHUNKS; ++h)
@@ -411,7 +425,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
             }
             commit_to<CG>(empty_bar(s));   // frees the slot once these MMAs finish
             if (C::MX && (kt % C::SF_GROUP == C::SF_GROUP - 1 || kt + 1 == KT))
-              commit_to<CG>(sf_empty_bar(g));   // the scale-factor slot too
+              commit_to<CG>(t_empty_bar(g));   // the re-tiled scale slot too
           }
           if (C::MX && (kt % C::SF_GROUP == C::SF_GROUP - 1 || kt + 1 == KT)) ++gi;
           issued = true;
@@ -442,22 +456,28 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
     bool ok = true;
     for (uint32_t t = cluster_id; t < num_tiles && ok; t += num_clusters) {
       for (uint32_t q = 0; q < groups; ++q, ++gi) {
-        const uint32_t g = gi % C::SF_SLOTS;
-        if (!warp_wait(sf_full_bar(g), (gi / C::SF_SLOTS) & 1u, wd, kSiteSfFull, lane)) {
+        const uint32_t gr = gi % C::RAW_SLOTS;
+        const uint32_t gt = gi % C::T_SLOTS;
+        // the scale bytes have landed, and the MMAs that read this re-tiled
+        // slot last time have completed
+        if (!warp_wait(raw_full_bar(gr), (gi / C::RAW_SLOTS) & 1u, wd, kSiteSfFull, lane) ||
+            !warp_wait(t_empty_bar(gt), ((gi / C::T_SLOTS) & 1u) ^ 1u, wd, kSiteSfFull, lane)) {
           ok = false;
           break;
         }
-        uint8_t* const sp = base_ptr + (sf0 + g * C::SF_SLOT_BYTES - base);
-        retile_scales<1>(sp + C::OFF_SFA_RAW, sp + C::OFF_T, C::T_PER_KT, 0, C::BLOCK_M, lane);
-        retile_scales<C::SFB_CHUNKS>(sp + C::OFF_SFB_RAW, sp + C::OFF_T, C::T_PER_KT, C::SFA_T,
-                                     C::SFB_ROWS, lane);
+        const uint8_t* const rp = base_ptr + (raw0 + gr * C::RAW_SLOT_BYTES - base);
+        uint8_t* const tp = base_ptr + (t0 + gt * C::T_SLOT_BYTES - base);
+        retile_scales<1>(rp + C::OFF_SFA_RAW, tp, C::T_PER_KT, 0, C::BLOCK_M, lane);
+        retile_scales<C::SFB_CHUNKS>(rp + C::OFF_SFB_RAW, tp, C::T_PER_KT, C::SFA_T, C::SFB_ROWS,
+                                     lane);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
+          mbar_arrive(raw_empty_bar(gr));      // the raw slot may be reloaded
           if constexpr (CG == 1)
-            mbar_arrive(sf_ready_bar(g));
+            mbar_arrive(t_ready_bar(gt));
           else
-            mbar_arrive_cluster(mapa_shared(sf_ready_bar(g), 0));
+            mbar_arrive_cluster(mapa_shared(t_ready_bar(gt), 0));
         }
       }
     }
