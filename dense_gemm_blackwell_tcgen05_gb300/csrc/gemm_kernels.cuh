@@ -81,8 +81,9 @@ struct GemmCfg {
   // of SF_GROUP = 4 K-tiles (one 16-byte TMA box row carries 4 K-tiles'
   // scales: 4 x 4 UE8M0 bytes):
   //   raw ring (RAW_SLOTS): the TMA boxes of this CTA's A rows and of all the
-  //     tile's B rows; freed by the scale-factor warp as soon as it re-tiled
-  //     them, so loading never waits for the tensor core;
+  //     tile's B rows.  The scale-factor warp loads them itself and reloads a
+  //     slot as soon as it has re-tiled it, so scale bytes run ahead of the
+  //     operand ring instead of arriving with it;
   //   re-tiled ring (T_SLOTS): one 32x16-byte chunk per 128 rows and K-tile,
   //     the layout tcgen05.cp ... 32x128b.warpx4 copies into TMEM; freed by
   //     the MMA issuer's commit after the group's last K-tile.  Its depth is
@@ -130,7 +131,7 @@ struct GemmCfg {
   static constexpr uint32_t SMEM_BYTES =
       ALIGN_SLACK + STAGES * STAGE_BYTES + SF_BYTES + EPI_BYTES + BAR_BYTES;
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
-  static_assert((2 * STAGES + 2 * RAW_SLOTS + 2 * T_SLOTS + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
+  static_assert((2 * STAGES + RAW_SLOTS + 2 * T_SLOTS + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
 };
 
 // Re-tile one slot's scale bytes for tcgen05.cp ... 32x128b.warpx4.  The raw
@@ -242,8 +243,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
   const auto empty_bar = [&](uint32_t s) { return bar0 + 8 * (C::STAGES + s); };
   constexpr uint32_t kSfBar0 = 2 * C::STAGES;
   const auto raw_full_bar = [&](uint32_t g) { return bar0 + 8 * (kSfBar0 + g); };
-  const auto raw_empty_bar = [&](uint32_t g) { return bar0 + 8 * (kSfBar0 + C::RAW_SLOTS + g); };
-  constexpr uint32_t kTBar0 = kSfBar0 + 2 * C::RAW_SLOTS;
+  constexpr uint32_t kTBar0 = kSfBar0 + C::RAW_SLOTS;
   const auto t_ready_bar = [&](uint32_t g) { return bar0 + 8 * (kTBar0 + g); };
   const auto t_empty_bar = [&](uint32_t g) { return bar0 + 8 * (kTBar0 + C::T_SLOTS + g); };
   constexpr uint32_t kAccBar0 = kTBar0 + 2 * C::T_SLOTS;
@@ -271,7 +271,6 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
     }
     for (uint32_t g = 0; g < C::RAW_SLOTS; ++g) {
       mbar_init(raw_full_bar(g), 1);   // this CTA's scale bytes landed (expect_tx)
-      mbar_init(raw_empty_bar(g), 1);  // this CTA's SF warp re-tiled them
     }
     for (uint32_t g = 0; g < C::T_SLOTS; ++g) {
       mbar_init(t_ready_bar(g), CG);   // leader: every CTA's SF warp filled the slot
@@ -309,7 +308,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
     // ==================== TMA producer: one elected thread ====================
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_last();
-      uint32_t it = 0, gi = 0;
+      uint32_t it = 0;
       bool ok = true;
       for (uint32_t t = cluster_id; t < num_tiles && ok; t += num_clusters) {
         uint32_t mb, nb;
@@ -317,25 +316,6 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
         const int32_t a_row = static_cast<int32_t>(mb * C::UMMA_M + rank * C::BLOCK_M);
         const int32_t b_row = static_cast<int32_t>(nb * C::UMMA_N + rank * C::B_ROWS);
         for (uint32_t kt = 0; kt < KT; ++kt, ++it) {
-          if constexpr (C::MX) {
-            if (kt % C::SF_GROUP == 0) {
-              // a new scale-factor slot: 4 K-tiles' scales of this CTA's A rows and
-              // of all the tile's B rows, landing on this CTA's own barrier
-              const uint32_t g = gi % C::RAW_SLOTS;
-              if (!wait_bounded(raw_empty_bar(g), ((gi / C::RAW_SLOTS) & 1u) ^ 1u, wd,
-                                kSiteProducerEmpty)) {
-                ok = false;
-                break;
-              }
-              const uint32_t slot = raw0 + g * C::RAW_SLOT_BYTES;
-              const int32_t sx = static_cast<int32_t>((kt / C::SF_GROUP) * 16);
-              mbar_arrive_expect_tx(raw_full_bar(g), C::SF_TX);
-              tma_load_2d(slot + C::OFF_SFA_RAW, &tmSFA, raw_full_bar(g), sx, a_row, pol);
-              tma_load_2d(slot + C::OFF_SFB_RAW, &tmSFB, raw_full_bar(g), sx,
-                          static_cast<int32_t>(nb * C::UMMA_N), pol);
-              ++gi;
-            }
-          }
           const uint32_t s = it % C::STAGES;
           const uint32_t round = it / C::STAGES;
           // free barrier: the MMA that last read this slot has completed
@@ -364,11 +344,6 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
         if (leader)
           for (uint32_t i = first; i < it; ++i)
             drain_wait(full_bar(i % C::STAGES), (i / C::STAGES) & 1u, wd, kSiteProducerDrain);
-        if constexpr (C::MX) {
-          const uint32_t gfirst = gi > C::RAW_SLOTS ? gi - C::RAW_SLOTS : 0u;
-          for (uint32_t i = gfirst; i < gi; ++i)
-            drain_wait(raw_full_bar(i % C::RAW_SLOTS), (i / C::RAW_SLOTS) & 1u, wd, kSiteProducerDrain);
-        }
       }
     }
   } else if (warp == 1) {
@@ -448,38 +423,61 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
     }
   } else if (C::MX && warp == C::kSfWarp) {
     // ==================== scale-factor warp (every CTA) ===========================
-    // Re-tile every landed scale-factor slot of this CTA into the tcgen05.cp
-    // layout and report to the leader's slot-ready barrier (one arrival per
-    // CTA and slot, i.e. per 4 K-tiles).
+    // Load this CTA's scale bytes group by group (RAW_SLOTS groups ahead),
+    // re-tile each landed group into the tcgen05.cp layout and report it to
+    // the leader's slot-ready barrier (one arrival per CTA and group).
     const uint32_t groups = (KT + C::SF_GROUP - 1) / C::SF_GROUP;
+    const uint32_t my_tiles = cluster_id < num_tiles ? (num_tiles - cluster_id + num_clusters - 1) / num_clusters : 0u;
+    const uint32_t total = my_tiles * groups;
+    const uint64_t pol = l2_policy_evict_last();
+    // group gi -> its TMA loads into raw slot gi % RAW_SLOTS (lane 0 only)
+    const auto load_group = [&](uint32_t gi) {
+      const uint32_t t = cluster_id + (gi / groups) * num_clusters;
+      const uint32_t q = gi % groups;
+      uint32_t mb, nb;
+      tile_coords(t, args.num_m_blocks, args.num_n_blocks, args.group_m, mb, nb);
+      const uint32_t g = gi % C::RAW_SLOTS;
+      const uint32_t slot = raw0 + g * C::RAW_SLOT_BYTES;
+      const int32_t sx = static_cast<int32_t>(q * 16);
+      mbar_arrive_expect_tx(raw_full_bar(g), C::SF_TX);
+      tma_load_2d(slot + C::OFF_SFA_RAW, &tmSFA, raw_full_bar(g), sx,
+                  static_cast<int32_t>(mb * C::UMMA_M + rank * C::BLOCK_M), pol);
+      tma_load_2d(slot + C::OFF_SFB_RAW, &tmSFB, raw_full_bar(g), sx,
+                  static_cast<int32_t>(nb * C::UMMA_N), pol);
+    };
+    if (lane == 0)
+      for (uint32_t gi = 0; gi < C::RAW_SLOTS && gi < total; ++gi) load_group(gi);
+    __syncwarp();
     uint32_t gi = 0;
-    bool ok = true;
-    for (uint32_t t = cluster_id; t < num_tiles && ok; t += num_clusters) {
-      for (uint32_t q = 0; q < groups; ++q, ++gi) {
-        const uint32_t gr = gi % C::RAW_SLOTS;
-        const uint32_t gt = gi % C::T_SLOTS;
-        // the scale bytes have landed, and the MMAs that read this re-tiled
-        // slot last time have completed
-        if (!warp_wait(raw_full_bar(gr), (gi / C::RAW_SLOTS) & 1u, wd, kSiteSfFull, lane) ||
-            !warp_wait(t_empty_bar(gt), ((gi / C::T_SLOTS) & 1u) ^ 1u, wd, kSiteSfFull, lane)) {
-          ok = false;
-          break;
-        }
-        const uint8_t* const rp = base_ptr + (raw0 + gr * C::RAW_SLOT_BYTES - base);
-        uint8_t* const tp = base_ptr + (t0 + gt * C::T_SLOT_BYTES - base);
-        retile_scales<1>(rp + C::OFF_SFA_RAW, tp, C::T_PER_KT, 0, C::BLOCK_M, lane);
-        retile_scales<C::SFB_CHUNKS>(rp + C::OFF_SFB_RAW, tp, C::T_PER_KT, C::SFA_T, C::SFB_ROWS,
-                                     lane);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(raw_empty_bar(gr));      // the raw slot may be reloaded
-          if constexpr (CG == 1)
-            mbar_arrive(t_ready_bar(gt));
-          else
-            mbar_arrive_cluster(mapa_shared(t_ready_bar(gt), 0));
-        }
+    for (; gi < total; ++gi) {
+      const uint32_t gr = gi % C::RAW_SLOTS;
+      const uint32_t gt = gi % C::T_SLOTS;
+      // the scale bytes have landed, and the MMAs that read this re-tiled slot
+      // last time have completed
+      if (!warp_wait(raw_full_bar(gr), (gi / C::RAW_SLOTS) & 1u, wd, kSiteSfFull, lane) ||
+          !warp_wait(t_empty_bar(gt), ((gi / C::T_SLOTS) & 1u) ^ 1u, wd, kSiteSfFull, lane))
+        break;
+      const uint8_t* const rp = base_ptr + (raw0 + gr * C::RAW_SLOT_BYTES - base);
+      uint8_t* const tp = base_ptr + (t0 + gt * C::T_SLOT_BYTES - base);
+      retile_scales<1>(rp + C::OFF_SFA_RAW, tp, C::T_PER_KT, 0, C::BLOCK_M, lane);
+      retile_scales<C::SFB_CHUNKS>(rp + C::OFF_SFB_RAW, tp, C::T_PER_KT, C::SFA_T, C::SFB_ROWS,
+                                   lane);
+      fence_proxy_async_smem();
+      __syncwarp();   // every lane's reads of the raw slot are done
+      if (lane == 0) {
+        if constexpr (CG == 1)
+          mbar_arrive(t_ready_bar(gt));
+        else
+          mbar_arrive_cluster(mapa_shared(t_ready_bar(gt), 0));
+        if (gi + C::RAW_SLOTS < total) load_group(gi + C::RAW_SLOTS);   // refill this raw slot
       }
+      __syncwarp();
+    }
+    // Exit path after a give-up: let this warp's scale loads still in flight land.
+    if (lane == 0 && *abort_flag) {
+      const uint32_t issued = total < gi + C::RAW_SLOTS ? total : gi + C::RAW_SLOTS;
+      for (uint32_t i = gi; i < issued; ++i)
+        drain_wait(raw_full_bar(i % C::RAW_SLOTS), (i / C::RAW_SLOTS) & 1u, wd, kSiteProducerDrain);
     }
   } else if (warp >= 2 && warp < 6) {
     // ==================== epilogue: four warps, one TMEM lane quarter each =========
