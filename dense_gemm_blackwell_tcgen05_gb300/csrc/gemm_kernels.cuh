@@ -347,15 +347,17 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ==================== MMA issuer (leader CTA of the pair) ===================
-    if (leader) {
+    // ==================== MMA issuer: one thread of the leader CTA ==============
+    // A single thread waits and issues: no warp-collective steps sit between
+    // consecutive MMAs (an FP8 K-tile is only ~450 tensor cycles).
+    if (leader && lane == 0) {
       uint32_t it = 0, j = 0, gi = 0;
       bool issued = false;
       for (uint32_t t = cluster_id; t < num_tiles; t += num_clusters, ++j) {
         const uint32_t b = j % C::ACC_STAGES;
         const uint32_t around = j / C::ACC_STAGES;
         // accumulator b must have been drained by every epilogue warp
-        if (!warp_wait(acce_bar(b), (around & 1u) ^ 1u, wd, kSiteMmaAccEmpty, lane)) break;
+        if (!wait_bounded(acce_bar(b), (around & 1u) ^ 1u, wd, kSiteMmaAccEmpty)) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + b * C::UMMA_N;
         bool ok = true;
@@ -366,60 +368,56 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
           if constexpr (C::MX) {
             // first K-tile of a scale-factor group: every CTA filled the slot
             if (kt % C::SF_GROUP == 0 &&
-                !warp_wait(t_ready_bar(g), (gi / C::T_SLOTS) & 1u, wd, kSiteMmaFull, lane)) {
+                !wait_bounded(t_ready_bar(g), (gi / C::T_SLOTS) & 1u, wd, kSiteMmaFull)) {
               ok = false;
               break;
             }
           }
-          if (!warp_wait(full_bar(s), round & 1u, wd, kSiteMmaFull, lane)) {
+          if (!wait_bounded(full_bar(s), round & 1u, wd, kSiteMmaFull)) {
             ok = false;
             break;
           }
           const uint32_t sb = stage0 + s * C::STAGE_BYTES;
-          if (lane == 0) {
-            tc_fence_after_sync();
-            const uint64_t adesc = smem_desc_sw128(sb);
-            const uint64_t bdesc = smem_desc_sw128(sb + C::OFF_B);
-            if constexpr (C::MX) {
-              const uint32_t sfa_t = tmem_base + C::SF_TMEM_COL;
-              const uint32_t sfb_t = sfa_t + 4;
-              const uint32_t tsrc = t0 + g * C::T_SLOT_BYTES + (kt % C::SF_GROUP) * C::T_PER_KT;
-              tmem_cp_32x128b_warpx4<CG>(sfa_t, smem_desc_rows16(tsrc));
+          tc_fence_after_sync();
+          const uint64_t adesc = smem_desc_sw128(sb);
+          const uint64_t bdesc = smem_desc_sw128(sb + C::OFF_B);
+          if constexpr (C::MX) {
+            const uint32_t sfa_t = tmem_base + C::SF_TMEM_COL;
+            const uint32_t sfb_t = sfa_t + 4;
+            const uint32_t tsrc = t0 + g * C::T_SLOT_BYTES + (kt % C::SF_GROUP) * C::T_PER_KT;
+            tmem_cp_32x128b_warpx4<CG>(sfa_t, smem_desc_rows16(tsrc));
 #pragma unroll
-              for (uint32_t h = 0; h < C::SFB_CHUNKS; ++h)
-                tmem_cp_32x128b_warpx4<CG>(sfb_t + 4 * h, smem_desc_rows16(tsrc + C::SFA_T + 512 * h));
+            for (uint32_t h = 0; h < C::SFB_CHUNKS; ++h)
+              tmem_cp_32x128b_warpx4<CG>(sfb_t + 4 * h, smem_desc_rows16(tsrc + C::SFA_T + 512 * h));
 #pragma unroll
-              for (uint32_t k = 0; k < C::K_STEPS; ++k)
-                mma_mxf8<CG>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc_mxf8(C::UMMA_M, C::UMMA_N, k, k),
-                             sfa_t, sfb_t, (kt | k) != 0u);
-            } else {
-              constexpr uint32_t idesc = idesc_bf16(C::UMMA_M, C::UMMA_N);
+            for (uint32_t k = 0; k < C::K_STEPS; ++k)
+              mma_mxf8<CG>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc_mxf8(C::UMMA_M, C::UMMA_N, k, k),
+                           sfa_t, sfb_t, (kt | k) != 0u);
+          } else {
+            constexpr uint32_t idesc = idesc_bf16(C::UMMA_M, C::UMMA_N);
 #pragma unroll
-              for (uint32_t k = 0; k < C::K_STEPS; ++k)
-                mma_bf16<CG>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kt | k) != 0u);
-            }
-            commit_to<CG>(empty_bar(s));   // frees the slot once these MMAs finish
-            if (C::MX && (kt % C::SF_GROUP == C::SF_GROUP - 1 || kt + 1 == KT))
-              commit_to<CG>(t_empty_bar(g));   // the re-tiled scale slot too
+            for (uint32_t k = 0; k < C::K_STEPS; ++k)
+              mma_bf16<CG>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kt | k) != 0u);
           }
-          if (C::MX && (kt % C::SF_GROUP == C::SF_GROUP - 1 || kt + 1 == KT)) ++gi;
+          commit_to<CG>(empty_bar(s));   // frees the stage once these MMAs finish
+          if (C::MX && (kt % C::SF_GROUP == C::SF_GROUP - 1 || kt + 1 == KT)) {
+            commit_to<CG>(t_empty_bar(g));   // and the re-tiled scale slot
+            ++gi;
+          }
           issued = true;
-          __syncwarp();
         }
         if (!ok) break;
-        if (lane == 0) commit_to<CG>(accf_bar(b));   // accumulator b complete
-        __syncwarp();
+        commit_to<CG>(accf_bar(b));   // accumulator b complete
       }
       // Exit path: every tcgen05 op this thread issued completes before TMEM
       // is released.
-      if (lane == 0 && issued) {
+      if (issued) {
         if constexpr (CG == 1)
           tc_commit(drain_bar);
         else
           tc_commit_pair_multicast(drain_bar, 0x1);
         drain_wait(drain_bar, 0, wd, kSiteMmaDrain);
       }
-      __syncwarp();
     }
   } else if (C::MX && warp == C::kSfWarp) {
     // ==================== scale-factor warp (every CTA) ===========================
@@ -562,6 +560,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
   }
 
   // ---- teardown: every role is done with TMEM and with the peer's barriers ----
+  __syncwarp();   // reconverge the single-lane roles before the aligned barriers below
   tc_fence_before_sync();
   __syncthreads();
   if constexpr (CG == 2) cluster_sync();
