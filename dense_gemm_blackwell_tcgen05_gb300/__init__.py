@@ -22,7 +22,8 @@ __all__ = [
     "GemmError", "load", "library_path", "EXPORTED_SYMBOLS",
     "gemm_bf16", "gemm_bf16_variant", "gemm_mxfp8", "gemm_mxfp8_variant",
     "gemm_last_status", "gemm_last_status_word", "gemm_status_string", "gemm_set_watchdog_ms",
-    "gemm_kernel_plan", "gemm_last_cuda_error", "matmul_bf16", "matmul_mxfp8",
+    "gemm_kernel_plan", "gemm_last_cuda_error", "gemm_debug_stall_next_launch", "matmul_bf16",
+    "matmul_mxfp8",
 ]
 
 GEMM_OK = 0
@@ -43,7 +44,7 @@ VARIANT_DIRECT_STORE = 0x100
 EXPORTED_SYMBOLS = (
     "gemm_bf16", "gemm_bf16_variant", "gemm_mxfp8", "gemm_mxfp8_variant", "gemm_last_status",
     "gemm_last_status_word", "gemm_status_string", "gemm_set_watchdog_ms", "gemm_kernel_plan",
-    "gemm_last_cuda_error",
+    "gemm_last_cuda_error", "gemm_debug_stall_next_launch",
 )
 
 _lock = threading.Lock()
@@ -88,6 +89,8 @@ def load() -> ctypes.CDLL:
             L.gemm_last_status_word.restype = ctypes.c_uint64
             L.gemm_status_string.argtypes = [ctypes.c_int]
             L.gemm_status_string.restype = ctypes.c_char_p
+            L.gemm_debug_stall_next_launch.argtypes = [_i64]
+            L.gemm_debug_stall_next_launch.restype = ctypes.c_int
             L.gemm_last_cuda_error.argtypes = []
             L.gemm_last_cuda_error.restype = ctypes.c_int
             L.gemm_set_watchdog_ms.argtypes = [_i64]
@@ -137,6 +140,10 @@ def gemm_status_string(status: int) -> str:
 
 def gemm_last_cuda_error() -> int:
     return int(load().gemm_last_cuda_error())
+
+
+def gemm_debug_stall_next_launch(k_iteration: int) -> int:
+    return int(load().gemm_debug_stall_next_launch(k_iteration))
 
 
 def gemm_set_watchdog_ms(ms: int) -> int:

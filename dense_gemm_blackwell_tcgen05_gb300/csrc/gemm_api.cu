@@ -34,6 +34,14 @@ DeviceState g_devices[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::atomic<int64_t> g_watchdog_ms{-1};
 thread_local int t_last_cuda_error = 0;
+thread_local int64_t t_stall_next = -1;   // one-shot watchdog test hook
+
+// Consumes the calling thread's pending stall request, if any.
+uint32_t take_stall() {
+  const int64_t v = t_stall_next;
+  t_stall_next = -1;
+  return v < 0 ? 0xFFFFFFFFu : static_cast<uint32_t>(v);
+}
 
 int64_t watchdog_ms() {
   int64_t v = g_watchdog_ms.load();
@@ -195,6 +203,7 @@ int gemm_bf16_variant(int variant, const void* A, const void* B, void* D, int64_
   if (!is_device_pointer(A, ctx.device) || !is_device_pointer(B, ctx.device))
     return GEMM_ERR_INVALID_ARG;
   ctx.timeout_ns = static_cast<unsigned long long>(timeout_ns_for(K));
+  p.stall_iter = take_stall();
   const bool tma_store = tma_store_ok(D, N, ldd, direct);
   switch (base) {
     case GEMM_VARIANT_SYNC:
@@ -253,6 +262,7 @@ int gemm_mxfp8_variant(int variant, const void* A, const void* B, const void* SF
       !is_device_pointer(SFA, ctx.device) || !is_device_pointer(SFB, ctx.device))
     return GEMM_ERR_INVALID_ARG;
   ctx.timeout_ns = static_cast<unsigned long long>(timeout_ns_for(K));
+  p.stall_iter = take_stall();
   // The automatic MXFP8 choice is the single-CTA kernel with the masked-store
   // epilogue: without TMA-store staging it keeps four operand stages, which
   // measures faster than three stages with TMA stores.
@@ -319,6 +329,12 @@ const char* gemm_status_string(int status) {
 }
 
 int gemm_last_cuda_error(void) { return t_last_cuda_error; }
+
+int gemm_debug_stall_next_launch(int64_t k_iteration) {
+  if (k_iteration < 0 || k_iteration >= 0xFFFFFFFFll) return GEMM_ERR_INVALID_ARG;
+  t_stall_next = k_iteration;
+  return GEMM_OK;
+}
 
 int64_t gemm_set_watchdog_ms(int64_t ms) {
   const int64_t old = watchdog_ms();

@@ -17,6 +17,7 @@ struct Problem {
   const void* SFA;
   const void* SFB;
   void* D;
+  uint32_t stall_iter = 0xFFFFFFFFu;   // watchdog test hook (see gemm_debug_stall_next_launch)
 };
 
 struct LaunchCtx {

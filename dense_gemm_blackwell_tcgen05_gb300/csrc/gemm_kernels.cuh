@@ -37,6 +37,8 @@ struct GemmArgs {
   uint64_t ldd;               // D row pitch in elements
   unsigned long long* status; // device status word
   unsigned long long timeout_ns;
+  uint32_t stall_iter;        // watchdog test hook: K-tile iteration whose loads are
+                              // withheld (0xFFFFFFFF: none)
 };
 
 __host__ __device__ constexpr uint32_t align_up_u32(uint32_t x, uint32_t a) {
@@ -318,6 +320,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
         for (uint32_t kt = 0; kt < KT; ++kt, ++it) {
           const uint32_t s = it % C::STAGES;
           const uint32_t round = it / C::STAGES;
+          if (it == args.stall_iter) continue;   // watchdog test: this stage never fills
           // free barrier: the MMA that last read this slot has completed
           if (!wait_bounded(empty_bar(s), (round & 1u) ^ 1u, wd, kSiteProducerEmpty)) {
             ok = false;
@@ -343,7 +346,8 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
         const uint32_t first = it > C::STAGES ? it - C::STAGES : 0u;
         if (leader)
           for (uint32_t i = first; i < it; ++i)
-            drain_wait(full_bar(i % C::STAGES), (i / C::STAGES) & 1u, wd, kSiteProducerDrain);
+            if (i != args.stall_iter)
+              drain_wait(full_bar(i % C::STAGES), (i / C::STAGES) & 1u, wd, kSiteProducerDrain);
       }
     }
   } else if (warp == 1) {

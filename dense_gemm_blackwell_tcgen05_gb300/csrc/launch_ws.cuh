@@ -95,6 +95,7 @@ int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) 
   a.ldd = p.ldd;
   a.status = ctx.status;
   a.timeout_ns = ctx.timeout_ns;
+  a.stall_iter = p.stall_iter;
 
   const uint64_t tiles = static_cast<uint64_t>(a.num_m_blocks) * a.num_n_blocks;
   cudaLaunchConfig_t cfg = {};

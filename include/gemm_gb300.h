@@ -125,6 +125,16 @@ uint64_t gemm_last_status_word(cudaStream_t stream);
  * tensor map; 0 if none.  Diagnostic only. */
 int gemm_last_cuda_error(void);
 
+/* Test hook for the device watchdog (no counterpart on the pages: it exists to
+ * exercise the failure path without faulting a GPU).  The calling thread's NEXT
+ * persistent-kernel launch (gemm_bf16/gemm_mxfp8 variants 0-2) withholds the
+ * operand loads of the given K-tile iteration in every CTA, so the consumers'
+ * bounded waits run out: that launch then releases its TMEM, returns, leaves D
+ * undefined, and gemm_last_status() reports GEMM_ERR_TIMEOUT.  Pair it with a
+ * short gemm_set_watchdog_ms().  Returns GEMM_ERR_INVALID_ARG for a negative
+ * iteration. */
+int gemm_debug_stall_next_launch(int64_t k_iteration);
+
 /* Static text for a gemm_status_t value. */
 const char* gemm_status_string(int status);
 
