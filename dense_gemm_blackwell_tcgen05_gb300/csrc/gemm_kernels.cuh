@@ -94,7 +94,7 @@ struct GemmCfg {
   // core multiplies by all of them) and of its own 128 A rows.
   static constexpr uint32_t SF_GROUP = 4;
   static constexpr uint32_t RAW_SLOTS = 2;
-  static constexpr uint32_t T_SLOTS = CG == 2 ? 4 : 3;
+  static constexpr uint32_t T_SLOTS = CG == 2 ? 4 : 2;
   static constexpr uint32_t SFB_ROWS = MX ? UMMA_N : 0;
   static constexpr uint32_t SFB_CHUNKS = (SFB_ROWS + 127) / 128;
   static constexpr uint32_t SFA_RAW = MX ? BLOCK_M * 16 : 0;
@@ -119,9 +119,13 @@ struct GemmCfg {
   // Epilogue staging for TMA stores: per epilogue warp, two 32x64 bf16
   // buffers (32 rows of 128 bytes, 128-byte swizzled).
   static_assert(!TMA_STORE || UMMA_N % 64 == 0, "TMA-store epilogue works in 64-column chunks");
+  // The masked-store epilogue instead stages one 32x32 chunk per warp (2 KB)
+  // and writes it back row by row, lanes across columns, so its global stores
+  // are coalesced whatever the pitch.
   static constexpr uint32_t EPI_BUF_BYTES = 32 * 128;
   static constexpr uint32_t EPI_BUFS = 2;
-  static constexpr uint32_t EPI_BYTES = TMA_STORE ? 4 * EPI_BUFS * EPI_BUF_BYTES : 0;
+  static constexpr uint32_t CHUNK_BYTES = 32 * 64;
+  static constexpr uint32_t EPI_BYTES = TMA_STORE ? 4 * EPI_BUFS * EPI_BUF_BYTES : 4 * CHUNK_BYTES;
 
   static constexpr uint32_t SMEM_LIMIT = 232448;  // 227 KB opt-in per CTA
   static constexpr uint32_t BAR_BYTES = 512;
@@ -224,6 +228,53 @@ __device__ __forceinline__ void store_row32(uint16_t* D, uint64_t ldd, uint32_t 
       if (2 * i + 1 < n) dst[2 * i + 1] = static_cast<uint16_t>(p[i] >> 16);
     }
   }
+}
+
+// Masked epilogue store of a 32x32 chunk held one row per thread (thread t:
+// row row0+t, columns col0..col0+31 as fp32 bits): convert to bf16, stage in
+// the warp's 2 KB buffer (16-byte pieces XOR-swizzled by row, conflict free),
+// then write row by row with the warp spread over the columns, so each store
+// instruction covers one contiguous row segment.  Any pitch and alignment;
+// rows >= M and columns >= N are skipped.
+__device__ __forceinline__ void store_chunk32_staged(uint8_t* buf, uint16_t* D, uint64_t ldd,
+                                                     uint32_t M, uint32_t N, uint32_t row0,
+                                                     uint32_t col0, const uint32_t (&v)[32],
+                                                     uint32_t lane) {
+#pragma unroll
+  for (uint32_t j = 0; j < 4; ++j) {
+    const uint4 piece = make_uint4(
+        pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1])),
+        pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
+        pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
+        pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
+    *reinterpret_cast<uint4*>(buf + lane * 64 + ((j ^ ((lane >> 1) & 3u)) << 4)) = piece;
+  }
+  __syncwarp();
+  const uint32_t ncols = min(32u, N - col0);
+  const uint32_t nrows = row0 < M ? min(32u, M - row0) : 0u;
+  const bool vec = ncols == 32 && ((reinterpret_cast<uintptr_t>(D + col0) | (ldd * 2)) & 15) == 0;
+  if (vec) {
+    // 16 bytes per lane: lane l covers row 8*i + l/4, piece l%4
+#pragma unroll
+    for (uint32_t i = 0; i < 4; ++i) {
+      const uint32_t r = 8 * i + (lane >> 2), j = lane & 3u;
+      if (r < nrows) {
+        const uint4 piece = *reinterpret_cast<const uint4*>(buf + r * 64 + ((j ^ ((r >> 1) & 3u)) << 4));
+        *reinterpret_cast<uint4*>(D + static_cast<uint64_t>(row0 + r) * ldd + col0 + 8 * j) = piece;
+      }
+    }
+  } else {
+    // one bf16 per lane: lane l covers column l of each row
+    const uint32_t j = lane >> 3, e = lane & 7u;
+#pragma unroll 4
+    for (uint32_t r = 0; r < nrows; ++r) {
+      if (lane < ncols) {
+        const uint16_t x = *reinterpret_cast<const uint16_t*>(buf + r * 64 + ((j ^ ((r >> 1) & 3u)) << 4) + 2 * e);
+        D[static_cast<uint64_t>(row0 + r) * ldd + col0 + lane] = x;
+      }
+    }
+  }
+  __syncwarp();
 }
 
 template <int CG, Kind KIND, bool TMA_STORE>
@@ -542,8 +593,9 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
             uint32_t v[32];
             tmem_ld_32x32b_x32(t_addr + c * 32, v);
             tmem_wait_ld();
-            store_row32(static_cast<uint16_t*>(args.D), args.ldd, args.M, args.N, row0 + lane,
-                        col_base + c * 32, v);
+            store_chunk32_staged(base_ptr + (epi0 - base) + ew * C::CHUNK_BYTES,
+                                 static_cast<uint16_t*>(args.D), args.ldd, args.M, args.N, row0,
+                                 col_base + c * 32, v, lane);
           }
         }
       }
