@@ -157,10 +157,48 @@ int64_t timeout_ns_for(int64_t K) {
 
 void note_cuda_error(cudaError_t e) { t_last_cuda_error = static_cast<int>(e); }
 
+namespace {
+// Encoded tensor maps are pure functions of their arguments, so a small
+// per-thread direct-mapped cache saves the driver call on repeated shapes.
+struct MapKey {
+  const void* base;
+  uint64_t inner, rows, pitch;
+  uint32_t box_inner, box_rows;
+  int dtype, swizzle;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && inner == o.inner && rows == o.rows && pitch == o.pitch &&
+           box_inner == o.box_inner && box_rows == o.box_rows && dtype == o.dtype &&
+           swizzle == o.swizzle;
+  }
+};
+struct MapEntry {
+  bool valid = false;
+  MapKey key;
+  CUtensorMap map;
+};
+constexpr int kMapCacheSize = 64;
+thread_local MapEntry t_map_cache[kMapCacheSize];
+
+uint32_t map_slot(const MapKey& k) {
+  uint64_t h = reinterpret_cast<uintptr_t>(k.base) * 0x9E3779B97F4A7C15ull;
+  h ^= (k.inner + 31 * k.rows + 131 * k.pitch + 1009ull * k.box_inner + 9176ull * k.box_rows +
+        7ull * static_cast<uint64_t>(k.dtype) + 3ull * static_cast<uint64_t>(k.swizzle)) *
+       0xC2B2AE3D27D4EB4Full;
+  return static_cast<uint32_t>(h >> 58) % kMapCacheSize;
+}
+}  // namespace
+
 bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
                    uint64_t rows, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_rows,
                    CUtensorMapSwizzle swizzle) {
   if (g_encode == nullptr) return false;
+  const MapKey key{base, inner, rows, pitch_bytes, box_inner, box_rows, static_cast<int>(dtype),
+                   static_cast<int>(swizzle)};
+  MapEntry& slot = t_map_cache[map_slot(key)];
+  if (slot.valid && slot.key == key) {
+    *map = slot.map;
+    return true;
+  }
   const cuuint64_t dims[2] = {inner, rows};
   const cuuint64_t strides[1] = {pitch_bytes};
   const cuuint32_t box[2] = {box_inner, box_rows};
@@ -168,8 +206,14 @@ bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base
   const CUresult r = g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
                               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) t_last_cuda_error = 100000 + static_cast<int>(r);
-  return r == CUDA_SUCCESS;
+  if (r != CUDA_SUCCESS) {
+    t_last_cuda_error = 100000 + static_cast<int>(r);
+    return false;
+  }
+  slot.valid = true;
+  slot.key = key;
+  slot.map = *map;
+  return true;
 }
 
 }  // namespace gb300
