@@ -60,6 +60,10 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     for name in ("oracle_gemm_bf16", "oracle_gemm_bf16_entries",
                  "oracle_gemm_mxfp8", "oracle_gemm_mxfp8_entries"):
         getattr(L, name).restype = None
+    L.oracle_mxfp8_quantize.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _p, _i64]
+    L.oracle_mxfp8_quantize.restype = None
+    L.oracle_f64_to_e4m3_rne.argtypes = [ctypes.c_double]
+    L.oracle_f64_to_e4m3_rne.restype = ctypes.c_uint8
     return L
 
 
@@ -126,6 +130,25 @@ class Oracle:
         """Round fp64 values to bf16 (round-to-nearest-even); uint16 codes."""
         return self._map("oracle_f64_to_bf16_rne_array",
                          np.asarray(values, np.float64), np.float64, np.uint16)
+
+    def f64_to_e4m3_rne(self, values) -> np.ndarray:
+        """Round fp64 values (|v| <= 448) to E4M3 codes, ties to even."""
+        v = np.asarray(values, np.float64).ravel()
+        return np.array([self.L.oracle_f64_to_e4m3_rne(float(x)) for x in v],
+                        np.uint8).reshape(np.shape(values))
+
+    def mxfp8_quantize(self, X, K: int | None = None):
+        """MXFP8-encode float32 rows X [rows, ldx] (first K columns): returns
+        (Q uint8 [rows, K], SF uint8 [rows, ceil(K/32)])."""
+        X = _as_c(X, np.float32)
+        rows = X.shape[0]
+        K = X.shape[1] if K is None else int(K)
+        _check_2d(X, rows, K, "X")
+        nblk = (K + 31) // 32
+        Q = np.empty((rows, K), np.uint8)
+        SF = np.empty((rows, nblk), np.uint8)
+        self.L.oracle_mxfp8_quantize(_ptr(X), rows, K, X.shape[1], _ptr(Q), K, _ptr(SF), nblk)
+        return Q, SF
 
     # ----------------------------------------------------------------- GEMMs
     def gemm_bf16(self, A, B, K: int | None = None):
@@ -229,6 +252,14 @@ def ue8m0_to_f64(codes):
 
 def f64_to_bf16_rne(values):
     return default().f64_to_bf16_rne(values)
+
+
+def f64_to_e4m3_rne(values):
+    return default().f64_to_e4m3_rne(values)
+
+
+def mxfp8_quantize(X, K=None):
+    return default().mxfp8_quantize(X, K)
 
 
 def gemm_bf16(A, B, K=None):

@@ -221,3 +221,86 @@ void oracle_f64_to_bf16_rne_array(const double *in, int64_t n, uint16_t *out)
     for (int64_t t = 0; t < n; ++t)
         out[t] = oracle_f64_to_bf16_rne(in[t]);
 }
+
+/* ------------------------------------------------------ MXFP8 quantisation */
+
+/*
+ * Round an fp64 value to the nearest E4M3 ("e4m3fn") code, ties to even.
+ * E4M3 keeps 4 significant bits; the smallest normal exponent is -6 and
+ * below it the spacing is 2^-9; the largest finite value is 448.  Values
+ * of magnitude above 448 are outside the encoder's domain here (the
+ * quantiser below never produces them).
+ */
+uint8_t oracle_f64_to_e4m3_rne(double v)
+{
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs(v);
+    if (isnan(v))
+        return (uint8_t)(sign | 0x7F);
+    if (a == 0.0)
+        return sign;
+    int ex;
+    (void)frexp(a, &ex);
+    int lead = ex - 1;                        /* exponent of the leading bit */
+    if (lead < -6)
+        lead = -6;
+    double quantum = ldexp(1.0, lead - 3);
+    double r = rint(a / quantum) * quantum;   /* ties to even */
+    if (r == 0.0)
+        return sign;
+    /* encode r: normal if r >= 2^-6, else subnormal (exponent field 0) */
+    if (r < ldexp(1.0, -6))
+        return (uint8_t)(sign | (uint8_t)(r / ldexp(1.0, -9)));
+    int e2;
+    double m = frexp(r, &e2);                 /* r = m * 2^e2, m in [0.5, 1) */
+    int biased = (e2 - 1) + 7;
+    int mant = (int)((m * 2.0 - 1.0) * 8.0);  /* exact: r has 4 significant bits */
+    return (uint8_t)(sign | (biased << 3) | mant);
+}
+
+/*
+ * MXFP8 quantisation of float rows X [rows, K] (pitch ldx elements): for each
+ * block of 32 consecutive k (the last block may be partial), amax = the
+ * largest |x| over the block's finite values, the scale exponent e is the
+ * smallest integer with amax <= 448 * 2^e (clamped to [-127, 127]; amax = 0
+ * gives e = -127), SF[r, b] = e + 127 (UE8M0) and Q[r, k] = RNE-to-E4M3 of
+ * x * 2^-e; a NaN or infinite x encodes as E4M3 NaN with its sign.
+ */
+void oracle_mxfp8_quantize(const float *X, int64_t rows, int64_t K, int64_t ldx,
+                           uint8_t *Q, int64_t ldq, uint8_t *SF, int64_t ldsf)
+{
+    int64_t nblk = (K + 31) / 32;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t b = 0; b < nblk; ++b) {
+            int64_t k0 = b * 32, k1 = k0 + 32 < K ? k0 + 32 : K;
+            double amax = 0.0;
+            for (int64_t k = k0; k < k1; ++k) {
+                double x = (double)X[r * ldx + k];
+                if (isfinite(x) && fabs(x) > amax)
+                    amax = fabs(x);
+            }
+            int e = -127;
+            if (amax > 0.0) {
+                /* exact search: start at the float guess, then step to the minimum */
+                e = (int)ceil(log2(amax / 448.0));
+                while (amax > ldexp(448.0, e))
+                    ++e;
+                while (e > -127 && amax <= ldexp(448.0, e - 1))
+                    --e;
+                if (e > 127)
+                    e = 127;
+                if (e < -127)
+                    e = -127;
+            }
+            SF[r * ldsf + b] = (uint8_t)(e + 127);
+            for (int64_t k = k0; k < k1; ++k) {
+                double x = (double)X[r * ldx + k];
+                if (!isfinite(x))
+                    Q[r * ldq + k] = (uint8_t)((signbit(x) ? 0x80 : 0x00) | 0x7F);
+                else
+                    Q[r * ldq + k] = oracle_f64_to_e4m3_rne(ldexp(x, -e));
+            }
+        }
+    }
+}

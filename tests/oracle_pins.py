@@ -267,6 +267,96 @@ def pin_entries_mxfp8(o):
     assert np.array_equal(De, D[rows, cols]) and np.array_equal(Se, S[rows, cols]), "mx entries"
 
 
+# ------------------------------------------------------ MXFP8 quantisation
+
+def _e4m3_table():
+    codes = np.arange(256, dtype=np.uint16).astype(np.uint8)
+    vals = torch_e4m3_f64(codes)
+    ok = ~np.isnan(vals)
+    return codes[ok], vals[ok]
+
+
+def _nearest_e4m3(x: float) -> int:
+    """Brute force: the E4M3 code nearest to x, ties to the even code, zero
+    keeping the sign of x."""
+    codes, vals = _e4m3_table()
+    d = np.abs(vals - x)
+    best = codes[d == d.min()]
+    if len(best) > 1:
+        even = [c for c in best if (c & 1) == 0]
+        best = even or list(best)
+    c = int(best[0])
+    if vals[codes == c][0] == 0.0:
+        c = 0x80 if np.signbit(x) else 0x00
+    return c
+
+
+def pin_e4m3_encode(o):
+    codes, vals = _e4m3_table()
+    got = o.f64_to_e4m3_rne(vals)
+    assert np.array_equal(got, codes), "encode(decode(c)) != c"
+    # midpoints between neighbours and random values against brute force
+    fin = np.sort(np.unique(vals[vals >= 0]))
+    mids = (fin[1:] + fin[:-1]) / 2
+    rng = np.random.default_rng(12)
+    xs = np.concatenate([mids, -mids, rng.uniform(-448, 448, 300), rng.uniform(-1e-2, 1e-2, 100)])
+    want = np.array([_nearest_e4m3(float(x)) for x in xs], np.uint8)
+    assert np.array_equal(o.f64_to_e4m3_rne(xs), want), "E4M3 rounding"
+    x32 = rng.uniform(-448, 448, 500).astype(np.float32)
+    ref = torch.from_numpy(x32).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(o.f64_to_e4m3_rne(x32.astype(np.float64)), ref), "vs torch cast"
+
+
+def _quant_inputs():
+    rng = np.random.default_rng(13)
+    X = rng.standard_normal((6, 101)).astype(np.float32)
+    X[1, :32] = 0.0                              # an all-zero block
+    X[2] *= 1e6                                  # large
+    X[3] *= 1e-7                                 # small
+    X[4, 5] = 448.0 * 8                          # amax exactly 448 * 2^3
+    X[4, 40] = np.float32(448.0 * 8 * (1 + 2 ** -20))   # just above a boundary
+    X[5, 3] = 1e-40                              # a float32 subnormal
+    return X
+
+
+def pin_quantize_definition(o):
+    X = _quant_inputs()
+    Q, SF = o.mxfp8_quantize(X)
+    K = X.shape[1]
+    for r in range(X.shape[0]):
+        for b in range((K + 31) // 32):
+            blk = X[r, 32 * b:32 * b + 32].astype(np.float64)
+            amax = np.abs(blk).max()
+            e = int(SF[r, b]) - 127
+            if amax == 0:
+                assert e == -127
+            else:
+                assert amax <= 448.0 * 2.0 ** e and amax > 448.0 * 2.0 ** (e - 1), (r, b)
+            for t, x in enumerate(blk):
+                assert Q[r, 32 * b + t] == _nearest_e4m3(float(x) * 2.0 ** -e), (r, b, t)
+
+
+def pin_quantize_vs_inputs_encoder(o):
+    """The oracle's quantiser and the torch-based input encoder are written
+    independently; on finite inputs they must agree bit for bit."""
+    import gemm_inputs as gi
+    X = _quant_inputs()
+    Q, SF = o.mxfp8_quantize(X)
+    q2, sf2 = gi.mxfp8_quantize(torch.from_numpy(X))
+    assert np.array_equal(Q, q2.numpy()) and np.array_equal(SF, sf2.numpy()[:, :SF.shape[1]])
+
+
+def pin_quantize_nonfinite(o):
+    X = np.ones((2, 40), np.float32)
+    X[0, 3] = np.nan
+    X[0, 7] = -np.inf
+    X[1, 33] = np.inf
+    Q, SF = o.mxfp8_quantize(X)
+    assert Q[0, 3] & 0x7F == 0x7F and Q[0, 7] == 0xFF and Q[1, 33] == 0x7F
+    assert SF[0, 0] == 127 - 8 and SF[1, 1] == 127 - 8      # scale from the finite 1.0s
+    assert np.all(Q[0, [0, 1, 2]] == _nearest_e4m3(2.0 ** 8))
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 
 

@@ -32,6 +32,13 @@ MUTANTS = {
     "bf16_ties_away": ("rint(x / quantum)", "round(x / quantum)"),
     "bf16_precision": ("ldexp(1.0, lead - 7)", "ldexp(1.0, lead - 8)"),
     "bf16_decode_shift": ("(uint32_t)h << 16", "(uint32_t)h << 15"),
+    "e4m3_enc_trunc": ("rint(a / quantum) * quantum;   /* ties to even */",
+                       "trunc(a / quantum) * quantum;   /* ties to even */"),
+    "e4m3_enc_min_exp": ("    if (lead < -6)\n        lead = -6;", "    if (lead < -7)\n        lead = -7;"),
+    "quant_448": ("amax <= ldexp(448.0, e - 1)", "amax <= ldexp(480.0, e - 1)"),
+    "quant_not_minimal": ("while (e > -127 && amax <= ldexp(448.0, e - 1))", "while (e > -127 && amax < ldexp(448.0, e - 2))"),
+    "quant_block_16": ("int64_t k0 = b * 32, k1 = k0 + 32 < K ? k0 + 32 : K;", "int64_t k0 = b * 32, k1 = k0 + 16 < K ? k0 + 16 : K;"),
+    "quant_scale_sign": ("oracle_f64_to_e4m3_rne(ldexp(x, -e))", "oracle_f64_to_e4m3_rne(ldexp(x, e))"),
 }
 
 
