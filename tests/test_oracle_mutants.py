@@ -36,7 +36,8 @@ MUTANTS = {
                        "trunc(a / quantum) * quantum;   /* ties to even */"),
     "e4m3_enc_min_exp": ("    if (lead < -6)\n        lead = -6;", "    if (lead < -7)\n        lead = -7;"),
     "quant_448": ("amax <= ldexp(448.0, e - 1)", "amax <= ldexp(480.0, e - 1)"),
-    "quant_not_minimal": ("while (e > -127 && amax <= ldexp(448.0, e - 1))", "while (e > -127 && amax < ldexp(448.0, e - 2))"),
+    "quant_not_minimal": ("e = (int)ceil(log2(amax / 448.0));\n                while (amax > ldexp(448.0, e))\n                    ++e;\n                while (e > -127 && amax <= ldexp(448.0, e - 1))\n                    --e;",
+                          "e = (int)ceil(log2(amax / 448.0)) + 1;\n                while (amax > ldexp(448.0, e))\n                    ++e;"),
     "quant_block_16": ("int64_t k0 = b * 32, k1 = k0 + 32 < K ? k0 + 32 : K;", "int64_t k0 = b * 32, k1 = k0 + 16 < K ? k0 + 16 : K;"),
     "quant_scale_sign": ("oracle_f64_to_e4m3_rne(ldexp(x, -e))", "oracle_f64_to_e4m3_rne(ldexp(x, e))"),
 }
