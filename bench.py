@@ -188,6 +188,8 @@ def host_operands(w, pinned: bool = True):
 
 
 def alg_bytes(w) -> int:
+    if w.kind == "quant":
+        return 4 * w.M * w.K + w.M * w.K + w.M * ((w.K + 31) // 32)
     if w.kind == "bf16":
         return 2 * (w.M * w.K + w.N * w.K + w.M * w.N)
     nblk = (w.K + 31) // 32
@@ -202,14 +204,25 @@ class Problem:
         self.w = w
         self.host = host
         self.dev = tuple(t.to(device, non_blocking=False) for t in host)
-        self.D = torch.empty(w.M, w.N, dtype=torch.bfloat16, device=device)
-        self.D_host = torch.empty(w.M, w.N, dtype=torch.bfloat16).pin_memory()
+        if w.kind == "quant":
+            pitch = max(16, ((w.K + 31) // 32 + 15) // 16 * 16)
+            self.D = torch.empty(w.M, w.K, dtype=torch.uint8, device=device)       # codes
+            self.SF = torch.zeros(w.M, pitch, dtype=torch.uint8, device=device)
+            self.D_host = torch.empty(w.M, w.K, dtype=torch.uint8).pin_memory()
+        else:
+            self.D = torch.empty(w.M, w.N, dtype=torch.bfloat16, device=device)
+            self.D_host = torch.empty(w.M, w.N, dtype=torch.bfloat16).pin_memory()
         self.variant = variant
 
     def launch(self, stream_handle: int, bufs=None) -> int:
         import dense_gemm_blackwell_tcgen05_gb300 as g
         w = self.w
         b = self.dev if bufs is None else bufs
+        if w.kind == "quant":
+            (X,) = b
+            return g.gemm_mxfp8_quantize(X.data_ptr(), w.M, w.K, X.stride(0), self.D.data_ptr(),
+                                         self.D.stride(0), self.SF.data_ptr(), self.SF.stride(0),
+                                         stream_handle)
         if w.kind == "bf16":
             A, B = b
             return g.gemm_bf16_variant(self.variant, A.data_ptr(), B.data_ptr(), self.D.data_ptr(),
@@ -236,11 +249,15 @@ def oracle_entries(w, host, n: int) -> float:
 
     import gemm_inputs as gi
     import oracle
+    ncols = w.K if w.kind == "quant" else w.N
     t = np.arange(n, dtype=np.int64)
-    r, c = t // w.N, t % w.N
+    r, c = t // ncols, t % ncols
     rows = int(r[-1]) + 1
     t0 = time.perf_counter()
-    if w.kind == "bf16":
+    if w.kind == "quant":
+        (X,) = host
+        oracle.mxfp8_quantize(X.numpy()[:rows])
+    elif w.kind == "bf16":
         A, B = host
         oracle.gemm_bf16_entries(gi.bf16_codes(A[:rows]), gi.bf16_codes(B), r, c)
     else:
@@ -253,9 +270,10 @@ def plan_oracle_sample(works, hosts, seconds: float):
     """Entries per workload so that one pass of the sample takes about `seconds`."""
     plan = []
     for w, h in zip(works, hosts):
-        probe = min(w.M * w.N, 4096)
+        total = w.M * (w.K if w.kind == "quant" else w.N)
+        probe = min(total, 4096 if w.kind != "quant" else 65536)
         t1 = max(oracle_entries(w, h, probe) / probe, 1e-9)
-        n = int(max(1, min(w.M * w.N, (seconds / len(works)) / t1)))
+        n = int(max(1, min(total, (seconds / len(works)) / t1)))
         plan.append(n)
     return plan
 
@@ -265,8 +283,17 @@ def oracle_pass(works, hosts, plan):
     flops = 0
     for w, h, n in zip(works, hosts, plan):
         secs += oracle_entries(w, h, n)
-        flops += 2 * n * w.K
+        flops += n * 5 + (n + 31) // 32 if w.kind == "quant" else 2 * n * w.K   # quantiser: bytes
     return flops, secs
+
+
+def step_unit(works):
+    """The step's amount per pass, its unit and scale: algorithmic FLOPs in
+    TFLOP/s when any GEMM is in the step, else algorithmic bytes in GB/s."""
+    flops = sum(w.flops for w in works)
+    if flops:
+        return flops, "TFLOP/s", 1e12
+    return sum(alg_bytes(w) for w in works), "GB/s", 1e9
 
 
 def sample_text(works, plan) -> str:
@@ -293,17 +320,18 @@ def run_reference(args, rank, world):
         f, s = oracle_pass(works, hosts, plan)
         flops += f
         secs += s
-    value = flops / secs / 1e12
+    _, unit, scale = step_unit(works)
+    value = flops / secs / scale
     cores = oracle.num_threads()
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "impl": "reference", "metric": METRIC, "value": value, "unit": unit,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": " + ".join(w.name for w in works), "parallelism": "none (CPU)"},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
                          "sample": sample_text(works, plan) + " per step"},
-        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -323,7 +351,7 @@ def run_ours(args, rank, world, local):
     probs = [Problem(w, h, args.variant, device) for w, h in zip(works, hosts)]
     stream = torch.cuda.current_stream(device)
     sh = stream.cuda_stream
-    step_flops = sum(w.flops for w in works)
+    step_flops, unit, scale = step_unit(works)
 
     def step():
         for p in probs:
@@ -364,7 +392,7 @@ def run_ours(args, rank, world, local):
     if st != g.GEMM_OK:
         raise g.GemmError(st, "timed region")
     elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world)
-    value = world * args.steps * step_flops / (elapsed_ms / 1e3) / 1e12
+    value = world * args.steps * step_flops / (elapsed_ms / 1e3) / scale
     kern_ms = [statistics.fmean(s.elapsed_time(e) for s, e in zip(starts[j], ends[j]))
                for j in range(len(probs))]
 
@@ -395,7 +423,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize(device)
     barrier(world)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
-    e2e_value = world * e2e_steps * step_flops / (e2e_ms / 1e3) / 1e12
+    e2e_value = world * e2e_steps * step_flops / (e2e_ms / 1e3) / scale
 
     # ---- roofline of each kernel (the first workload's kernel dominates) ----
     peaks, peak_src = load_peaks()
@@ -406,13 +434,13 @@ def run_ours(args, rank, world, local):
         tflops = w.flops / (ms / 1e3) / 1e12
         gbs = alg_bytes(w) / (ms / 1e3) / 1e9
         if w.kind == "bf16" and w.K >= 256:
-            bound, ach, pk, unit = "tensor", tflops, bf16_peak, "TFLOP/s"
+            bound, ach, pk, kunit = "tensor", tflops, bf16_peak, "TFLOP/s"
         elif w.kind == "mxfp8":
-            bound, ach, pk, unit = "tensor", tflops, bf16_peak * FP8_OVER_BF16, "TFLOP/s"
+            bound, ach, pk, kunit = "tensor", tflops, bf16_peak * FP8_OVER_BF16, "TFLOP/s"
         else:
-            bound, ach, pk, unit = "hbm", gbs, peaks["hbm_gbs"], "GB/s"
+            bound, ach, pk, kunit = "hbm", gbs, peaks["hbm_gbs"], "GB/s"
         key = f"{w.name}/variant{args.variant}"
-        kernels[w.name] = {"bound": bound, "achieved": ach, "peak": pk, "unit": unit,
+        kernels[w.name] = {"bound": bound, "achieved": ach, "peak": pk, "unit": kunit,
                            "frac": ach / pk, "traffic": stored_traffic(key),
                            "ms_per_launch": ms, "tflops": tflops, "alg_bytes": alg_bytes(w)}
     dom = max(range(len(probs)), key=lambda j: kern_ms[j])
@@ -428,12 +456,12 @@ def run_ours(args, rank, world, local):
         oracle.default()
         plan = plan_oracle_sample(works, hosts, args.cpu_seconds)
         f, s = oracle_pass(works, hosts, plan)
-        cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+        cpu = {"value": f / s / scale, "unit": unit, "cores": oracle.num_threads(),
                "kind": "oracle", "sample": sample_text(works, plan), "seconds": s}
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "+".join(sorted({"bf16" if w.kind == "bf16" else "e4m3" for w in works})) + "->f32",
@@ -444,7 +472,7 @@ def run_ours(args, rank, world, local):
             "roofline": roof,
             "kernels": kernels,
             "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
             "gpu_launches": args.steps * len(probs),
             "clocks": clk,

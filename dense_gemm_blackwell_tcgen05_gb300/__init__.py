@@ -22,8 +22,8 @@ __all__ = [
     "GemmError", "load", "library_path", "EXPORTED_SYMBOLS",
     "gemm_bf16", "gemm_bf16_variant", "gemm_mxfp8", "gemm_mxfp8_variant",
     "gemm_last_status", "gemm_last_status_word", "gemm_status_string", "gemm_set_watchdog_ms",
-    "gemm_kernel_plan", "gemm_last_cuda_error", "gemm_debug_stall_next_launch", "matmul_bf16",
-    "matmul_mxfp8",
+    "gemm_kernel_plan", "gemm_last_cuda_error", "gemm_debug_stall_next_launch",
+    "gemm_mxfp8_quantize", "quantize_mxfp8", "matmul_bf16", "matmul_mxfp8",
 ]
 
 GEMM_OK = 0
@@ -44,7 +44,7 @@ VARIANT_DIRECT_STORE = 0x100
 EXPORTED_SYMBOLS = (
     "gemm_bf16", "gemm_bf16_variant", "gemm_mxfp8", "gemm_mxfp8_variant", "gemm_last_status",
     "gemm_last_status_word", "gemm_status_string", "gemm_set_watchdog_ms", "gemm_kernel_plan",
-    "gemm_last_cuda_error", "gemm_debug_stall_next_launch",
+    "gemm_last_cuda_error", "gemm_debug_stall_next_launch", "gemm_mxfp8_quantize",
 )
 
 _lock = threading.Lock()
@@ -83,6 +83,8 @@ def load() -> ctypes.CDLL:
                                              _i64, _i64, _i64, _i64, _i64, _i64, _vp]
             for name in ("gemm_bf16", "gemm_bf16_variant", "gemm_mxfp8", "gemm_mxfp8_variant"):
                 getattr(L, name).restype = ctypes.c_int
+            L.gemm_mxfp8_quantize.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp]
+            L.gemm_mxfp8_quantize.restype = ctypes.c_int
             L.gemm_last_status.argtypes = [_vp]
             L.gemm_last_status.restype = ctypes.c_int
             L.gemm_last_status_word.argtypes = [_vp]
@@ -124,6 +126,11 @@ def gemm_mxfp8_variant(variant: int, A: int, B: int, SFA: int, SFB: int, D: int,
                        stream: int = 0) -> int:
     return load().gemm_mxfp8_variant(variant, A, B, SFA, SFB, D, M, N, K, lda, ldb, ldsfa, ldsfb,
                                      ldd, stream)
+
+
+def gemm_mxfp8_quantize(X: int, rows: int, K: int, ldx: int, Q: int, ldq: int, SF: int,
+                        ldsf: int, stream: int = 0) -> int:
+    return load().gemm_mxfp8_quantize(X, rows, K, ldx, Q, ldq, SF, ldsf, stream)
 
 
 def gemm_last_status(stream: int = 0) -> int:
@@ -216,3 +223,22 @@ def matmul_mxfp8(A, SFA, B, SFB, out=None, variant: int = VARIANT_AUTO, stream=N
     if rc != GEMM_OK:
         raise GemmError(rc, "gemm_mxfp8")
     return out
+
+
+def quantize_mxfp8(X, stream=None):
+    """MXFP8-encode a float32 CUDA tensor X [rows, K]: returns (Q uint8
+    [rows, K], SF uint8 [rows, pitch]) with the scale pitch padded to a
+    multiple of 16 bytes (the pitch gemm_mxfp8 requires), padding zeroed."""
+    import torch
+    _check_2d(X, "X")
+    if X.dtype != torch.float32:
+        raise TypeError("X must be float32")
+    rows, K = X.shape
+    pitch = max(16, ((K + 31) // 32 + 15) // 16 * 16)
+    Q = torch.empty(rows, K, dtype=torch.uint8, device=X.device)
+    SF = torch.zeros(rows, pitch, dtype=torch.uint8, device=X.device)
+    rc = gemm_mxfp8_quantize(X.data_ptr(), rows, K, X.stride(0), Q.data_ptr(), Q.stride(0),
+                             SF.data_ptr(), SF.stride(0), _stream_handle(stream))
+    if rc != GEMM_OK:
+        raise GemmError(rc, "gemm_mxfp8_quantize")
+    return Q, SF

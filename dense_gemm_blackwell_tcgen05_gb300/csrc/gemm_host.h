@@ -51,6 +51,9 @@ int launch_bf16_sync(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream
 int launch_mxf8_ws(int cg, bool tma_store, const Problem& p, const LaunchCtx& ctx,
                    cudaStream_t stream);
 int launch_zero_fill(const Problem& p, cudaStream_t stream);
+int launch_mxfp8_quantize(const float* X, uint32_t rows, uint32_t K, uint64_t ldx, uint8_t* Q,
+                          uint64_t ldq, uint8_t* SF, uint64_t ldsf, int num_sms,
+                          cudaStream_t stream);
 
 // Compile-time plans for gemm_kernel_plan().
 struct KernelPlan {

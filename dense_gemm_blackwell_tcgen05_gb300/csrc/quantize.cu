@@ -1,0 +1,138 @@
+// MXFP8 quantisation on the GPU: float32 rows -> E4M3 codes + one UE8M0 scale
+// per 32 consecutive k, the encoding the block-scaled GEMM consumes
+// (b200-tmem-lifecycle-planner, "A1 -- Case 2: block-scaled MMA": block-scaled
+// operands travel with their scale factors).  The per-block rule:
+//   amax = largest |x| over the block's finite values
+//   e    = smallest integer with amax <= 448 * 2^e, clamped to [-127, 127]
+//          (amax = 0 gives e = -127); scale byte = e + 127
+//   q    = round-to-nearest-even E4M3 of x * 2^-e (exact power-of-two scaling;
+//          |x * 2^-e| <= 448 by construction); NaN / +-Inf -> E4M3 NaN.
+// HBM-bound: 4 bytes read and ~1.03 bytes written per element.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "gemm_gb300.h"
+#include "gemm_host.h"
+
+namespace gb300 {
+namespace {
+
+struct QuantArgs {
+  const float* X;
+  uint8_t* Q;
+  uint8_t* SF;
+  uint32_t rows, K;
+  uint64_t ldx, ldq, ldsf;
+  uint32_t units_per_row;   // ceil(K / 512)
+  bool vec_in, vec_out;     // 16-byte loads / 4-byte stores are aligned everywhere
+};
+
+constexpr uint32_t kUnit = 512;   // elements per warp iteration (16 blocks of 32)
+
+// Smallest e with amax <= 448 * 2^e for a finite amax >= 0, from its bits:
+// amax = (1 + f) 2^(E-127) with 448 = 1.75 * 2^8, so e = E - 135 + (f > 0.75).
+__device__ __forceinline__ int scale_exponent(float amax) {
+  const uint32_t b = __float_as_uint(amax);
+  const int E = static_cast<int>((b >> 23) & 0xFFu);
+  int e = E - 135 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+  e = e < -127 ? -127 : e;
+  e = e > 127 ? 127 : e;
+  return e;
+}
+
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t encode_one(float x, float scale) {
+  if (!isfinite(x)) return (__float_as_uint(x) >> 24 & 0x80u) | 0x7Fu;
+  return e4m3x2(x * scale, 0.0f) & 0xFFu;
+}
+
+__global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const QuantArgs a) {
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const uint32_t warps = (gridDim.x * blockDim.x) >> 5;
+  const uint64_t units = static_cast<uint64_t>(a.rows) * a.units_per_row;
+  for (uint64_t u = warp_global; u < units; u += warps) {
+    const uint32_t row = static_cast<uint32_t>(u / a.units_per_row);
+    const uint32_t k0 = static_cast<uint32_t>(u % a.units_per_row) * kUnit;
+    const float* xr = a.X + row * a.ldx;
+    // lane l holds elements k0 + 128 j + 4 l .. +3, j = 0..3 (block 4 j + l / 8)
+    float x[4][4];
+#pragma unroll
+    for (uint32_t j = 0; j < 4; ++j) {
+      const uint32_t k = k0 + 128 * j + 4 * lane;
+      if (a.vec_in && k + 4 <= a.K) {
+        const float4 v = *reinterpret_cast<const float4*>(xr + k);
+        x[j][0] = v.x; x[j][1] = v.y; x[j][2] = v.z; x[j][3] = v.w;
+      } else {
+#pragma unroll
+        for (uint32_t t = 0; t < 4; ++t) x[j][t] = (k + t < a.K) ? xr[k + t] : 0.0f;
+      }
+    }
+#pragma unroll
+    for (uint32_t j = 0; j < 4; ++j) {
+      const uint32_t kb = k0 + 128 * j + 32 * (lane >> 3);   // first k of this lane's block
+      float m = 0.0f;
+#pragma unroll
+      for (uint32_t t = 0; t < 4; ++t) {
+        const float ax = fabsf(x[j][t]);
+        if (ax <= 3.402823466e38f && ax > m) m = ax;        // finite values only
+      }
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+      if (kb >= a.K) continue;   // whole block past K (all lanes took part in the shuffles)
+      const int e = scale_exponent(m);
+      const float scale = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);   // 2^-e, e <= 126
+      const uint32_t k = k0 + 128 * j + 4 * lane;
+      uint32_t q = 0;
+#pragma unroll
+      for (uint32_t t = 0; t < 4; ++t) q |= encode_one(x[j][t], scale) << (8 * t);
+      uint8_t* qr = a.Q + row * a.ldq;
+      if (a.vec_out && k + 4 <= a.K) {
+        *reinterpret_cast<uint32_t*>(qr + k) = q;
+      } else {
+#pragma unroll
+        for (uint32_t t = 0; t < 4; ++t)
+          if (k + t < a.K) qr[k + t] = static_cast<uint8_t>(q >> (8 * t));
+      }
+      if ((lane & 7u) == 0) a.SF[row * a.ldsf + kb / 32] = static_cast<uint8_t>(e + 127);
+    }
+  }
+}
+
+}  // namespace
+
+int launch_mxfp8_quantize(const float* X, uint32_t rows, uint32_t K, uint64_t ldx, uint8_t* Q,
+                          uint64_t ldq, uint8_t* SF, uint64_t ldsf, int num_sms,
+                          cudaStream_t stream) {
+  QuantArgs a;
+  a.X = X;
+  a.Q = Q;
+  a.SF = SF;
+  a.rows = rows;
+  a.K = K;
+  a.ldx = ldx;
+  a.ldq = ldq;
+  a.ldsf = ldsf;
+  a.units_per_row = (K + kUnit - 1) / kUnit;
+  a.vec_in = (reinterpret_cast<uintptr_t>(X) & 15u) == 0 && (ldx % 4) == 0;
+  a.vec_out = (reinterpret_cast<uintptr_t>(Q) & 3u) == 0 && (ldq % 4) == 0;
+  const uint64_t units = static_cast<uint64_t>(rows) * a.units_per_row;
+  const uint64_t want = (units + 7) / 8;                      // 8 warps per block
+  const uint64_t cap = static_cast<uint64_t>(num_sms) * 8;    // 8 blocks (64 warps) per SM
+  const unsigned blocks = static_cast<unsigned>(want < cap ? want : cap);
+  mxfp8_quantize_kernel<<<blocks, 256, 0, stream>>>(a);
+  if (const cudaError_t e = cudaGetLastError(); e != cudaSuccess) {
+    note_cuda_error(e);
+    return GEMM_ERR_LAUNCH;
+  }
+  return GEMM_OK;
+}
+
+}  // namespace gb300

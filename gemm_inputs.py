@@ -17,6 +17,8 @@ ragged_k1040           M=4099, N=2053, K=1040, N(0,1) -> bf16  2
 ragged_k8              M=4099, N=2053, K=8,    N(0,1) -> bf16  2
 square_8192            M=N=K=8192, 0.5*N(0,1) -> bf16          3
 mxfp8_8192             M=N=K=8192, N(0,1) -> MXFP8             4
+quantize_8192          [8192, 8192] float32 N(0,1) (the A       4
+                       operand above, before encoding)
 ===================== ===================================== ==================
 
 bf16 rounding is torch's float32 -> bfloat16 cast (round-to-nearest-even).
@@ -45,11 +47,11 @@ class Workload:
     seed: int
     dist: str            # "uniform" | "normal"
     scale: float = 1.0
-    kind: str = "bf16"   # "bf16" | "mxfp8"
+    kind: str = "bf16"   # "bf16" | "mxfp8" | "quant" (MXFP8 encoding of float32 rows [M, K])
 
     @property
     def flops(self) -> int:
-        return 2 * self.M * self.N * self.K
+        return 0 if self.kind == "quant" else 2 * self.M * self.N * self.K
 
 
 WORKLOADS = {
@@ -60,6 +62,7 @@ WORKLOADS = {
         Workload("ragged_k8", 4099, 2053, 8, 2, "normal"),
         Workload("square_8192", 8192, 8192, 8192, 3, "normal", 0.5),
         Workload("mxfp8_8192", 8192, 8192, 8192, 4, "normal", 1.0, "mxfp8"),
+        Workload("quantize_8192", 8192, 0, 8192, 4, "normal", 1.0, "quant"),
     ]
 }
 
@@ -135,8 +138,11 @@ def mxfp8_operands(M: int, N: int, K: int, seed: int, dist: str = "normal",
 
 
 def workload_operands(name: str):
-    """Operands of a named workload: (A, B) for bf16, (A, SFA, B, SFB) for MXFP8."""
+    """Operands of a named workload: (A, B) for bf16, (A, SFA, B, SFB) for MXFP8,
+    (X,) float32 for the quantiser (the MXFP8 workload's A operand)."""
     w = WORKLOADS[name]
+    if w.kind == "quant":
+        return (float_operands(w.M, 1, w.K, w.seed, w.dist, w.scale)[0],)
     if w.kind == "bf16":
         return bf16_operands(w.M, w.N, w.K, w.seed, w.dist, w.scale)
     return mxfp8_operands(w.M, w.N, w.K, w.seed, w.dist, w.scale)

@@ -109,6 +109,26 @@ int gemm_mxfp8_variant(int variant, const void* A, const void* B, const void* SF
                        cudaStream_t stream);
 
 /*
+ * MXFP8 quantisation on the GPU: the encoding the block-scaled GEMM consumes
+ * (b200-tmem-lifecycle-planner, "A1 -- Case 2: block-scaled MMA").
+ * X [rows, K]: float32, row pitch ldx >= K elements (any alignment).
+ * For every row and every block of 32 consecutive k (the last may be partial):
+ *   amax = largest |x| over the block's finite values;
+ *   e    = smallest integer with amax <= 448 * 2^e, clamped to [-127, 127]
+ *          (amax = 0 gives e = -127);
+ *   SF[r * ldsf + b] = e + 127 (UE8M0);
+ *   Q[r * ldq + k]   = x * 2^-e rounded to E4M3 ("e4m3fn"), nearest even;
+ *                      NaN and +-Inf encode as E4M3 NaN with their sign.
+ * Q [rows, ldq >= K] and SF [rows, ldsf >= ceil(K/32)] are caller-owned device
+ * buffers; a gemm_mxfp8 call may consume them directly (its own rules on lda
+ * and ldsf apply there).  Asynchronous on `stream`.  Errors: INVALID_ARG for
+ * negative or too-large sizes, short pitches, NULL or non-device pointers;
+ * rows == 0 or K == 0 is a no-op.
+ */
+int gemm_mxfp8_quantize(const float* X, int64_t rows, int64_t K, int64_t ldx, void* Q,
+                        int64_t ldq, void* SF, int64_t ldsf, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then returns and clears the current device's status
  * word: GEMM_OK, GEMM_ERR_TIMEOUT when a kernel's bounded barrier wait gave up
  * (the kernel released its TMEM and returned; D is undefined), or

@@ -107,3 +107,16 @@ def test_kernel_plans_fit_the_sm(mx, variant):
         assert p["cluster"] == 2 and p["tile_m"] == 256 and p["tile_n"] == (224 if mx else 256)
     if (variant & 0xFF) in (1, 2):
         assert p["stages"] >= 3
+
+
+def test_quantize_validation():
+    q = lambda **k: g.gemm_mxfp8_quantize(k.get("X", FAKE), k.get("rows", 4), k.get("K", 64),
+                                          k.get("ldx", 64), k.get("Q", FAKE), k.get("ldq", 64),
+                                          k.get("SF", FAKE), k.get("ldsf", 2), 0)
+    assert q(rows=-1) == g.GEMM_ERR_INVALID_ARG
+    assert q(K=-1) == g.GEMM_ERR_INVALID_ARG
+    assert q(ldx=63) == g.GEMM_ERR_INVALID_ARG
+    assert q(ldq=10) == g.GEMM_ERR_INVALID_ARG
+    assert q(ldsf=1) == g.GEMM_ERR_INVALID_ARG
+    assert q(X=NULL) == g.GEMM_ERR_INVALID_ARG
+    assert q(rows=0) == g.GEMM_OK and q(K=0) == g.GEMM_OK
