@@ -23,7 +23,9 @@ __all__ = [
     "gemm_bf16", "gemm_bf16_variant", "gemm_mxfp8", "gemm_mxfp8_variant",
     "gemm_last_status", "gemm_last_status_word", "gemm_status_string", "gemm_set_watchdog_ms",
     "gemm_kernel_plan", "gemm_last_cuda_error", "gemm_debug_stall_next_launch",
-    "gemm_mxfp8_quantize", "quantize_mxfp8", "matmul_bf16", "matmul_mxfp8",
+    "gemm_mxfp8_quantize", "quantize_mxfp8", "gemm_bf16_streamk", "gemm_mxfp8_streamk",
+    "gemm_streamk_workspace_bytes", "gemm_last_schedule", "streamk_workspace", "matmul_bf16",
+    "matmul_mxfp8",
 ]
 
 GEMM_OK = 0
@@ -45,6 +47,8 @@ EXPORTED_SYMBOLS = (
     "gemm_bf16", "gemm_bf16_variant", "gemm_mxfp8", "gemm_mxfp8_variant", "gemm_last_status",
     "gemm_last_status_word", "gemm_status_string", "gemm_set_watchdog_ms", "gemm_kernel_plan",
     "gemm_last_cuda_error", "gemm_debug_stall_next_launch", "gemm_mxfp8_quantize",
+    "gemm_bf16_streamk", "gemm_mxfp8_streamk", "gemm_streamk_workspace_bytes",
+    "gemm_last_schedule",
 )
 
 _lock = threading.Lock()
@@ -83,6 +87,16 @@ def load() -> ctypes.CDLL:
                                              _i64, _i64, _i64, _i64, _i64, _i64, _vp]
             for name in ("gemm_bf16", "gemm_bf16_variant", "gemm_mxfp8", "gemm_mxfp8_variant"):
                 getattr(L, name).restype = ctypes.c_int
+            L.gemm_bf16_streamk.argtypes = [ctypes.c_int, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
+                                            _i64, _i64, _vp, _i64, _vp]
+            L.gemm_bf16_streamk.restype = ctypes.c_int
+            L.gemm_mxfp8_streamk.argtypes = [ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _i64, _i64,
+                                             _i64, _i64, _i64, _i64, _i64, _i64, _vp, _i64, _vp]
+            L.gemm_mxfp8_streamk.restype = ctypes.c_int
+            L.gemm_streamk_workspace_bytes.argtypes = [ctypes.c_int, ctypes.c_int]
+            L.gemm_streamk_workspace_bytes.restype = _i64
+            L.gemm_last_schedule.argtypes = [ctypes.POINTER(_i64)]
+            L.gemm_last_schedule.restype = ctypes.c_int
             L.gemm_mxfp8_quantize.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp]
             L.gemm_mxfp8_quantize.restype = ctypes.c_int
             L.gemm_last_status.argtypes = [_vp]
@@ -126,6 +140,44 @@ def gemm_mxfp8_variant(variant: int, A: int, B: int, SFA: int, SFB: int, D: int,
                        stream: int = 0) -> int:
     return load().gemm_mxfp8_variant(variant, A, B, SFA, SFB, D, M, N, K, lda, ldb, ldsfa, ldsfb,
                                      ldd, stream)
+
+
+def gemm_bf16_streamk(variant: int, A: int, B: int, D: int, M: int, N: int, K: int, lda: int,
+                      ldb: int, ldd: int, workspace: int, workspace_bytes: int,
+                      stream: int = 0) -> int:
+    return load().gemm_bf16_streamk(variant, A, B, D, M, N, K, lda, ldb, ldd, workspace,
+                                    workspace_bytes, stream)
+
+
+def gemm_mxfp8_streamk(variant: int, A: int, B: int, SFA: int, SFB: int, D: int, M: int, N: int,
+                       K: int, lda: int, ldb: int, ldsfa: int, ldsfb: int, ldd: int,
+                       workspace: int, workspace_bytes: int, stream: int = 0) -> int:
+    return load().gemm_mxfp8_streamk(variant, A, B, SFA, SFB, D, M, N, K, lda, ldb, ldsfa, ldsfb,
+                                     ldd, workspace, workspace_bytes, stream)
+
+
+def gemm_streamk_workspace_bytes(mxfp8: bool, variant: int) -> int:
+    return int(load().gemm_streamk_workspace_bytes(int(bool(mxfp8)), variant))
+
+
+def gemm_last_schedule() -> dict:
+    """Schedule of this thread's last persistent-kernel launch."""
+    out = (ctypes.c_int64 * 5)()
+    rc = load().gemm_last_schedule(out)
+    if rc != GEMM_OK:
+        raise GemmError(rc, "gemm_last_schedule")
+    return {"clusters": out[0], "ctas_per_cluster": out[1], "dp_tiles": out[2],
+            "sk_tiles": out[3], "sk_unit": out[4]}
+
+
+def streamk_workspace(mxfp8: bool = False, variant: int = VARIANT_AUTO, device=None):
+    """A zeroed device buffer sized for the stream-K entry points (one per
+    stream: calls sharing a workspace must not overlap on the GPU)."""
+    import torch
+    n = gemm_streamk_workspace_bytes(mxfp8, variant)
+    if n < 0:
+        raise GemmError(n, "gemm_streamk_workspace_bytes")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
 
 
 def gemm_mxfp8_quantize(X: int, rows: int, K: int, ldx: int, Q: int, ldq: int, SF: int,
@@ -181,8 +233,9 @@ def _check_2d(t, name):
         raise ValueError(f"{name} must be a CUDA tensor")
 
 
-def matmul_bf16(A, B, out=None, variant: int = VARIANT_AUTO, stream=None):
-    """D = A @ B.T for bf16 CUDA tensors A [M,K], B [N,K]; returns D [M,N] bf16."""
+def matmul_bf16(A, B, out=None, variant: int = VARIANT_AUTO, stream=None, workspace=None):
+    """D = A @ B.T for bf16 CUDA tensors A [M,K], B [N,K]; returns D [M,N] bf16.
+    With `workspace` (from streamk_workspace) the stream-K schedule is used."""
     import torch
     _check_2d(A, "A")
     _check_2d(B, "B")
@@ -195,16 +248,24 @@ def matmul_bf16(A, B, out=None, variant: int = VARIANT_AUTO, stream=None):
     if out is None:
         out = torch.empty(M, N, dtype=torch.bfloat16, device=A.device)
     _check_2d(out, "out")
-    rc = gemm_bf16_variant(variant, A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K,
-                           A.stride(0), B.stride(0), out.stride(0), _stream_handle(stream))
+    if workspace is None:
+        rc = gemm_bf16_variant(variant, A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K,
+                               A.stride(0), B.stride(0), out.stride(0), _stream_handle(stream))
+    else:
+        rc = gemm_bf16_streamk(variant, A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K,
+                               A.stride(0), B.stride(0), out.stride(0), workspace.data_ptr(),
+                               workspace.numel() * workspace.element_size(),
+                               _stream_handle(stream))
     if rc != GEMM_OK:
         raise GemmError(rc, "gemm_bf16")
     return out
 
 
-def matmul_mxfp8(A, SFA, B, SFB, out=None, variant: int = VARIANT_AUTO, stream=None):
+def matmul_mxfp8(A, SFA, B, SFB, out=None, variant: int = VARIANT_AUTO, stream=None,
+                 workspace=None):
     """Block-scaled D = A @ B.T: A [M,K], B [N,K] E4M3 codes (uint8 or
-    float8_e4m3fn), SFA [M,>=ceil(K/32)], SFB [N,>=ceil(K/32)] UE8M0 bytes."""
+    float8_e4m3fn), SFA [M,>=ceil(K/32)], SFB [N,>=ceil(K/32)] UE8M0 bytes.
+    With `workspace` (from streamk_workspace) the stream-K schedule is used."""
     import torch
     for t, n in ((A, "A"), (B, "B"), (SFA, "SFA"), (SFB, "SFB")):
         _check_2d(t, n)
@@ -217,9 +278,17 @@ def matmul_mxfp8(A, SFA, B, SFB, out=None, variant: int = VARIANT_AUTO, stream=N
     if out is None:
         out = torch.empty(M, N, dtype=torch.bfloat16, device=A.device)
     _check_2d(out, "out")
-    rc = gemm_mxfp8_variant(variant, A.data_ptr(), B.data_ptr(), SFA.data_ptr(), SFB.data_ptr(),
-                            out.data_ptr(), M, N, K, A.stride(0), B.stride(0), SFA.stride(0),
-                            SFB.stride(0), out.stride(0), _stream_handle(stream))
+    if workspace is None:
+        rc = gemm_mxfp8_variant(variant, A.data_ptr(), B.data_ptr(), SFA.data_ptr(),
+                                SFB.data_ptr(), out.data_ptr(), M, N, K, A.stride(0), B.stride(0),
+                                SFA.stride(0), SFB.stride(0), out.stride(0),
+                                _stream_handle(stream))
+    else:
+        rc = gemm_mxfp8_streamk(variant, A.data_ptr(), B.data_ptr(), SFA.data_ptr(),
+                                SFB.data_ptr(), out.data_ptr(), M, N, K, A.stride(0), B.stride(0),
+                                SFA.stride(0), SFB.stride(0), out.stride(0), workspace.data_ptr(),
+                                workspace.numel() * workspace.element_size(),
+                                _stream_handle(stream))
     if rc != GEMM_OK:
         raise GemmError(rc, "gemm_mxfp8")
     return out

@@ -35,6 +35,7 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::atomic<int64_t> g_watchdog_ms{-1};
 thread_local int t_last_cuda_error = 0;
 thread_local int64_t t_stall_next = -1;   // one-shot watchdog test hook
+thread_local int64_t t_schedule[5] = {0, 0, 0, 0, 0};
 
 // Consumes the calling thread's pending stall request, if any.
 uint32_t take_stall() {
@@ -157,6 +158,15 @@ int64_t timeout_ns_for(int64_t K) {
 
 void note_cuda_error(cudaError_t e) { t_last_cuda_error = static_cast<int>(e); }
 
+void note_schedule(uint32_t clusters, uint32_t cg, uint32_t dp_tiles, uint32_t sk_tiles,
+                   uint32_t sk_unit) {
+  t_schedule[0] = clusters;
+  t_schedule[1] = cg;
+  t_schedule[2] = dp_tiles;
+  t_schedule[3] = sk_tiles;
+  t_schedule[4] = sk_unit;
+}
+
 namespace {
 // Encoded tensor maps are pure functions of their arguments, so a small
 // per-thread direct-mapped cache saves the driver call on repeated shapes.
@@ -222,8 +232,9 @@ using namespace gb300;
 
 extern "C" {
 
-int gemm_bf16_variant(int variant, const void* A, const void* B, void* D, int64_t M, int64_t N,
-                      int64_t K, int64_t lda, int64_t ldb, int64_t ldd, cudaStream_t stream) {
+static int bf16_impl(int variant, const void* A, const void* B, void* D, int64_t M, int64_t N,
+                     int64_t K, int64_t lda, int64_t ldb, int64_t ldd, void* ws, int64_t ws_bytes,
+                     cudaStream_t stream) {
   const int base = variant & 0xFF;
   const bool direct = (variant & GEMM_VARIANT_DIRECT_STORE) != 0;
   if ((variant & ~(0xFF | GEMM_VARIANT_DIRECT_STORE)) != 0 || base > GEMM_VARIANT_SYNC)
@@ -248,6 +259,10 @@ int gemm_bf16_variant(int variant, const void* A, const void* B, void* D, int64_
     return GEMM_ERR_INVALID_ARG;
   ctx.timeout_ns = static_cast<unsigned long long>(timeout_ns_for(K));
   p.stall_iter = take_stall();
+  p.workspace = ws;
+  p.workspace_bytes = ws_bytes > 0 ? static_cast<uint64_t>(ws_bytes) : 0u;
+  if (ws != nullptr && (base == GEMM_VARIANT_SYNC || !is_device_pointer(ws, ctx.device)))
+    return GEMM_ERR_INVALID_ARG;
   const bool tma_store = tma_store_ok(D, N, ldd, direct);
   switch (base) {
     case GEMM_VARIANT_SYNC:
@@ -261,15 +276,27 @@ int gemm_bf16_variant(int variant, const void* A, const void* B, void* D, int64_
   }
 }
 
+int gemm_bf16_variant(int variant, const void* A, const void* B, void* D, int64_t M, int64_t N,
+                      int64_t K, int64_t lda, int64_t ldb, int64_t ldd, cudaStream_t stream) {
+  return bf16_impl(variant, A, B, D, M, N, K, lda, ldb, ldd, nullptr, 0, stream);
+}
+
+int gemm_bf16_streamk(int variant, const void* A, const void* B, void* D, int64_t M, int64_t N,
+                      int64_t K, int64_t lda, int64_t ldb, int64_t ldd, void* workspace,
+                      int64_t workspace_bytes, cudaStream_t stream) {
+  if (workspace == nullptr) return GEMM_ERR_INVALID_ARG;
+  return bf16_impl(variant, A, B, D, M, N, K, lda, ldb, ldd, workspace, workspace_bytes, stream);
+}
+
 int gemm_bf16(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
               int64_t lda, int64_t ldb, int64_t ldd, cudaStream_t stream) {
   return gemm_bf16_variant(GEMM_VARIANT_AUTO, A, B, D, M, N, K, lda, ldb, ldd, stream);
 }
 
-int gemm_mxfp8_variant(int variant, const void* A, const void* B, const void* SFA,
-                       const void* SFB, void* D, int64_t M, int64_t N, int64_t K, int64_t lda,
-                       int64_t ldb, int64_t ldsfa, int64_t ldsfb, int64_t ldd,
-                       cudaStream_t stream) {
+static int mxfp8_impl(int variant, const void* A, const void* B, const void* SFA,
+                      const void* SFB, void* D, int64_t M, int64_t N, int64_t K, int64_t lda,
+                      int64_t ldb, int64_t ldsfa, int64_t ldsfb, int64_t ldd, void* ws,
+                      int64_t ws_bytes, cudaStream_t stream) {
   const int base = variant & 0xFF;
   const bool direct = (variant & GEMM_VARIANT_DIRECT_STORE) != 0;
   if ((variant & ~(0xFF | GEMM_VARIANT_DIRECT_STORE)) != 0 || base > GEMM_VARIANT_2CTA)
@@ -307,11 +334,45 @@ int gemm_mxfp8_variant(int variant, const void* A, const void* B, const void* SF
     return GEMM_ERR_INVALID_ARG;
   ctx.timeout_ns = static_cast<unsigned long long>(timeout_ns_for(K));
   p.stall_iter = take_stall();
+  p.workspace = ws;
+  p.workspace_bytes = ws_bytes > 0 ? static_cast<uint64_t>(ws_bytes) : 0u;
+  if (ws != nullptr && !is_device_pointer(ws, ctx.device)) return GEMM_ERR_INVALID_ARG;
   // The automatic MXFP8 choice is the single-CTA kernel with the masked-store
   // epilogue: without TMA-store staging it keeps four operand stages, which
   // measures faster than three stages with TMA stores.
   const bool tma_store = base != GEMM_VARIANT_AUTO && tma_store_ok(D, N, ldd, direct);
   return launch_mxf8_ws(base == GEMM_VARIANT_2CTA ? 2 : 1, tma_store, p, ctx, stream);
+}
+
+int gemm_mxfp8_variant(int variant, const void* A, const void* B, const void* SFA,
+                       const void* SFB, void* D, int64_t M, int64_t N, int64_t K, int64_t lda,
+                       int64_t ldb, int64_t ldsfa, int64_t ldsfb, int64_t ldd,
+                       cudaStream_t stream) {
+  return mxfp8_impl(variant, A, B, SFA, SFB, D, M, N, K, lda, ldb, ldsfa, ldsfb, ldd, nullptr, 0,
+                    stream);
+}
+
+int gemm_mxfp8_streamk(int variant, const void* A, const void* B, const void* SFA,
+                       const void* SFB, void* D, int64_t M, int64_t N, int64_t K, int64_t lda,
+                       int64_t ldb, int64_t ldsfa, int64_t ldsfb, int64_t ldd, void* workspace,
+                       int64_t workspace_bytes, cudaStream_t stream) {
+  if (workspace == nullptr) return GEMM_ERR_INVALID_ARG;
+  return mxfp8_impl(variant, A, B, SFA, SFB, D, M, N, K, lda, ldb, ldsfa, ldsfb, ldd, workspace,
+                    workspace_bytes, stream);
+}
+
+int64_t gemm_streamk_workspace_bytes(int mxfp8, int variant) {
+  LaunchCtx ctx;
+  const int rc = current_device(&ctx);
+  if (rc != GEMM_OK) return rc;
+  const int base = variant & 0xFF;
+  if (base > GEMM_VARIANT_2CTA) return GEMM_ERR_INVALID_ARG;
+  KernelPlan k;
+  const bool ok = mxfp8 ? plan_mxf8(base == GEMM_VARIANT_2CTA ? 2 : 1, false, &k)
+                        : plan_bf16(base == GEMM_VARIANT_1CTA ? 1 : 2, false, &k);
+  if (!ok) return GEMM_ERR_INVALID_ARG;
+  return static_cast<int64_t>(static_cast<uint64_t>(ctx.num_sms) *
+                              streamk_bytes_per_cta(static_cast<uint32_t>(k.tile_n)));
 }
 
 int gemm_mxfp8(const void* A, const void* B, const void* SFA, const void* SFB, void* D,
@@ -393,6 +454,12 @@ const char* gemm_status_string(int status) {
 }
 
 int gemm_last_cuda_error(void) { return t_last_cuda_error; }
+
+int gemm_last_schedule(int64_t* out) {
+  if (out == nullptr) return GEMM_ERR_INVALID_ARG;
+  for (int i = 0; i < 5; ++i) out[i] = t_schedule[i];
+  return GEMM_OK;
+}
 
 int gemm_debug_stall_next_launch(int64_t k_iteration) {
   if (k_iteration < 0 || k_iteration >= 0xFFFFFFFFll) return GEMM_ERR_INVALID_ARG;

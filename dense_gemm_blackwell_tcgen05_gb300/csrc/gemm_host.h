@@ -18,7 +18,15 @@ struct Problem {
   const void* SFB;
   void* D;
   uint32_t stall_iter = 0xFFFFFFFFu;   // watchdog test hook (see gemm_debug_stall_next_launch)
+  void* workspace = nullptr;           // stream-K partials + flags (nullptr: data-parallel only)
+  uint64_t workspace_bytes = 0;
 };
+
+// Stream-K workspace per CTA: 4 epilogue warps x 32 rows x tile_n fp32, plus
+// 4 flags; the library sizes it for every SM of the device.
+inline uint64_t streamk_bytes_per_cta(uint32_t tile_n) {
+  return 4ull * 32ull * tile_n * 4ull + 4ull * 4ull;
+}
 
 struct LaunchCtx {
   int device;
@@ -37,6 +45,9 @@ struct Maps {
 
 // Records the CUDA error behind a GEMM_ERR_LAUNCH for gemm_last_cuda_error().
 void note_cuda_error(cudaError_t e);
+// Records the calling thread's last persistent-kernel schedule (gemm_last_schedule).
+void note_schedule(uint32_t clusters, uint32_t cg, uint32_t dp_tiles, uint32_t sk_tiles,
+                   uint32_t sk_unit);
 
 // Encodes a 2-D tiled tensor map (rows of `inner` elements, pitch in bytes).
 // Returns false when the driver rejects it.

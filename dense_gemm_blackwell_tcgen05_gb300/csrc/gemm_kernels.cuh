@@ -39,7 +39,107 @@ struct GemmArgs {
   unsigned long long timeout_ns;
   uint32_t stall_iter;        // watchdog test hook: K-tile iteration whose loads are
                               // withheld (0xFFFFFFFF: none)
+  // Schedule: the first dp_tiles tiles go whole to clusters round-robin; the
+  // next sk_tiles tiles are cut into units of sk_unit K-tiles and the units
+  // are dealt out in equal contiguous ranges to all clusters (stream-K).
+  uint32_t dp_tiles;
+  uint32_t sk_tiles;
+  uint32_t sk_unit;
+  float* ws_part;             // stream-K partial accumulators, one slot per cluster
+  uint32_t* ws_flag;          // per (slot, CTA, epilogue warp) ready flags
+  uint32_t epoch;             // this launch's flag value (never 0)
 };
+
+// One piece of work for a cluster: K-tiles [k_begin, k_end) of a tile.
+//   kind 0: the whole tile;  1: the first K-range of a split tile (this
+//   cluster owns it: adds the later ranges' partials and stores D);
+//   2: a later K-range (partial accumulator goes to this cluster's slot).
+struct WorkItem {
+  uint32_t tile, k_begin, k_end, kind;
+};
+
+__device__ __forceinline__ uint64_t sk_bound(uint64_t units, uint32_t c, uint32_t G) {
+  return units * c / G;
+}
+
+// The wi-th work item of cluster c among G clusters; false past the last.
+// Every role of every CTA calls this with the same arguments, so they all
+// walk the same sequence.
+__device__ __forceinline__ bool work_item(const GemmArgs& a, uint32_t c, uint32_t G, uint32_t KT,
+                                          uint32_t wi, WorkItem& w) {
+  const uint32_t n_dp = a.dp_tiles > c ? (a.dp_tiles - c + G - 1) / G : 0u;
+  if (wi < n_dp) {
+    w.tile = c + wi * G;
+    w.k_begin = 0;
+    w.k_end = KT;
+    w.kind = 0;
+    return true;
+  }
+  if (a.sk_tiles == 0) return false;
+  const uint32_t KU = (KT + a.sk_unit - 1) / a.sk_unit;   // units per tile
+  const uint64_t U = static_cast<uint64_t>(a.sk_tiles) * KU;
+  const uint64_t u0 = sk_bound(U, c, G), u1 = sk_bound(U, c + 1, G);
+  const uint64_t j = wi - n_dp;
+  const uint64_t start = j == 0 ? u0 : (u0 / KU + j) * KU;
+  if (start >= u1) return false;
+  const uint64_t ts = start / KU;
+  const uint64_t end = u1 < (ts + 1) * KU ? u1 : (ts + 1) * KU;
+  const uint32_t ub = static_cast<uint32_t>(start - ts * KU);
+  const uint32_t ue = static_cast<uint32_t>(end - ts * KU);
+  w.tile = a.dp_tiles + static_cast<uint32_t>(ts);
+  w.k_begin = ub * a.sk_unit;
+  w.k_end = min(KT, ue * a.sk_unit);
+  w.kind = (ub == 0 && ue == KU) ? 0u : (ub == 0 ? 1u : 2u);
+  return true;
+}
+
+// Clusters whose partials an owner (kind 1 at cluster c) adds: the clusters
+// after c with non-empty unit ranges, until the tile's last unit is covered.
+// Calls f(cluster) for each.
+template <typename F>
+__device__ __forceinline__ void for_each_contributor(const GemmArgs& a, uint32_t c, uint32_t G,
+                                                     uint32_t KT, uint32_t tile, F&& f) {
+  const uint32_t KU = (KT + a.sk_unit - 1) / a.sk_unit;
+  const uint64_t U = static_cast<uint64_t>(a.sk_tiles) * KU;
+  const uint64_t tile_end = static_cast<uint64_t>(tile - a.dp_tiles + 1) * KU;
+  for (uint32_t cc = c + 1; cc < G; ++cc) {
+    const uint64_t b0 = sk_bound(U, cc, G), b1 = sk_bound(U, cc + 1, G);
+    if (b0 >= tile_end) break;
+    if (b1 > b0) f(cc);
+  }
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Bounded wait (lane 0) for a stream-K flag to reach `epoch`; warp-uniform result.
+__device__ __forceinline__ bool wait_flag(const uint32_t* f, uint32_t epoch, const Watchdog& wd,
+                                          uint32_t lane) {
+  bool ok = true;
+  if (lane == 0) {
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t n = 0;; ++n) {
+      if (ld_acquire_u32(f) == epoch) break;
+      if ((n & 31u) == 31u) {
+        if (*wd.abort_flag) { ok = false; break; }
+        if (global_timer_ns() - t0 > wd.timeout_ns) {
+          *wd.abort_flag = 1u;
+          report_error(wd.status, kDevTimeout, kSiteStreamKFlag);
+          ok = false;
+          break;
+        }
+      }
+    }
+  }
+  return __shfl_sync(0xffffffffu, ok ? 1u : 0u, 0) != 0;
+}
 
 __host__ __device__ constexpr uint32_t align_up_u32(uint32_t x, uint32_t a) {
   return (x + a - 1) / a * a;
@@ -277,6 +377,20 @@ __device__ __forceinline__ void store_chunk32_staged(uint8_t* buf, uint16_t* D, 
   __syncwarp();
 }
 
+// v[i] += the matching element of a stream-K partial chunk (read through L2:
+// another SM wrote it during this launch).
+__device__ __forceinline__ void add_partial32(uint32_t (&v)[32], const float* chunk, uint32_t lane) {
+  const float4* src = reinterpret_cast<const float4*>(chunk);
+#pragma unroll
+  for (uint32_t i4 = 0; i4 < 8; ++i4) {
+    const float4 p = __ldcg(src + i4 * 32 + lane);
+    v[4 * i4 + 0] = __float_as_uint(__uint_as_float(v[4 * i4 + 0]) + p.x);
+    v[4 * i4 + 1] = __float_as_uint(__uint_as_float(v[4 * i4 + 1]) + p.y);
+    v[4 * i4 + 2] = __float_as_uint(__uint_as_float(v[4 * i4 + 2]) + p.z);
+    v[4 * i4 + 3] = __float_as_uint(__uint_as_float(v[4 * i4 + 3]) + p.w);
+  }
+}
+
 template <int CG, Kind KIND, bool TMA_STORE>
 __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
     gemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -354,7 +468,6 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
-  const uint32_t num_tiles = args.num_m_blocks * args.num_n_blocks;
   const uint32_t KT = args.num_k_tiles;
 
   if (warp == 0) {
@@ -363,12 +476,13 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
       const uint64_t pol = l2_policy_evict_last();
       uint32_t it = 0;
       bool ok = true;
-      for (uint32_t t = cluster_id; t < num_tiles && ok; t += num_clusters) {
+      WorkItem w;
+      for (uint32_t wi = 0; ok && work_item(args, cluster_id, num_clusters, KT, wi, w); ++wi) {
         uint32_t mb, nb;
-        tile_coords(t, args.num_m_blocks, args.num_n_blocks, args.group_m, mb, nb);
+        tile_coords(w.tile, args.num_m_blocks, args.num_n_blocks, args.group_m, mb, nb);
         const int32_t a_row = static_cast<int32_t>(mb * C::UMMA_M + rank * C::BLOCK_M);
         const int32_t b_row = static_cast<int32_t>(nb * C::UMMA_N + rank * C::B_ROWS);
-        for (uint32_t kt = 0; kt < KT; ++kt, ++it) {
+        for (uint32_t kt = w.k_begin; kt < w.k_end; ++kt, ++it) {
           const uint32_t s = it % C::STAGES;
           const uint32_t round = it / C::STAGES;
           if (it == args.stall_iter) continue;   // watchdog test: this stage never fills
@@ -408,7 +522,8 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
     if (leader && lane == 0) {
       uint32_t it = 0, j = 0, gi = 0;
       bool issued = false;
-      for (uint32_t t = cluster_id; t < num_tiles; t += num_clusters, ++j) {
+      WorkItem w;
+      for (uint32_t wi = 0; work_item(args, cluster_id, num_clusters, KT, wi, w); ++wi, ++j) {
         const uint32_t b = j % C::ACC_STAGES;
         const uint32_t around = j / C::ACC_STAGES;
         // accumulator b must have been drained by every epilogue warp
@@ -416,7 +531,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + b * C::UMMA_N;
         bool ok = true;
-        for (uint32_t kt = 0; kt < KT; ++kt, ++it) {
+        for (uint32_t kt = w.k_begin; kt < w.k_end; ++kt, ++it) {
           const uint32_t s = it % C::STAGES;
           const uint32_t round = it / C::STAGES;
           const uint32_t g = gi % C::T_SLOTS;
@@ -447,15 +562,15 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
 #pragma unroll
             for (uint32_t k = 0; k < C::K_STEPS; ++k)
               mma_mxf8<CG>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc_mxf8(C::UMMA_M, C::UMMA_N, k, k),
-                           sfa_t, sfb_t, (kt | k) != 0u);
+                           sfa_t, sfb_t, (kt != w.k_begin || k != 0u));
           } else {
             constexpr uint32_t idesc = idesc_bf16(C::UMMA_M, C::UMMA_N);
 #pragma unroll
             for (uint32_t k = 0; k < C::K_STEPS; ++k)
-              mma_bf16<CG>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kt | k) != 0u);
+              mma_bf16<CG>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kt != w.k_begin || k != 0u));
           }
           commit_to<CG>(empty_bar(s));   // frees the stage once these MMAs finish
-          if (C::MX && (kt % C::SF_GROUP == C::SF_GROUP - 1 || kt + 1 == KT)) {
+          if (C::MX && (kt % C::SF_GROUP == C::SF_GROUP - 1 || kt + 1 == w.k_end)) {
             commit_to<CG>(t_empty_bar(g));   // and the re-tiled scale slot
             ++gi;
           }
@@ -478,31 +593,50 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
     // ==================== scale-factor warp (every CTA) ===========================
     // Load this CTA's scale bytes group by group (RAW_SLOTS groups ahead),
     // re-tile each landed group into the tcgen05.cp layout and report it to
-    // the leader's slot-ready barrier (one arrival per CTA and group).
-    const uint32_t groups = (KT + C::SF_GROUP - 1) / C::SF_GROUP;
-    const uint32_t my_tiles = cluster_id < num_tiles ? (num_tiles - cluster_id + num_clusters - 1) / num_clusters : 0u;
-    const uint32_t total = my_tiles * groups;
+    // the leader's slot-ready barrier (one arrival per CTA and group).  A
+    // cursor walks (work item, group) in the MMA issuer's order; K ranges
+    // start on group boundaries (stream-K units are whole groups).
+    struct GroupCursor {
+      uint32_t wi, q;
+      WorkItem w;
+      bool valid;
+    };
+    const auto cur_first = [&](GroupCursor& g) {
+      g.wi = 0;
+      g.q = 0;
+      g.valid = work_item(args, cluster_id, num_clusters, KT, 0, g.w);
+    };
+    const auto cur_next = [&](GroupCursor& g) {
+      if (!g.valid) return;
+      const uint32_t ng = (g.w.k_end - g.w.k_begin + C::SF_GROUP - 1) / C::SF_GROUP;
+      if (++g.q < ng) return;
+      g.q = 0;
+      ++g.wi;
+      g.valid = work_item(args, cluster_id, num_clusters, KT, g.wi, g.w);
+    };
     const uint64_t pol = l2_policy_evict_last();
-    // group gi -> its TMA loads into raw slot gi % RAW_SLOTS (lane 0 only)
-    const auto load_group = [&](uint32_t gi) {
-      const uint32_t t = cluster_id + (gi / groups) * num_clusters;
-      const uint32_t q = gi % groups;
+    // TMA loads of one group into raw slot gi % RAW_SLOTS (lane 0 only)
+    const auto load_group = [&](const GroupCursor& g, uint32_t gi) {
       uint32_t mb, nb;
-      tile_coords(t, args.num_m_blocks, args.num_n_blocks, args.group_m, mb, nb);
-      const uint32_t g = gi % C::RAW_SLOTS;
-      const uint32_t slot = raw0 + g * C::RAW_SLOT_BYTES;
-      const int32_t sx = static_cast<int32_t>(q * 16);
-      mbar_arrive_expect_tx(raw_full_bar(g), C::SF_TX);
-      tma_load_2d(slot + C::OFF_SFA_RAW, &tmSFA, raw_full_bar(g), sx,
+      tile_coords(g.w.tile, args.num_m_blocks, args.num_n_blocks, args.group_m, mb, nb);
+      const uint32_t r = gi % C::RAW_SLOTS;
+      const uint32_t slot = raw0 + r * C::RAW_SLOT_BYTES;
+      const int32_t sx = static_cast<int32_t>((g.w.k_begin / C::SF_GROUP + g.q) * 16);
+      mbar_arrive_expect_tx(raw_full_bar(r), C::SF_TX);
+      tma_load_2d(slot + C::OFF_SFA_RAW, &tmSFA, raw_full_bar(r), sx,
                   static_cast<int32_t>(mb * C::UMMA_M + rank * C::BLOCK_M), pol);
-      tma_load_2d(slot + C::OFF_SFB_RAW, &tmSFB, raw_full_bar(g), sx,
+      tma_load_2d(slot + C::OFF_SFB_RAW, &tmSFB, raw_full_bar(r), sx,
                   static_cast<int32_t>(nb * C::UMMA_N), pol);
     };
-    if (lane == 0)
-      for (uint32_t gi = 0; gi < C::RAW_SLOTS && gi < total; ++gi) load_group(gi);
+    GroupCursor lc, pc;   // load cursor (RAW_SLOTS ahead) and processing cursor
+    cur_first(lc);
+    cur_first(pc);
+    uint32_t issued = 0;
+    for (; issued < C::RAW_SLOTS && lc.valid; ++issued, cur_next(lc))
+      if (lane == 0) load_group(lc, issued);
     __syncwarp();
     uint32_t gi = 0;
-    for (; gi < total; ++gi) {
+    for (; pc.valid; ++gi, cur_next(pc)) {
       const uint32_t gr = gi % C::RAW_SLOTS;
       const uint32_t gt = gi % C::T_SLOTS;
       // the scale bytes have landed, and the MMAs that read this re-tiled slot
@@ -522,32 +656,66 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
           mbar_arrive(t_ready_bar(gt));
         else
           mbar_arrive_cluster(mapa_shared(t_ready_bar(gt), 0));
-        if (gi + C::RAW_SLOTS < total) load_group(gi + C::RAW_SLOTS);   // refill this raw slot
+      }
+      if (lc.valid) {   // refill this raw slot with the next group to load
+        if (lane == 0) load_group(lc, issued);
+        ++issued;
+        cur_next(lc);
       }
       __syncwarp();
     }
     // Exit path after a give-up: let this warp's scale loads still in flight land.
-    if (lane == 0 && *abort_flag) {
-      const uint32_t issued = total < gi + C::RAW_SLOTS ? total : gi + C::RAW_SLOTS;
+    if (lane == 0 && *abort_flag)
       for (uint32_t i = gi; i < issued; ++i)
         drain_wait(raw_full_bar(i % C::RAW_SLOTS), (i / C::RAW_SLOTS) & 1u, wd, kSiteProducerDrain);
-    }
   } else if (warp >= 2 && warp < 6) {
     // ==================== epilogue: four warps, one TMEM lane quarter each =========
     const uint32_t q = warp & 3u;            // TMEM lanes 32q .. 32q+31
     const uint32_t ew = warp - 2u;           // staging slot owner
     uint32_t j = 0, chunk_ctr = 0;
-    for (uint32_t t = cluster_id; t < num_tiles; t += num_clusters, ++j) {
+    bool ok = true;
+    // this warp's 32 x UMMA_N fp32 slice of a stream-K partial slot, and its flag
+    const auto part_ptr = [&](uint32_t slot) {
+      return args.ws_part + (static_cast<uint64_t>(slot * CG + rank) * 4 + q) * (32u * C::UMMA_N);
+    };
+    const auto flag_ptr = [&](uint32_t slot) { return args.ws_flag + (slot * CG + rank) * 4 + q; };
+    WorkItem w;
+    for (uint32_t wi = 0; ok && work_item(args, cluster_id, num_clusters, KT, wi, w); ++wi, ++j) {
       const uint32_t b = j % C::ACC_STAGES;
       const uint32_t around = j / C::ACC_STAGES;
       if (!warp_wait(accf_bar(b), around & 1u, wd, kSiteEpiAccFull, lane)) break;
       tc_fence_after_sync();
       uint32_t mb, nb;
-      tile_coords(t, args.num_m_blocks, args.num_n_blocks, args.group_m, mb, nb);
+      tile_coords(w.tile, args.num_m_blocks, args.num_n_blocks, args.group_m, mb, nb);
       const uint32_t row0 = mb * C::UMMA_M + rank * C::BLOCK_M + q * 32;
       const uint32_t col_base = nb * C::UMMA_N;
       const uint32_t t_addr = tmem_base + ((q * 32u) << 16) + b * C::UMMA_N;
-      if (row0 < args.M) {
+      if (w.kind == 2) {
+        // a later K-range of a split tile: park the fp32 slice in this
+        // cluster's slot (float4 index (chunk * 8 + i / 4) * 32 + lane, so each
+        // store instruction writes 512 contiguous bytes), then raise the flag
+        float* const part = part_ptr(cluster_id);
+#pragma unroll 1
+        for (uint32_t c = 0; c < C::UMMA_N / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(t_addr + c * 32, v);
+          tmem_wait_ld();
+          float4* dst = reinterpret_cast<float4*>(part + c * 1024);
+#pragma unroll
+          for (uint32_t i4 = 0; i4 < 8; ++i4)
+            dst[i4 * 32 + lane] = make_float4(__uint_as_float(v[4 * i4]), __uint_as_float(v[4 * i4 + 1]),
+                                              __uint_as_float(v[4 * i4 + 2]), __uint_as_float(v[4 * i4 + 3]));
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release_u32(flag_ptr(cluster_id), args.epoch);
+      } else {
+        if (w.kind == 1)   // the first K-range: wait for every later range's partial
+          for_each_contributor(args, cluster_id, num_clusters, KT, w.tile, [&](uint32_t cc) {
+            if (ok) ok = wait_flag(flag_ptr(cc), args.epoch, wd, lane);
+          });
+      }
+      if (w.kind != 2 && ok && row0 < args.M) {
         if constexpr (TMA_STORE) {
 #pragma unroll 1
           for (uint32_t c = 0; c < C::UMMA_N / 64; ++c) {
@@ -556,6 +724,11 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
             tmem_ld_32x32b_x32(t_addr + c * 64, v0);
             tmem_ld_32x32b_x32(t_addr + c * 64 + 32, v1);
             tmem_wait_ld();
+            if (w.kind == 1)
+              for_each_contributor(args, cluster_id, num_clusters, KT, w.tile, [&](uint32_t cc) {
+                add_partial32(v0, part_ptr(cc) + (2 * c) * 1024, lane);
+                add_partial32(v1, part_ptr(cc) + (2 * c + 1) * 1024, lane);
+              });
             const uint32_t buf = epi0 + (ew * C::EPI_BUFS + (chunk_ctr % C::EPI_BUFS)) * C::EPI_BUF_BYTES;
             if (lane == 0) bulk_wait_group_read<C::EPI_BUFS - 1>();   // this buffer's last store has read it
             __syncwarp();
@@ -593,11 +766,22 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
             uint32_t v[32];
             tmem_ld_32x32b_x32(t_addr + c * 32, v);
             tmem_wait_ld();
+            if (w.kind == 1)
+              for_each_contributor(args, cluster_id, num_clusters, KT, w.tile, [&](uint32_t cc) {
+                add_partial32(v, part_ptr(cc) + c * 1024, lane);
+              });
             store_chunk32_staged(base_ptr + (epi0 - base) + ew * C::CHUNK_BYTES,
                                  static_cast<uint16_t*>(args.D), args.ldd, args.M, args.N, row0,
                                  col_base + c * 32, v, lane);
           }
         }
+      }
+      if (w.kind == 1 && ok) {
+        // partials consumed: leave the flags at zero for the next launch
+        __syncwarp();
+        if (lane == 0)
+          for_each_contributor(args, cluster_id, num_clusters, KT, w.tile,
+                               [&](uint32_t cc) { *flag_ptr(cc) = 0u; });
       }
       // all TMEM reads of accumulator b by this warp are complete
       tc_fence_before_sync();

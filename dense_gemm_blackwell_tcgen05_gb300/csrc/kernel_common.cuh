@@ -21,6 +21,7 @@ enum WaitSite : uint32_t {
   kSiteProducerDrain = 6,   // producer draining its own TMA loads at exit
   kSiteSyncMma = 7,         // single-tile kernel waiting for its MMA
   kSiteSfFull = 8,          // scale-factor warp waiting for its scale bytes
+  kSiteStreamKFlag = 9,     // stream-K owner waiting for a partial accumulator
 };
 
 struct Watchdog {

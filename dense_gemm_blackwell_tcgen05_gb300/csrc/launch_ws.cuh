@@ -83,6 +83,7 @@ int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) 
       return GEMM_ERR_LAUNCH;
   }
 
+  static std::atomic<uint32_t> epoch_counter{0};
   GemmArgs a;
   a.M = p.M;
   a.N = p.N;
@@ -96,17 +97,47 @@ int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) 
   a.status = ctx.status;
   a.timeout_ns = ctx.timeout_ns;
   a.stall_iter = p.stall_iter;
+  a.ws_part = nullptr;
+  a.ws_flag = nullptr;
+  a.epoch = 0;
 
   const uint64_t tiles = static_cast<uint64_t>(a.num_m_blocks) * a.num_n_blocks;
+  const uint64_t resident = CG == 2 ? static_cast<uint64_t>(max_clusters[ctx.device])
+                                    : static_cast<uint64_t>(ctx.num_sms);
+  // Schedule.  Data-parallel: whole tiles round-robin over min(tiles, resident)
+  // clusters.  Stream-K (when the caller gives a workspace and the last wave
+  // would be partial): the tiles of the last partial wave plus one full wave
+  // are cut into units of sk_unit K-tiles dealt out evenly to all resident
+  // clusters, the rest stay whole.
+  a.dp_tiles = static_cast<uint32_t>(tiles);
+  a.sk_tiles = 0;
+  a.sk_unit = C::MX ? C::SF_GROUP : 1u;
+  uint64_t clusters = tiles < resident ? tiles : resident;
+  if (p.workspace != nullptr) {
+    const uint64_t need = resident * CG * streamk_bytes_per_cta(C::UMMA_N);
+    if (p.workspace_bytes < need || (reinterpret_cast<uintptr_t>(p.workspace) & 15u) != 0)
+      return GEMM_ERR_INVALID_ARG;
+    const uint64_t units_per_tile = (a.num_k_tiles + a.sk_unit - 1) / a.sk_unit;
+    const uint64_t rem = tiles % resident, waves = tiles / resident;
+    if (rem != 0 && units_per_tile >= 2) {
+      const uint64_t sk = rem + (waves >= 1 ? resident : 0);
+      a.sk_tiles = static_cast<uint32_t>(sk);
+      a.dp_tiles = static_cast<uint32_t>(tiles - sk);
+      clusters = resident;
+      a.ws_part = static_cast<float*>(p.workspace);
+      a.ws_flag = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(p.workspace) +
+                                              resident * CG * (streamk_bytes_per_cta(C::UMMA_N) - 16));
+      uint32_t e = epoch_counter.fetch_add(1) + 1;
+      if (e == 0) e = epoch_counter.fetch_add(1) + 1;
+      a.epoch = e;
+    }
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   if constexpr (CG == 2) {
-    const uint64_t clusters = tiles < static_cast<uint64_t>(max_clusters[ctx.device])
-                                  ? tiles
-                                  : static_cast<uint64_t>(max_clusters[ctx.device]);
     cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -115,10 +146,9 @@ int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   } else {
-    const uint64_t ctas = tiles < static_cast<uint64_t>(ctx.num_sms) ? tiles
-                                                                     : static_cast<uint64_t>(ctx.num_sms);
-    cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters));
   }
+  note_schedule(static_cast<uint32_t>(clusters), CG, a.dp_tiles, a.sk_tiles, a.sk_unit);
   const cudaError_t err = cudaLaunchKernelEx(&cfg, kern, maps.A, maps.B, maps.D, maps.SFA, maps.SFB, a);
   if (err != cudaSuccess) {
     note_cuda_error(err);

@@ -109,6 +109,36 @@ int gemm_mxfp8_variant(int variant, const void* A, const void* B, const void* SF
                        cudaStream_t stream);
 
 /*
+ * Stream-K schedule (the scheduler row "dynamic / stream-K scheduling" of the
+ * optimisation ladder's persistent level: "check the tail and tile order",
+ * b200-gemm-optimization-ladder, "E -- Executable steps", level 6).  Same
+ * arguments and results as gemm_bf16_variant / gemm_mxfp8_variant (variants
+ * 0, 1, 2, optionally with GEMM_VARIANT_DIRECT_STORE), plus a caller-owned
+ * device workspace.  When the tiles do not fill the last wave of resident
+ * CTAs, the tiles of that partial wave and of one full wave before it are cut
+ * along K and spread evenly over all resident CTAs; a tile's first K-range
+ * owner adds the later ranges' fp32 partials (parked in the workspace) before
+ * storing D.  Otherwise the call behaves like the data-parallel entry point.
+ * workspace: 16-byte aligned device memory of at least
+ * gemm_streamk_workspace_bytes() bytes, ZEROED ONCE before its first use
+ * (every completed call leaves its flag words zero again; after a call that
+ * ended in GEMM_ERR_TIMEOUT, zero it again).  Calls that share a workspace
+ * must not overlap on the GPU.  Errors as the data-parallel entry points,
+ * plus GEMM_ERR_INVALID_ARG for a NULL, short or misaligned workspace.
+ */
+int gemm_bf16_streamk(int variant, const void* A, const void* B, void* D, int64_t M, int64_t N,
+                      int64_t K, int64_t lda, int64_t ldb, int64_t ldd, void* workspace,
+                      int64_t workspace_bytes, cudaStream_t stream);
+int gemm_mxfp8_streamk(int variant, const void* A, const void* B, const void* SFA,
+                       const void* SFB, void* D, int64_t M, int64_t N, int64_t K, int64_t lda,
+                       int64_t ldb, int64_t ldsfa, int64_t ldsfb, int64_t ldd, void* workspace,
+                       int64_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes the stream-K entry points need on the current device for a
+ * kernel variant (mxfp8: 0 = bf16, 1 = MXFP8); negative gemm_status_t on error. */
+int64_t gemm_streamk_workspace_bytes(int mxfp8, int variant);
+
+/*
  * MXFP8 quantisation on the GPU: the encoding the block-scaled GEMM consumes
  * (b200-tmem-lifecycle-planner, "A1 -- Case 2: block-scaled MMA").
  * X [rows, K]: float32, row pitch ldx >= K elements (any alignment).
@@ -144,6 +174,13 @@ uint64_t gemm_last_status_word(cudaStream_t stream);
  * recent GEMM_ERR_LAUNCH, or 100000 + CUresult when the driver rejected a
  * tensor map; 0 if none.  Diagnostic only. */
 int gemm_last_cuda_error(void);
+
+/* Schedule of the calling thread's most recent persistent-kernel launch
+ * (diagnostic, no counterpart on the pages): out[0] clusters launched,
+ * out[1] CTAs per cluster, out[2] tiles computed whole, out[3] tiles split
+ * along K by the stream-K schedule, out[4] K-tiles per stream-K unit.  `out`
+ * holds 5 values.  Returns GEMM_OK, or GEMM_ERR_INVALID_ARG for NULL. */
+int gemm_last_schedule(int64_t* out);
 
 /* Test hook for the device watchdog (no counterpart on the pages: it exists to
  * exercise the failure path without faulting a GPU).  The calling thread's NEXT

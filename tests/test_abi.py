@@ -120,3 +120,25 @@ def test_quantize_validation():
     assert q(ldsf=1) == g.GEMM_ERR_INVALID_ARG
     assert q(X=NULL) == g.GEMM_ERR_INVALID_ARG
     assert q(rows=0) == g.GEMM_OK and q(K=0) == g.GEMM_OK
+
+
+def test_streamk_validation_without_device():
+    # a NULL workspace is refused before anything else
+    assert g.gemm_bf16_streamk(2, FAKE, FAKE, FAKE, 4, 4, 16, 16, 16, 4, NULL, 1 << 20, 0) == \
+        g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_mxfp8_streamk(1, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 4, 32, 32, 32, 16, 16, 4, NULL,
+                                1 << 20, 0) == g.GEMM_ERR_INVALID_ARG
+    # shapes are checked like the data-parallel entry points
+    assert g.gemm_bf16_streamk(2, FAKE, FAKE, FAKE, -1, 4, 16, 16, 16, 4, FAKE, 1 << 20, 0) == \
+        g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_bf16_streamk(0x40, FAKE, FAKE, FAKE, 4, 4, 16, 16, 16, 4, FAKE, 1 << 20, 0) == \
+        g.GEMM_ERR_INVALID_ARG
+    sched = g.gemm_last_schedule()
+    assert set(sched) == {"clusters", "ctas_per_cluster", "dp_tiles", "sk_tiles", "sk_unit"}
+
+
+def test_streamk_workspace_query_without_device():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert g.gemm_streamk_workspace_bytes(False, 2) == g.GEMM_ERR_UNSUPPORTED_DEVICE
