@@ -24,7 +24,8 @@ __all__ = [
     "gemm_last_status", "gemm_last_status_word", "gemm_status_string", "gemm_set_watchdog_ms",
     "gemm_kernel_plan", "gemm_last_cuda_error", "gemm_debug_stall_next_launch",
     "gemm_mxfp8_quantize", "quantize_mxfp8", "gemm_bf16_streamk", "gemm_mxfp8_streamk",
-    "gemm_streamk_workspace_bytes", "gemm_last_schedule", "streamk_workspace", "matmul_bf16",
+    "gemm_streamk_workspace_bytes", "gemm_last_schedule", "streamk_workspace",
+    "gemm_bf16_streamk_noalloc", "matmul_bf16",
     "matmul_mxfp8",
 ]
 
@@ -48,7 +49,7 @@ EXPORTED_SYMBOLS = (
     "gemm_last_status_word", "gemm_status_string", "gemm_set_watchdog_ms", "gemm_kernel_plan",
     "gemm_last_cuda_error", "gemm_debug_stall_next_launch", "gemm_mxfp8_quantize",
     "gemm_bf16_streamk", "gemm_mxfp8_streamk", "gemm_streamk_workspace_bytes",
-    "gemm_last_schedule",
+    "gemm_last_schedule", "gemm_bf16_streamk_noalloc",
 )
 
 _lock = threading.Lock()
@@ -95,6 +96,9 @@ def load() -> ctypes.CDLL:
             L.gemm_mxfp8_streamk.restype = ctypes.c_int
             L.gemm_streamk_workspace_bytes.argtypes = [ctypes.c_int, ctypes.c_int]
             L.gemm_streamk_workspace_bytes.restype = _i64
+            L.gemm_bf16_streamk_noalloc.argtypes = [ctypes.c_int, _vp, _vp, _vp, _i64, _i64, _i64,
+                                                    _i64, _i64, _i64, _vp]
+            L.gemm_bf16_streamk_noalloc.restype = ctypes.c_int
             L.gemm_last_schedule.argtypes = [ctypes.POINTER(_i64)]
             L.gemm_last_schedule.restype = ctypes.c_int
             L.gemm_mxfp8_quantize.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp]
@@ -154,6 +158,11 @@ def gemm_mxfp8_streamk(variant: int, A: int, B: int, SFA: int, SFB: int, D: int,
                        workspace: int, workspace_bytes: int, stream: int = 0) -> int:
     return load().gemm_mxfp8_streamk(variant, A, B, SFA, SFB, D, M, N, K, lda, ldb, ldsfa, ldsfb,
                                      ldd, workspace, workspace_bytes, stream)
+
+
+def gemm_bf16_streamk_noalloc(variant: int, A: int, B: int, D: int, M: int, N: int, K: int,
+                              lda: int, ldb: int, ldd: int, stream: int = 0) -> int:
+    return load().gemm_bf16_streamk_noalloc(variant, A, B, D, M, N, K, lda, ldb, ldd, stream)
 
 
 def gemm_streamk_workspace_bytes(mxfp8: bool, variant: int) -> int:

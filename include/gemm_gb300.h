@@ -134,6 +134,29 @@ int gemm_mxfp8_streamk(int variant, const void* A, const void* B, const void* SF
                        int64_t ldb, int64_t ldsfa, int64_t ldsfb, int64_t ldd, void* workspace,
                        int64_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * gemm_bf16_streamk without a caller workspace; it allocates nothing.  The
+ * pages have no counterpart: this entry point exists for callers that must
+ * not allocate device memory where they multiply -- code inside a memory
+ * allocator's own out-of-memory or defragmentation path, where an allocation
+ * would re-enter the allocator, or a serving loop that reserves its device
+ * memory at start-up and may not grow it later.  The scratch is a library-owned
+ * static device buffer of 24 MiB per device (enough for 191 resident CTAs;
+ * a GB300 runs 152).  Same arguments, results and errors as
+ * gemm_bf16_streamk (variants 0, 1, 2, optionally | GEMM_VARIANT_DIRECT_STORE)
+ * minus the workspace, plus GEMM_ERR_INVALID_ARG when the device would need
+ * more scratch than the buffer holds.
+ * First call per device: with that device current, it looks up the buffer's
+ * address and clears it synchronously (cudaMemset), so make the first call
+ * for each device before any stream capture begins.
+ * Every call on a device shares the one buffer: calls that overlap on the GPU
+ * (other streams, other host threads) race and give wrong results; order
+ * them on one stream or synchronise between them.
+ */
+int gemm_bf16_streamk_noalloc(int variant, const void* A, const void* B, void* D, int64_t M,
+                              int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldd,
+                              cudaStream_t stream);
+
 /* Workspace bytes the stream-K entry points need on the current device for a
  * kernel variant (mxfp8: 0 = bf16, 1 = MXFP8); negative gemm_status_t on error. */
 int64_t gemm_streamk_workspace_bytes(int mxfp8, int variant);

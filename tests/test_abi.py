@@ -142,3 +142,8 @@ def test_streamk_workspace_query_without_device():
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert g.gemm_streamk_workspace_bytes(False, 2) == g.GEMM_ERR_UNSUPPORTED_DEVICE
+
+
+def test_noalloc_variant_checked_before_device_setup():
+    assert g.gemm_bf16_streamk_noalloc(3, FAKE, FAKE, FAKE, 4, 4, 16, 16, 16, 4, 0) == \
+        g.GEMM_ERR_INVALID_ARG
