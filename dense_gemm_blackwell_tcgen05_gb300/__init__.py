@@ -25,7 +25,8 @@ __all__ = [
     "gemm_kernel_plan", "gemm_last_cuda_error", "gemm_debug_stall_next_launch",
     "gemm_mxfp8_quantize", "quantize_mxfp8", "gemm_bf16_streamk", "gemm_mxfp8_streamk",
     "gemm_streamk_workspace_bytes", "gemm_last_schedule", "streamk_workspace",
-    "gemm_bf16_streamk_noalloc", "matmul_bf16",
+    "gemm_bf16_streamk_noalloc", "gemm_set_streamk_mode", "STREAMK_AUTO", "STREAMK_ALWAYS",
+    "STREAMK_NEVER", "gemm_streamk_plan", "matmul_bf16",
     "matmul_mxfp8",
 ]
 
@@ -49,7 +50,8 @@ EXPORTED_SYMBOLS = (
     "gemm_last_status_word", "gemm_status_string", "gemm_set_watchdog_ms", "gemm_kernel_plan",
     "gemm_last_cuda_error", "gemm_debug_stall_next_launch", "gemm_mxfp8_quantize",
     "gemm_bf16_streamk", "gemm_mxfp8_streamk", "gemm_streamk_workspace_bytes",
-    "gemm_last_schedule", "gemm_bf16_streamk_noalloc",
+    "gemm_last_schedule", "gemm_bf16_streamk_noalloc", "gemm_set_streamk_mode",
+    "gemm_streamk_plan",
 )
 
 _lock = threading.Lock()
@@ -99,6 +101,11 @@ def load() -> ctypes.CDLL:
             L.gemm_bf16_streamk_noalloc.argtypes = [ctypes.c_int, _vp, _vp, _vp, _i64, _i64, _i64,
                                                     _i64, _i64, _i64, _vp]
             L.gemm_bf16_streamk_noalloc.restype = ctypes.c_int
+            L.gemm_streamk_plan.argtypes = [_i64, _i64, _i64, _i64, ctypes.c_int,
+                                            ctypes.POINTER(_i64)]
+            L.gemm_streamk_plan.restype = ctypes.c_int
+            L.gemm_set_streamk_mode.argtypes = [ctypes.c_int]
+            L.gemm_set_streamk_mode.restype = ctypes.c_int
             L.gemm_last_schedule.argtypes = [ctypes.POINTER(_i64)]
             L.gemm_last_schedule.restype = ctypes.c_int
             L.gemm_mxfp8_quantize.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp]
@@ -167,6 +174,23 @@ def gemm_bf16_streamk_noalloc(variant: int, A: int, B: int, D: int, M: int, N: i
 
 def gemm_streamk_workspace_bytes(mxfp8: bool, variant: int) -> int:
     return int(load().gemm_streamk_workspace_bytes(int(bool(mxfp8)), variant))
+
+
+STREAMK_AUTO, STREAMK_ALWAYS, STREAMK_NEVER = 0, 1, 2
+
+
+def gemm_set_streamk_mode(mode: int) -> int:
+    return load().gemm_set_streamk_mode(mode)
+
+
+def gemm_streamk_plan(tiles: int, resident: int, k_tiles: int, unit: int,
+                      mode: int = STREAMK_AUTO) -> dict:
+    """The stream-K schedule for a tile count (host only)."""
+    out = (ctypes.c_int64 * 3)()
+    rc = load().gemm_streamk_plan(tiles, resident, k_tiles, unit, mode, out)
+    if rc != GEMM_OK:
+        raise GemmError(rc, "gemm_streamk_plan")
+    return {"dp_tiles": out[0], "sk_tiles": out[1], "clusters": out[2]}
 
 
 def gemm_last_schedule() -> dict:

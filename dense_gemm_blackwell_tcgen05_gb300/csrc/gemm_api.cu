@@ -33,6 +33,7 @@ std::mutex g_mu;
 DeviceState g_devices[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::atomic<int64_t> g_watchdog_ms{-1};
+std::atomic<int> g_streamk_mode{kStreamKAuto};
 thread_local int t_last_cuda_error = 0;
 thread_local int64_t t_stall_next = -1;   // one-shot watchdog test hook
 thread_local int64_t t_schedule[5] = {0, 0, 0, 0, 0};
@@ -157,6 +158,8 @@ int64_t timeout_ns_for(int64_t K) {
 }  // namespace
 
 void note_cuda_error(cudaError_t e) { t_last_cuda_error = static_cast<int>(e); }
+
+int streamk_mode() { return g_streamk_mode.load(); }
 
 void note_schedule(uint32_t clusters, uint32_t cg, uint32_t dp_tiles, uint32_t sk_tiles,
                    uint32_t sk_unit) {
@@ -454,6 +457,31 @@ const char* gemm_status_string(int status) {
 }
 
 int gemm_last_cuda_error(void) { return t_last_cuda_error; }
+
+int gemm_set_streamk_mode(int mode) {
+  if (mode < kStreamKAuto || mode > kStreamKNever) return GEMM_ERR_INVALID_ARG;
+  return g_streamk_mode.exchange(mode);
+}
+
+int gemm_streamk_plan(int64_t tiles, int64_t resident, int64_t k_tiles, int64_t unit, int mode,
+                      int64_t* out) {
+  if (out == nullptr || tiles < 0 || resident < 1 || k_tiles < 0 || unit < 1 ||
+      mode < kStreamKAuto || mode > kStreamKNever || tiles > 0x7FFFFFFF || resident > 0xFFFF ||
+      k_tiles > 0x7FFFFFFF || unit > 0xFFFF)
+    return GEMM_ERR_INVALID_ARG;
+  if (tiles == 0 || k_tiles == 0) {
+    out[0] = tiles;
+    out[1] = 0;
+    out[2] = 0;
+    return GEMM_OK;
+  }
+  const StreamKPlan sp = plan_streamk(static_cast<uint64_t>(tiles), static_cast<uint64_t>(resident),
+                                      static_cast<uint32_t>(k_tiles), static_cast<uint32_t>(unit), mode);
+  out[0] = sp.dp_tiles;
+  out[1] = sp.sk_tiles;
+  out[2] = sp.clusters;
+  return GEMM_OK;
+}
 
 int gemm_last_schedule(int64_t* out) {
   if (out == nullptr) return GEMM_ERR_INVALID_ARG;

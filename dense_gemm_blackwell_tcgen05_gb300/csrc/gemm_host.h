@@ -28,6 +28,61 @@ inline uint64_t streamk_bytes_per_cta(uint32_t tile_n) {
   return 4ull * 32ull * tile_n * 4ull + 4ull * 4ull;
 }
 
+// Stream-K schedule choice (host only).  Units are K-tiles of the kernel's
+// MMA time (about 0.37 us for every kernel here): a tile costs KT; a split
+// launch pays a fixed cost (contributor partial written, flag seen, owner
+// fix-up set up: about 11 us measured) plus about 3 us per contributor whose
+// 128 KB fp32 partial the owner streams in (the partial traffic moves at
+// about 45 GB/s per SM).  Constants fitted to per-CTA timelines on GB300.
+struct StreamKPlan {
+  uint32_t dp_tiles;   // tiles computed whole, round-robin over `clusters`
+  uint32_t sk_tiles;   // tiles after them, cut along K
+  uint32_t clusters;   // clusters launched
+};
+
+enum StreamKMode { kStreamKAuto = 0, kStreamKAlways = 1, kStreamKNever = 2 };
+int streamk_mode();
+
+inline StreamKPlan plan_streamk(uint64_t tiles, uint64_t resident, uint32_t kt, uint32_t unit,
+                                int mode) {
+  constexpr double kFixed = 30.0, kPerContributor = 8.0, kMinGain = 0.05;
+  const uint64_t ku = (kt + unit - 1) / unit;   // units per tile
+  const uint64_t waves = tiles / resident, rem = tiles % resident;
+  StreamKPlan dp{static_cast<uint32_t>(tiles), 0u,
+                 static_cast<uint32_t>(tiles < resident ? tiles : resident)};
+  if (mode == kStreamKNever || rem == 0 || ku < 2) return dp;
+  const double t_dp = static_cast<double>(waves + 1) * kt;
+  if (waves >= 1) {
+    // the partial wave plus one full wave, dealt over every resident cluster:
+    // each range spans more than one tile, so a tile has one contributor
+    const uint64_t sk = rem + resident;
+    StreamKPlan p{static_cast<uint32_t>(tiles - sk), static_cast<uint32_t>(sk),
+                  static_cast<uint32_t>(resident)};
+    const double t_sk = static_cast<double>(waves - 1) * kt +
+                        static_cast<double>((sk * ku + resident - 1) / resident) * unit + kFixed +
+                        kPerContributor;
+    return (mode == kStreamKAlways || t_sk < (1.0 - kMinGain) * t_dp) ? p : dp;
+  }
+  // fewer tiles than clusters: all tiles split; choose how many clusters
+  // (at most one per unit, so that no cluster's range is empty)
+  const uint64_t units = tiles * ku;
+  const uint64_t cap = units < resident ? units : resident;
+  StreamKPlan best = dp;
+  double t_best = 1e300;
+  for (uint64_t g = tiles + 1; g <= cap; ++g) {
+    const uint64_t per = (units + g - 1) / g;                  // units per cluster
+    const uint64_t contributors = (ku + per - 1) / per;        // later ranges touching a tile
+    const double t = static_cast<double>(per) * unit + kFixed + kPerContributor * contributors;
+    if (t < t_best || mode == kStreamKAlways) {
+      t_best = t;
+      best = StreamKPlan{0u, static_cast<uint32_t>(tiles), static_cast<uint32_t>(g)};
+      if (mode == kStreamKAlways) best.clusters = static_cast<uint32_t>(cap);
+    }
+  }
+  if (best.sk_tiles == 0) return dp;
+  return (mode == kStreamKAlways || t_best < (1.0 - kMinGain) * t_dp) ? best : dp;
+}
+
 struct LaunchCtx {
   int device;
   int num_sms;

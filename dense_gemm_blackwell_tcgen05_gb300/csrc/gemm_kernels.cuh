@@ -93,20 +93,18 @@ __device__ __forceinline__ bool work_item(const GemmArgs& a, uint32_t c, uint32_
   return true;
 }
 
-// Clusters whose partials an owner (kind 1 at cluster c) adds: the clusters
-// after c with non-empty unit ranges, until the tile's last unit is covered.
-// Calls f(cluster) for each.
-template <typename F>
-__device__ __forceinline__ void for_each_contributor(const GemmArgs& a, uint32_t c, uint32_t G,
-                                                     uint32_t KT, uint32_t tile, F&& f) {
+// Number of clusters whose partials the owner of `tile` (kind 1 at cluster c)
+// adds: c+1, c+2, ... up to the one holding the tile's last unit.  The host
+// launches no more clusters than units, so every cluster's range is
+// non-empty and the contributors are consecutive.
+__device__ __forceinline__ uint32_t num_contributors(const GemmArgs& a, uint32_t c, uint32_t G,
+                                                     uint32_t KT, uint32_t tile) {
   const uint32_t KU = (KT + a.sk_unit - 1) / a.sk_unit;
   const uint64_t U = static_cast<uint64_t>(a.sk_tiles) * KU;
   const uint64_t tile_end = static_cast<uint64_t>(tile - a.dp_tiles + 1) * KU;
-  for (uint32_t cc = c + 1; cc < G; ++cc) {
-    const uint64_t b0 = sk_bound(U, cc, G), b1 = sk_bound(U, cc + 1, G);
-    if (b0 >= tile_end) break;
-    if (b1 > b0) f(cc);
-  }
+  uint32_t n = 0;
+  for (uint32_t cc = c + 1; cc < G && sk_bound(U, cc, G) < tile_end; ++cc) ++n;
+  return n;
 }
 
 __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
@@ -237,7 +235,14 @@ struct GemmCfg {
   static constexpr uint32_t SMEM_BYTES =
       ALIGN_SLACK + STAGES * STAGE_BYTES + SF_BYTES + EPI_BYTES + BAR_BYTES;
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
-  static_assert((2 * STAGES + RAW_SLOTS + 2 * T_SLOTS + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
+  // Stream-K owner: each epilogue warp streams its contributors' partial
+  // chunks (32 rows x 32 fp32 columns, 4 KB) through FIX_SLOTS slots placed in
+  // the operand stages, which are idle once the CTA's last MMA has completed.
+  static constexpr uint32_t FIX_SLOTS = 8;
+  static constexpr uint32_t FIX_SLOT_BYTES = 32 * 32 * 4;
+  static_assert(4 * FIX_SLOTS * FIX_SLOT_BYTES <= STAGES * STAGE_BYTES, "partial ring fits the stages");
+  static_assert((2 * STAGES + RAW_SLOTS + 2 * T_SLOTS + 5) * 8 + 8 + 4 * FIX_SLOTS * 8 <= BAR_BYTES,
+                "barrier area");
 };
 
 // Re-tile one slot's scale bytes for tcgen05.cp ... 32x128b.warpx4.  The raw
@@ -377,20 +382,6 @@ __device__ __forceinline__ void store_chunk32_staged(uint8_t* buf, uint16_t* D, 
   __syncwarp();
 }
 
-// v[i] += the matching element of a stream-K partial chunk (read through L2:
-// another SM wrote it during this launch).
-__device__ __forceinline__ void add_partial32(uint32_t (&v)[32], const float* chunk, uint32_t lane) {
-  const float4* src = reinterpret_cast<const float4*>(chunk);
-#pragma unroll
-  for (uint32_t i4 = 0; i4 < 8; ++i4) {
-    const float4 p = __ldcg(src + i4 * 32 + lane);
-    v[4 * i4 + 0] = __float_as_uint(__uint_as_float(v[4 * i4 + 0]) + p.x);
-    v[4 * i4 + 1] = __float_as_uint(__uint_as_float(v[4 * i4 + 1]) + p.y);
-    v[4 * i4 + 2] = __float_as_uint(__uint_as_float(v[4 * i4 + 2]) + p.z);
-    v[4 * i4 + 3] = __float_as_uint(__uint_as_float(v[4 * i4 + 3]) + p.w);
-  }
-}
-
 template <int CG, Kind KIND, bool TMA_STORE>
 __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
     gemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -420,6 +411,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
   const auto acce_bar = [&](uint32_t b) { return bar0 + 8 * (kAccBar0 + 2 + b); };
   const uint32_t drain_bar = bar0 + 8 * (kAccBar0 + 4);
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + (bar0 - base) + 8 * (kAccBar0 + 5));
+  constexpr uint32_t kFixBar0 = kAccBar0 + 6;
   volatile uint32_t* const abort_flag = tmem_slot + 1;
 
   const uint32_t warp = warp_idx_sync();
@@ -448,6 +440,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
       mbar_init(acce_bar(b), 4 * CG);   // every epilogue warp of the pair
     }
     mbar_init(drain_bar, 1);
+    for (uint32_t i = 0; i < 4 * C::FIX_SLOTS; ++i) mbar_init(bar0 + 8 * (kFixBar0 + i), 1);
     *abort_flag = 0u;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
@@ -672,13 +665,50 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
     // ==================== epilogue: four warps, one TMEM lane quarter each =========
     const uint32_t q = warp & 3u;            // TMEM lanes 32q .. 32q+31
     const uint32_t ew = warp - 2u;           // staging slot owner
+    constexpr uint32_t NCH = C::UMMA_N / 32;
     uint32_t j = 0, chunk_ctr = 0;
     bool ok = true;
-    // this warp's 32 x UMMA_N fp32 slice of a stream-K partial slot, and its flag
+    // this warp's 32 x UMMA_N fp32 slice of a stream-K partial slot (chunk c
+    // of 32 columns at float offset 1024 c), and its flag
     const auto part_ptr = [&](uint32_t slot) {
       return args.ws_part + (static_cast<uint64_t>(slot * CG + rank) * 4 + q) * (32u * C::UMMA_N);
     };
     const auto flag_ptr = [&](uint32_t slot) { return args.ws_flag + (slot * CG + rank) * 4 + q; };
+    const auto fix_slot = [&](uint32_t r) { return stage0 + (ew * C::FIX_SLOTS + r) * C::FIX_SLOT_BYTES; };
+    const auto fix_bar = [&](uint32_t r) { return bar0 + 8 * (kFixBar0 + ew * C::FIX_SLOTS + r); };
+    // owner-side transfer stream: transfer n = chunk (n / nc) of contributor
+    // cluster_id + 1 + (n % nc); issued FIX_SLOTS ahead by lane 0
+    uint32_t nc = 0, nfix = 0, fix_issued = 0, fix_done = 0;
+    const auto issue_fix = [&](uint32_t n) {
+      const uint32_t r = n % C::FIX_SLOTS;
+      mbar_arrive_expect_tx(fix_bar(r), C::FIX_SLOT_BYTES);
+      bulk_load_1d(fix_slot(r), part_ptr(cluster_id + 1 + n % nc) + (n / nc) * 1024u, C::FIX_SLOT_BYTES,
+                   fix_bar(r));
+    };
+    // v += every contributor's partial of chunk c (in contributor order)
+    const auto add_partials = [&](uint32_t (&v)[32], uint32_t c) -> bool {
+      for (uint32_t i = 0; i < nc; ++i) {
+        const uint32_t n = c * nc + i;
+        const uint32_t r = n % C::FIX_SLOTS;
+        if (!warp_wait(fix_bar(r), (n / C::FIX_SLOTS) & 1u, wd, kSiteStreamKFlag, lane)) return false;
+        const float4* src = reinterpret_cast<const float4*>(base_ptr + (fix_slot(r) - base));
+#pragma unroll
+        for (uint32_t i4 = 0; i4 < 8; ++i4) {
+          const float4 p = src[i4 * 32 + lane];
+          v[4 * i4 + 0] = __float_as_uint(__uint_as_float(v[4 * i4 + 0]) + p.x);
+          v[4 * i4 + 1] = __float_as_uint(__uint_as_float(v[4 * i4 + 1]) + p.y);
+          v[4 * i4 + 2] = __float_as_uint(__uint_as_float(v[4 * i4 + 2]) + p.z);
+          v[4 * i4 + 3] = __float_as_uint(__uint_as_float(v[4 * i4 + 3]) + p.w);
+        }
+        __syncwarp();   // every lane has read the slot
+        ++fix_done;
+        if (fix_issued < nfix) {
+          if (lane == 0) issue_fix(fix_issued);
+          ++fix_issued;
+        }
+      }
+      return true;
+    };
     WorkItem w;
     for (uint32_t wi = 0; ok && work_item(args, cluster_id, num_clusters, KT, wi, w); ++wi, ++j) {
       const uint32_t b = j % C::ACC_STAGES;
@@ -690,13 +720,15 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
       const uint32_t row0 = mb * C::UMMA_M + rank * C::BLOCK_M + q * 32;
       const uint32_t col_base = nb * C::UMMA_N;
       const uint32_t t_addr = tmem_base + ((q * 32u) << 16) + b * C::UMMA_N;
+      // 32-column chunks of this tile inside N
+      const uint32_t live = min(NCH, (args.N - col_base + 31u) / 32u);
       if (w.kind == 2) {
         // a later K-range of a split tile: park the fp32 slice in this
         // cluster's slot (float4 index (chunk * 8 + i / 4) * 32 + lane, so each
         // store instruction writes 512 contiguous bytes), then raise the flag
         float* const part = part_ptr(cluster_id);
 #pragma unroll 1
-        for (uint32_t c = 0; c < C::UMMA_N / 32; ++c) {
+        for (uint32_t c = 0; c < live; ++c) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(t_addr + c * 32, v);
           tmem_wait_ld();
@@ -709,11 +741,20 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
         __threadfence();
         __syncwarp();
         if (lane == 0) st_release_u32(flag_ptr(cluster_id), args.epoch);
-      } else {
-        if (w.kind == 1)   // the first K-range: wait for every later range's partial
-          for_each_contributor(args, cluster_id, num_clusters, KT, w.tile, [&](uint32_t cc) {
-            if (ok) ok = wait_flag(flag_ptr(cc), args.epoch, wd, lane);
-          });
+      } else if (w.kind == 1) {
+        // the first K-range: this CTA's last item, so its operand stages are
+        // idle.  Wait for every later range's partial, then stream them in.
+        nc = num_contributors(args, cluster_id, num_clusters, KT, w.tile);
+        for (uint32_t i = 0; ok && i < nc; ++i) ok = wait_flag(flag_ptr(cluster_id + 1 + i), args.epoch, wd, lane);
+        if (ok && row0 < args.M) {
+          nfix = live * nc;
+          const uint32_t first = min(nfix, C::FIX_SLOTS);
+          if (lane == 0) {
+            fence_proxy_async_global();
+            for (uint32_t n = 0; n < first; ++n) issue_fix(n);
+          }
+          fix_issued = first;
+        }
       }
       if (w.kind != 2 && ok && row0 < args.M) {
         if constexpr (TMA_STORE) {
@@ -724,11 +765,10 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
             tmem_ld_32x32b_x32(t_addr + c * 64, v0);
             tmem_ld_32x32b_x32(t_addr + c * 64 + 32, v1);
             tmem_wait_ld();
-            if (w.kind == 1)
-              for_each_contributor(args, cluster_id, num_clusters, KT, w.tile, [&](uint32_t cc) {
-                add_partial32(v0, part_ptr(cc) + (2 * c) * 1024, lane);
-                add_partial32(v1, part_ptr(cc) + (2 * c + 1) * 1024, lane);
-              });
+            if (w.kind == 1) {
+              if (!add_partials(v0, 2 * c)) { ok = false; break; }
+              if (2 * c + 1 < live && !add_partials(v1, 2 * c + 1)) { ok = false; break; }
+            }
             const uint32_t buf = epi0 + (ew * C::EPI_BUFS + (chunk_ctr % C::EPI_BUFS)) * C::EPI_BUF_BYTES;
             if (lane == 0) bulk_wait_group_read<C::EPI_BUFS - 1>();   // this buffer's last store has read it
             __syncwarp();
@@ -761,15 +801,11 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
           }
         } else {
 #pragma unroll 1
-          for (uint32_t c = 0; c < C::UMMA_N / 32; ++c) {
-            if (col_base + c * 32 >= args.N) break;
+          for (uint32_t c = 0; c < live; ++c) {
             uint32_t v[32];
             tmem_ld_32x32b_x32(t_addr + c * 32, v);
             tmem_wait_ld();
-            if (w.kind == 1)
-              for_each_contributor(args, cluster_id, num_clusters, KT, w.tile, [&](uint32_t cc) {
-                add_partial32(v, part_ptr(cc) + c * 1024, lane);
-              });
+            if (w.kind == 1 && !add_partials(v, c)) { ok = false; break; }
             store_chunk32_staged(base_ptr + (epi0 - base) + ew * C::CHUNK_BYTES,
                                  static_cast<uint16_t*>(args.D), args.ldd, args.M, args.N, row0,
                                  col_base + c * 32, v, lane);
@@ -780,8 +816,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
         // partials consumed: leave the flags at zero for the next launch
         __syncwarp();
         if (lane == 0)
-          for_each_contributor(args, cluster_id, num_clusters, KT, w.tile,
-                               [&](uint32_t cc) { *flag_ptr(cc) = 0u; });
+          for (uint32_t i = 0; i < nc; ++i) *flag_ptr(cluster_id + 1 + i) = 0u;
       }
       // all TMEM reads of accumulator b by this warp are complete
       tc_fence_before_sync();
@@ -793,6 +828,10 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
           mbar_arrive_cluster(mapa_shared(acce_bar(b), 0));
       }
     }
+    // Exit path after a give-up: let the partial transfers still in flight land.
+    if (lane == 0)
+      for (uint32_t n = fix_done; n < fix_issued; ++n)
+        drain_wait(fix_bar(n % C::FIX_SLOTS), (n / C::FIX_SLOTS) & 1u, wd, kSiteStreamKFlag);
     if constexpr (TMA_STORE) {
       if (lane == 0) bulk_wait_group<0>();
       __syncwarp();

@@ -105,10 +105,11 @@ int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) 
   const uint64_t resident = CG == 2 ? static_cast<uint64_t>(max_clusters[ctx.device])
                                     : static_cast<uint64_t>(ctx.num_sms);
   // Schedule.  Data-parallel: whole tiles round-robin over min(tiles, resident)
-  // clusters.  Stream-K (when the caller gives a workspace and the last wave
-  // would be partial): the tiles of the last partial wave plus one full wave
-  // are cut into units of sk_unit K-tiles dealt out evenly to all resident
-  // clusters, the rest stay whole.
+  // clusters.  Stream-K (only with a caller workspace, and only where the
+  // cost model in plan_streamk predicts a gain, unless forced): the tiles of
+  // the last partial wave plus one full wave, or all tiles when there are
+  // fewer than clusters, are cut into units of sk_unit K-tiles dealt out in
+  // equal contiguous ranges.
   a.dp_tiles = static_cast<uint32_t>(tiles);
   a.sk_tiles = 0;
   a.sk_unit = C::MX ? C::SF_GROUP : 1u;
@@ -117,16 +118,14 @@ int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) 
     const uint64_t need = resident * CG * streamk_bytes_per_cta(C::UMMA_N);
     if (p.workspace_bytes < need || (reinterpret_cast<uintptr_t>(p.workspace) & 15u) != 0)
       return GEMM_ERR_INVALID_ARG;
-    const uint64_t units_per_tile = (a.num_k_tiles + a.sk_unit - 1) / a.sk_unit;
-    const uint64_t rem = tiles % resident, waves = tiles / resident;
-    if (rem != 0 && units_per_tile >= 2) {
-      const uint64_t sk = rem + (waves >= 1 ? resident : 0);
-      a.sk_tiles = static_cast<uint32_t>(sk);
-      a.dp_tiles = static_cast<uint32_t>(tiles - sk);
-      clusters = resident;
-      a.ws_part = static_cast<float*>(p.workspace);
-      a.ws_flag = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(p.workspace) +
-                                              resident * CG * (streamk_bytes_per_cta(C::UMMA_N) - 16));
+    const StreamKPlan sp = plan_streamk(tiles, resident, a.num_k_tiles, a.sk_unit, streamk_mode());
+    if (sp.sk_tiles != 0) {
+      a.dp_tiles = sp.dp_tiles;
+      a.sk_tiles = sp.sk_tiles;
+      clusters = sp.clusters;
+      // flags first (16 bytes per CTA slot), then the partial slots
+      a.ws_flag = static_cast<uint32_t*>(p.workspace);
+      a.ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(p.workspace) + resident * CG * 16);
       uint32_t e = epoch_counter.fetch_add(1) + 1;
       if (e == 0) e = epoch_counter.fetch_add(1) + 1;
       a.epoch = e;

@@ -115,14 +115,18 @@ int gemm_mxfp8_variant(int variant, const void* A, const void* B, const void* SF
  * arguments and results as gemm_bf16_variant / gemm_mxfp8_variant (variants
  * 0, 1, 2, optionally with GEMM_VARIANT_DIRECT_STORE), plus a caller-owned
  * device workspace.  When the tiles do not fill the last wave of resident
- * CTAs, the tiles of that partial wave and of one full wave before it are cut
- * along K and spread evenly over all resident CTAs; a tile's first K-range
- * owner adds the later ranges' fp32 partials (parked in the workspace) before
- * storing D.  Otherwise the call behaves like the data-parallel entry point.
+ * CTAs and the mode set by gemm_set_streamk_mode allows it (by default: where
+ * a cost model predicts a gain), the tiles of that partial wave and of one
+ * full wave before it -- or all tiles, when there are fewer tiles than
+ * resident CTAs -- are cut along K and spread evenly over the CTAs; a tile's
+ * first K-range owner adds the later ranges' fp32 partials (parked in the
+ * workspace) in K order before storing D, so results are deterministic.
+ * Otherwise the call behaves like the data-parallel entry point.
  * workspace: 16-byte aligned device memory of at least
- * gemm_streamk_workspace_bytes() bytes, ZEROED ONCE before its first use
- * (every completed call leaves its flag words zero again; after a call that
- * ended in GEMM_ERR_TIMEOUT, zero it again).  Calls that share a workspace
+ * gemm_streamk_workspace_bytes() bytes: 16 bytes of flags per CTA, then the
+ * partial slots.  ZERO IT ONCE before its first use (every completed call
+ * leaves its flag words zero again; after a call that ended in
+ * GEMM_ERR_TIMEOUT, zero it again).  Calls that share a workspace
  * must not overlap on the GPU.  Errors as the data-parallel entry points,
  * plus GEMM_ERR_INVALID_ARG for a NULL, short or misaligned workspace.
  */
@@ -156,6 +160,25 @@ int gemm_mxfp8_streamk(int variant, const void* A, const void* B, const void* SF
 int gemm_bf16_streamk_noalloc(int variant, const void* A, const void* B, void* D, int64_t M,
                               int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldd,
                               cudaStream_t stream);
+
+/* When the stream-K entry points split tiles, for later calls in this
+ * process: GEMM_STREAMK_AUTO (default) splits only where a cost model of the
+ * kernel (whole-tile waves against split ranges plus the fix-up of each
+ * split tile) predicts a gain of 5% or more; GEMM_STREAMK_ALWAYS splits
+ * whenever the tiles leave a partial wave and K has two units or more;
+ * GEMM_STREAMK_NEVER always runs the data-parallel schedule.  Returns the
+ * previous mode, or GEMM_ERR_INVALID_ARG for another value. */
+enum { GEMM_STREAMK_AUTO = 0, GEMM_STREAMK_ALWAYS = 1, GEMM_STREAMK_NEVER = 2 };
+int gemm_set_streamk_mode(int mode);
+
+/* The schedule the stream-K entry points would use (host only, no device
+ * needed): for `tiles` output tiles, `resident` co-resident clusters, K-tiles
+ * per tile and K-tiles per stream-K unit (1 for bf16, 4 for MXFP8) under
+ * `mode`, out[0] = tiles computed whole, out[1] = tiles split along K,
+ * out[2] = clusters launched (0 when there is nothing to compute).  `out`
+ * holds 3 values.  GEMM_ERR_INVALID_ARG for out-of-range arguments. */
+int gemm_streamk_plan(int64_t tiles, int64_t resident, int64_t k_tiles, int64_t unit, int mode,
+                      int64_t* out);
 
 /* Workspace bytes the stream-K entry points need on the current device for a
  * kernel variant (mxfp8: 0 = bf16, 1 = MXFP8); negative gemm_status_t on error. */

@@ -35,6 +35,15 @@ MX_VARIANTS = {
 _WS = {}
 
 
+@pytest.fixture(autouse=True)
+def _always_split():
+    """Parity cases force the split (the cost model would keep small cases
+    data-parallel); the mode is restored after each test."""
+    old = g.gemm_set_streamk_mode(g.STREAMK_ALWAYS)
+    yield
+    g.gemm_set_streamk_mode(old)
+
+
 def workspace(mx, variant):
     key = (bool(mx), variant & 0xFF)
     if key not in _WS:
@@ -43,25 +52,28 @@ def workspace(mx, variant):
 
 
 def flags_are_zero(ws, mx, variant, sched):
-    """The flag words (after the partial slots) are back at zero.  Only a
-    split launch runs on every resident cluster and uses the workspace."""
+    """The flag words (16 bytes per launched CTA at the start of the
+    workspace) are back at zero.  Only a split launch uses the workspace."""
     if sched["sk_tiles"] == 0:
         return True
-    tile_n = g.gemm_kernel_plan(bool(mx), variant)["tile_n"]
     ctas = sched["clusters"] * sched["ctas_per_cluster"]
-    off = ctas * 4 * 32 * tile_n * 4
-    return bool(torch.all(ws[off:off + ctas * 16] == 0).item())
+    return bool(torch.all(ws[:ctas * 16] == 0).item())
 
 
 def expected_split(sched, M, N, tile_m, tile_n, kt, unit):
-    """Tiles the launcher must have split: those of the partial last wave
-    plus one full wave, when the tile count leaves a partial wave."""
+    """Tiles the launcher must split when forced: those of the partial last
+    wave plus one full wave, or all tiles when there are fewer tiles than
+    resident clusters (then at most one cluster per K-unit is launched)."""
     tiles = -(-M // tile_m) * -(-N // tile_n)
     G = sched["clusters"]
     units = -(-kt // unit)
-    if tiles % G == 0 or units < 2:
+    assert sched["dp_tiles"] + sched["sk_tiles"] == tiles
+    if units < 2 or sched["sk_tiles"] == 0:
         return 0
-    return tiles % G + (G if tiles >= G else 0)
+    if sched["dp_tiles"] == 0:
+        assert G <= tiles * units
+        return tiles
+    return tiles % G + G
 
 
 def run_bf16(A_cpu, B_cpu, variant, ldd=None, calls=1):
@@ -184,7 +196,6 @@ def test_bf16_waves_plus_partial(v):
     tm, tn, bk = plan(False, variant)
     want = expected_split(sched, M, N, tm, tn, K // bk, 1)
     assert sched["sk_tiles"] == want
-    assert sched["dp_tiles"] + sched["sk_tiles"] == (M // tm) * (N // tn)
     if want == 0:
         pytest.skip(f"{sched['clusters']} clusters divide the tile count")
     assert sched["dp_tiles"] > 0
@@ -262,6 +273,36 @@ def test_mxfp8_waves_plus_partial(v):
     D_ref, _ = oracle.gemm_mxfp8_entries(A.numpy(), B.numpy(), SFA.numpy(), SFB.numpy(), rows,
                                          cols, K)
     assert np.array_equal(gi.bf16_codes(D)[rows, cols], oracle.f64_to_bf16_rne(D_ref))
+
+
+# -------------------------------------------------- the automatic choice
+
+def test_auto_mode_splits_a_long_k_problem_with_few_tiles():
+    g.gemm_set_streamk_mode(g.STREAMK_AUTO)
+    M, N, K = 1024, 1024, 16384
+    A, B = int_bf16(M, N, K, seed=12, lo=-1, hi=2)
+    for v in ("1cta", "2cta"):
+        (D,), sched = run_bf16(A, B, BF16_VARIANTS[v])
+        assert sched["sk_tiles"] > 0 and sched["dp_tiles"] == 0
+        rows, cols = P.sample_positions(M, N, 3000, seed=5)
+        D_ref, _ = oracle.gemm_bf16_entries(gi.bf16_codes(A), gi.bf16_codes(B), rows, cols)
+        assert np.array_equal(gi.bf16_codes(D)[rows, cols], oracle.f64_to_bf16_rne(D_ref))
+
+
+def test_auto_mode_keeps_short_k_data_parallel():
+    g.gemm_set_streamk_mode(g.STREAMK_AUTO)
+    A, B = int_bf16(300, 520, 1040, seed=3)
+    (D,), sched = run_bf16(A, B, g.VARIANT_2CTA)
+    assert sched["sk_tiles"] == 0
+    D_ref, _ = oracle.gemm_bf16(gi.bf16_codes(A), gi.bf16_codes(B))
+    assert_bitwise(D, D_ref, "auto short k")
+
+
+def test_never_mode_is_data_parallel():
+    g.gemm_set_streamk_mode(g.STREAMK_NEVER)
+    A, B = int_bf16(1024, 1024, 4096, seed=4, lo=-1, hi=2)
+    (_,), sched = run_bf16(A, B, g.VARIANT_1CTA)
+    assert sched["sk_tiles"] == 0 and sched["clusters"] == 32
 
 
 # ------------------------------------------------------------ argument errors

@@ -48,6 +48,15 @@ def test_noalloc_matches_workspace_entry_point(variant, shape):
     A_cpu, B_cpu = gi.bf16_operands(M, N, K, seed=M + N + K)
     A, B = A_cpu.cuda(), B_cpu.cuda()
     ws = g.streamk_workspace(False, variant)
+    # force the split so that the scratch is used whatever the cost model says
+    old_mode = g.gemm_set_streamk_mode(g.STREAMK_ALWAYS)
+    try:
+        _compare(A, B, A_cpu, B_cpu, variant, ws, M, N)
+    finally:
+        g.gemm_set_streamk_mode(old_mode)
+
+
+def _compare(A, B, A_cpu, B_cpu, variant, ws, M, N):
     want = _existing(A, B, variant, ws)
     # the bound's scale sum|a||b| from the oracle, on sampled entries
     rows, cols = P.sample_positions(M, N, 2000, seed=7)
