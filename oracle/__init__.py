@@ -60,6 +60,9 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     for name in ("oracle_gemm_bf16", "oracle_gemm_bf16_entries",
                  "oracle_gemm_mxfp8", "oracle_gemm_mxfp8_entries"):
         getattr(L, name).restype = None
+    L.oracle_epilogue.argtypes = [_p, _i64, _i64, ctypes.c_double, ctypes.c_double, _p, _i64, _p,
+                                  ctypes.c_int, _p]
+    L.oracle_epilogue.restype = None
     L.oracle_mxfp8_quantize.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _p, _i64]
     L.oracle_mxfp8_quantize.restype = None
     L.oracle_f64_to_e4m3_rne.argtypes = [ctypes.c_double]
@@ -136,6 +139,31 @@ class Oracle:
         v = np.asarray(values, np.float64).ravel()
         return np.array([self.L.oracle_f64_to_e4m3_rne(float(x)) for x in v],
                         np.uint8).reshape(np.shape(values))
+
+    def epilogue(self, P, alpha=1.0, beta=0.0, C=None, bias=None, act=0):
+        """act(alpha P + beta C + bias[j]) elementwise in fp64 (the fused
+        epilogue); P, C [M, N] and bias [N] as fp64 values."""
+        f64 = lambda x: np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+        P = f64(P)
+        M, N = P.shape
+        out = np.empty((M, N), dtype=np.float64)
+        Cp, ldc = None, 0
+        if C is not None:
+            C = f64(C)
+            if C.shape[0] != M or C.shape[1] < N:
+                raise ValueError("C must be [M, >=N]")
+            Cp, ldc = _ptr(C), C.shape[1]
+        bp = None
+        if bias is not None:
+            bias = f64(bias).reshape(-1)
+            if bias.shape[0] < N:
+                raise ValueError("bias must hold N values")
+            bp = _ptr(bias)
+        if act not in (0, 1, 2):
+            raise ValueError("act must be 0, 1 or 2")
+        self.L.oracle_epilogue(_ptr(P), M, N, float(alpha), float(beta), Cp, ldc, bp, int(act),
+                               _ptr(out))
+        return out
 
     def mxfp8_quantize(self, X, K: int | None = None):
         """MXFP8-encode float32 rows X [rows, ldx] (first K columns): returns
@@ -260,6 +288,10 @@ def f64_to_e4m3_rne(values):
 
 def mxfp8_quantize(X, K=None):
     return default().mxfp8_quantize(X, K)
+
+
+def epilogue(P, alpha=1.0, beta=0.0, C=None, bias=None, act=0):
+    return default().epilogue(P, alpha, beta, C, bias, act)
 
 
 def gemm_bf16(A, B, K=None):

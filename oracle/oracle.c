@@ -304,3 +304,45 @@ void oracle_mxfp8_quantize(const float *X, int64_t rows, int64_t K, int64_t ldx,
         }
     }
 }
+
+/* --------------------------------------------------------- fused epilogue */
+
+/*
+ * The epilogue fused into the TMEM -> register readback (b200-tmem-
+ * lifecycle-planner, "A1 -- Case 1: dense MMA accumulator": the warpgroup
+ * reads the fp32 accumulator back into registers for the cast/epilogue/store;
+ * b200-gemm-optimization-ladder, "B -- Boundaries", "Do not use when": custom
+ * fusion is a reason to own the kernel).  The pages name no particular
+ * epilogue; this is the plain linear-layer one.  Given the exact sums P of
+ * one of the GEMMs above, in fp64:
+ *
+ *     v[i][j] = alpha * P[i][j] + beta * C[i][j] + bias[j]
+ *     D[i][j] = act(v[i][j])
+ *
+ *   act 0: identity.
+ *   act 1: ReLU, 0 where v < 0 and v otherwise (NaN stays NaN).
+ *   act 2: GELU, v * Phi(v) with Phi the standard normal distribution
+ *          function, Phi(v) = (1 + erf(v / sqrt 2)) / 2.
+ *
+ * C (decoded, [M,N] with pitch ldc) and bias (decoded, [N]) may be NULL, in
+ * which case their term is absent.  out is dense [M,N].
+ */
+static double act_f64(double v, int act)
+{
+    if (act == 1) return v < 0.0 ? 0.0 : v;
+    if (act == 2) return v * 0.5 * (1.0 + erf(v / sqrt(2.0)));
+    return v;
+}
+
+void oracle_epilogue(const double *P, int64_t M, int64_t N, double alpha, double beta,
+                     const double *C, int64_t ldc, const double *bias, int act, double *out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j) {
+            double v = alpha * P[i * N + j];
+            if (C) v += beta * C[i * ldc + j];
+            if (bias) v += bias[j];
+            out[i * N + j] = act_f64(v, act);
+        }
+}

@@ -357,6 +357,64 @@ def pin_quantize_nonfinite(o):
     assert np.all(Q[0, [0, 1, 2]] == _nearest_e4m3(2.0 ** 8))
 
 
+# ---------------------------------------------------------- fused epilogue
+
+def _gelu_ref(v: float) -> float:
+    """v * Phi(v) with Python's math.erf (an independent libm path)."""
+    import math
+    return v * 0.5 * (1.0 + math.erf(v / math.sqrt(2.0)))
+
+
+def pin_epilogue_bruteforce(o):
+    """act(alpha sum + beta C + bias[j]) on tiny asymmetric shapes, the sums
+    exact in rationals, the rest in Python floats: a bias taken per row, a
+    beta applied to the product, an ignored C pitch or a mixed-up activation
+    changes a value."""
+    rng = np.random.default_rng(9)
+    M, N, K, lda = 3, 5, 7, 9
+    A = random_bf16_codes(rng, (M, lda), 2.0)
+    B = random_bf16_codes(rng, (N, K), 1.0)
+    P, _ = o.gemm_bf16(A, B, K)
+    C = rng.standard_normal((M, N + 3))
+    bias = rng.standard_normal(N)
+    Af, Bf = torch_bf16_f64(A), torch_bf16_f64(B)
+    for act in (0, 1, 2):
+        for alpha, beta, use_c, use_b in [(1.5, -0.75, True, True), (-2.0, 0.0, False, True),
+                                          (0.25, 3.0, True, False)]:
+            out = o.epilogue(P, alpha, beta, C if use_c else None, bias if use_b else None, act)
+            for i in range(M):
+                for j in range(N):
+                    s, _ = exact_dot([Fraction(x) for x in Af[i, :K]], [Fraction(x) for x in Bf[j, :K]])
+                    v = alpha * float(s) + (beta * C[i, j] if use_c else 0.0) + (bias[j] if use_b else 0.0)
+                    want = v if act == 0 else (max(v, 0.0) if act == 1 else _gelu_ref(v))
+                    assert abs(out[i, j] - want) <= 1e-12 * (1.0 + abs(want)), ("epilogue", act, i, j)
+
+
+def pin_gelu_textbook(o):
+    """GELU(x) = x Phi(x) at points where the standard normal distribution
+    function has well-known values: Phi(0) = 1/2, Phi(1) = 0.8413447460685429,
+    Phi(2) = 0.9772498680518208, Phi(-x) = 1 - Phi(x)."""
+    P = np.array([[0.0, 1.0, -1.0, 2.0, -2.0]])
+    out = o.epilogue(P, act=2)[0]
+    want = [0.0, 0.8413447460685429, -(1.0 - 0.8413447460685429), 2 * 0.9772498680518208,
+            -2 * (1.0 - 0.9772498680518208)]
+    assert np.allclose(out, want, rtol=1e-14, atol=1e-15), out
+    # odd part: GELU(x) - GELU(-x) = x for any x
+    xs = np.linspace(-6, 6, 25).reshape(1, -1)
+    g = o.epilogue(xs, act=2)[0]
+    assert np.allclose(g - g[::-1], xs[0], rtol=0, atol=1e-14)
+
+
+def pin_relu_and_identity(o):
+    P = np.array([[-3.5, -0.0, 0.0, 2.25, np.nan, -np.inf, np.inf]])
+    r = o.epilogue(P, act=1)[0]
+    assert r[0] == 0.0 and r[3] == 2.25 and np.isnan(r[4]) and r[5] == 0.0 and r[6] == np.inf
+    ident = o.epilogue(P)
+    assert same(ident, P)
+    # alpha only, no other term: exact scaling
+    assert same(o.epilogue(P[:, :4], alpha=-0.5)[0], -0.5 * P[0, :4])
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 
 

@@ -40,6 +40,12 @@ MUTANTS = {
                           "e = (int)ceil(log2(amax / 448.0)) + 1;\n                while (amax > ldexp(448.0, e))\n                    ++e;"),
     "quant_block_16": ("int64_t k0 = b * 32, k1 = k0 + 32 < K ? k0 + 32 : K;", "int64_t k0 = b * 32, k1 = k0 + 16 < K ? k0 + 16 : K;"),
     "quant_scale_sign": ("oracle_f64_to_e4m3_rne(ldexp(x, -e))", "oracle_f64_to_e4m3_rne(ldexp(x, e))"),
+    "epi_bias_by_row": ("if (bias) v += bias[j];", "if (bias) v += bias[i];"),
+    "epi_beta_as_alpha": ("if (C) v += beta * C[i * ldc + j];", "if (C) v += alpha * C[i * ldc + j];"),
+    "epi_ignores_ldc": ("if (C) v += beta * C[i * ldc + j];", "if (C) v += beta * C[i * N + j];"),
+    "epi_relu_sign": ("return v < 0.0 ? 0.0 : v;", "return v > 0.0 ? 0.0 : v;"),
+    "epi_gelu_scale": ("erf(v / sqrt(2.0))", "erf(v / 2.0)"),
+    "epi_gelu_half": ("return v * 0.5 * (1.0 + erf", "return v * (1.0 + erf"),
 }
 
 
