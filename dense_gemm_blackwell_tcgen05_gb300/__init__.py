@@ -26,7 +26,8 @@ __all__ = [
     "gemm_mxfp8_quantize", "quantize_mxfp8", "gemm_bf16_streamk", "gemm_mxfp8_streamk",
     "gemm_streamk_workspace_bytes", "gemm_last_schedule", "streamk_workspace",
     "gemm_bf16_streamk_noalloc", "gemm_set_streamk_mode", "STREAMK_AUTO", "STREAMK_ALWAYS",
-    "STREAMK_NEVER", "gemm_streamk_plan", "matmul_bf16",
+    "STREAMK_NEVER", "gemm_streamk_plan", "gemm_bf16_fused", "gemm_mxfp8_fused", "GemmEpilogue",
+    "make_epilogue", "matmul_fused", "DTYPE_BF16", "DTYPE_F32", "ACT_NONE", "ACT_RELU", "ACT_GELU", "matmul_bf16",
     "matmul_mxfp8",
 ]
 
@@ -51,7 +52,7 @@ EXPORTED_SYMBOLS = (
     "gemm_last_cuda_error", "gemm_debug_stall_next_launch", "gemm_mxfp8_quantize",
     "gemm_bf16_streamk", "gemm_mxfp8_streamk", "gemm_streamk_workspace_bytes",
     "gemm_last_schedule", "gemm_bf16_streamk_noalloc", "gemm_set_streamk_mode",
-    "gemm_streamk_plan",
+    "gemm_streamk_plan", "gemm_bf16_fused", "gemm_mxfp8_fused",
 )
 
 _lock = threading.Lock()
@@ -71,6 +72,18 @@ class GemmError(RuntimeError):
 
 def library_path() -> str:
     return _build.LIB_PATH
+
+
+DTYPE_BF16, DTYPE_F32 = 0, 1
+ACT_NONE, ACT_RELU, ACT_GELU = 0, 1, 2
+
+
+class GemmEpilogue(ctypes.Structure):
+    """Mirror of gemm_epilogue_t: D = act(alpha acc + beta C + bias[col])."""
+    _fields_ = [("alpha", ctypes.c_float), ("beta", ctypes.c_float), ("C", ctypes.c_void_p),
+                ("ldc", ctypes.c_int64), ("bias", ctypes.c_void_p), ("bias_dtype", ctypes.c_int32),
+                ("activation", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 def load() -> ctypes.CDLL:
@@ -101,6 +114,13 @@ def load() -> ctypes.CDLL:
             L.gemm_bf16_streamk_noalloc.argtypes = [ctypes.c_int, _vp, _vp, _vp, _i64, _i64, _i64,
                                                     _i64, _i64, _i64, _vp]
             L.gemm_bf16_streamk_noalloc.restype = ctypes.c_int
+            L.gemm_bf16_fused.argtypes = [ctypes.c_int, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
+                                          _i64, ctypes.POINTER(GemmEpilogue), _vp]
+            L.gemm_bf16_fused.restype = ctypes.c_int
+            L.gemm_mxfp8_fused.argtypes = [ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64,
+                                           _i64, _i64, _i64, _i64, _i64,
+                                           ctypes.POINTER(GemmEpilogue), _vp]
+            L.gemm_mxfp8_fused.restype = ctypes.c_int
             L.gemm_streamk_plan.argtypes = [_i64, _i64, _i64, _i64, ctypes.c_int,
                                             ctypes.POINTER(_i64)]
             L.gemm_streamk_plan.restype = ctypes.c_int
@@ -181,6 +201,80 @@ STREAMK_AUTO, STREAMK_ALWAYS, STREAMK_NEVER = 0, 1, 2
 
 def gemm_set_streamk_mode(mode: int) -> int:
     return load().gemm_set_streamk_mode(mode)
+
+
+def gemm_bf16_fused(variant: int, A: int, B: int, D: int, M: int, N: int, K: int, lda: int,
+                    ldb: int, ldd: int, epi: GemmEpilogue | None, stream: int = 0) -> int:
+    return load().gemm_bf16_fused(variant, A, B, D, M, N, K, lda, ldb, ldd,
+                                  None if epi is None else ctypes.byref(epi), stream)
+
+
+def gemm_mxfp8_fused(variant: int, A: int, B: int, SFA: int, SFB: int, D: int, M: int, N: int,
+                     K: int, lda: int, ldb: int, ldsfa: int, ldsfb: int, ldd: int,
+                     epi: GemmEpilogue | None, stream: int = 0) -> int:
+    return load().gemm_mxfp8_fused(variant, A, B, SFA, SFB, D, M, N, K, lda, ldb, ldsfa, ldsfb,
+                                   ldd, None if epi is None else ctypes.byref(epi), stream)
+
+
+_ACTS = {"none": ACT_NONE, "relu": ACT_RELU, "gelu": ACT_GELU}
+
+
+def make_epilogue(alpha=1.0, beta=0.0, C=None, bias=None, activation="none",
+                  out_dtype=None) -> GemmEpilogue:
+    """A GemmEpilogue from torch tensors: C [M, >=N] of the output dtype,
+    bias [N] bf16 or float32, activation "none" | "relu" | "gelu"."""
+    import torch
+    out_dtype = torch.bfloat16 if out_dtype is None else out_dtype
+    if out_dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("out_dtype must be bfloat16 or float32")
+    e = GemmEpilogue()
+    e.alpha, e.beta = float(alpha), float(beta)
+    e.out_dtype = DTYPE_F32 if out_dtype == torch.float32 else DTYPE_BF16
+    e.activation = _ACTS[activation]
+    if C is not None:
+        _check_2d(C, "C")
+        if C.dtype != out_dtype:
+            raise TypeError("C must have the output dtype")
+        e.C, e.ldc = C.data_ptr(), C.stride(0)
+    if bias is not None:
+        if bias.dim() != 1 or bias.stride(0) != 1 or bias.dtype not in (torch.bfloat16, torch.float32):
+            raise TypeError("bias must be a contiguous 1-D bfloat16 or float32 tensor")
+        e.bias = bias.data_ptr()
+        e.bias_dtype = DTYPE_F32 if bias.dtype == torch.float32 else DTYPE_BF16
+    return e
+
+
+def matmul_fused(A, B, SFA=None, SFB=None, *, alpha=1.0, beta=0.0, C=None, bias=None,
+                 activation="none", out_dtype=None, out=None, variant: int = VARIANT_AUTO,
+                 stream=None):
+    """D = act(alpha A @ B.T + beta C + bias): bf16 A [M,K], B [N,K], or
+    MXFP8 codes with SFA/SFB as in matmul_mxfp8; D of out_dtype (bf16 or fp32)."""
+    import torch
+    _check_2d(A, "A")
+    _check_2d(B, "B")
+    M, K = A.shape
+    N = B.shape[0]
+    if B.shape[1] != K:
+        raise ValueError("A and B disagree on K")
+    out_dtype = torch.bfloat16 if out_dtype is None else out_dtype
+    if out is None:
+        out = torch.empty(M, N, dtype=out_dtype, device=A.device)
+    _check_2d(out, "out")
+    if out.dtype != out_dtype:
+        raise TypeError("out must have out_dtype")
+    e = make_epilogue(alpha, beta, C, bias, activation, out_dtype)
+    if SFA is None:
+        if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
+            raise TypeError("A and B must be bfloat16 (or pass SFA/SFB for MXFP8)")
+        rc = gemm_bf16_fused(variant, A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K,
+                             A.stride(0), B.stride(0), out.stride(0), e, _stream_handle(stream))
+    else:
+        rc = gemm_mxfp8_fused(variant, A.data_ptr(), B.data_ptr(), SFA.data_ptr(), SFB.data_ptr(),
+                              out.data_ptr(), M, N, K, A.stride(0), B.stride(0), SFA.stride(0),
+                              SFB.stride(0), out.stride(0), e, _stream_handle(stream))
+    if rc != GEMM_OK:
+        raise GemmError(rc, "matmul_fused")
+    return out
 
 
 def gemm_streamk_plan(tiles: int, resident: int, k_tiles: int, unit: int,

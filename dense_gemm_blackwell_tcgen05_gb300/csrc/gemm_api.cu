@@ -155,6 +155,38 @@ int64_t timeout_ns_for(int64_t K) {
   return watchdog_ms() * 1000000ll + K * 64ll;
 }
 
+// Fills the fused-epilogue fields of `p` from `e` (NULL: the plain store).
+// N, D and ldd are the call's; returns a gemm_status_t.
+int parse_epilogue(const gemm_epilogue_t* e, int64_t N, const void* D, int64_t ldd, int device,
+                   Problem& p) {
+  if (e == nullptr) return GEMM_OK;
+  if (e->reserved != 0 || (e->out_dtype != GEMM_DTYPE_BF16 && e->out_dtype != GEMM_DTYPE_F32) ||
+      e->activation < GEMM_ACT_NONE || e->activation > GEMM_ACT_GELU)
+    return GEMM_ERR_INVALID_ARG;
+  uint32_t mode = static_cast<uint32_t>(e->activation) << kEpiActShift;
+  if (e->out_dtype == GEMM_DTYPE_F32) mode |= kEpiOutF32;
+  if (!(e->alpha == 1.0f)) mode |= kEpiAlpha;
+  if (e->C != nullptr) {
+    if (e->ldc < N || e->ldc > (int64_t(1) << 36) || !is_device_pointer(e->C, device) ||
+        (e->C == D && e->ldc != ldd))
+      return GEMM_ERR_INVALID_ARG;
+    mode |= kEpiC;
+  }
+  if (e->bias != nullptr) {
+    if ((e->bias_dtype != GEMM_DTYPE_BF16 && e->bias_dtype != GEMM_DTYPE_F32) ||
+        !is_device_pointer(e->bias, device))
+      return GEMM_ERR_INVALID_ARG;
+    mode |= kEpiBias | (e->bias_dtype == GEMM_DTYPE_F32 ? kEpiBiasF32 : 0u);
+  }
+  p.epi_mode = mode;
+  p.alpha = e->alpha;
+  p.beta = e->beta;
+  p.C = e->C;
+  p.ldc = static_cast<uint64_t>(e->C != nullptr ? e->ldc : 0);
+  p.bias = e->bias;
+  return GEMM_OK;
+}
+
 }  // namespace
 
 void note_cuda_error(cudaError_t e) { t_last_cuda_error = static_cast<int>(e); }
@@ -237,7 +269,7 @@ extern "C" {
 
 static int bf16_impl(int variant, const void* A, const void* B, void* D, int64_t M, int64_t N,
                      int64_t K, int64_t lda, int64_t ldb, int64_t ldd, void* ws, int64_t ws_bytes,
-                     cudaStream_t stream) {
+                     const gemm_epilogue_t* epi, cudaStream_t stream) {
   const int base = variant & 0xFF;
   const bool direct = (variant & GEMM_VARIANT_DIRECT_STORE) != 0;
   if ((variant & ~(0xFF | GEMM_VARIANT_DIRECT_STORE)) != 0 || base > GEMM_VARIANT_SYNC)
@@ -257,7 +289,10 @@ static int bf16_impl(int variant, const void* A, const void* B, void* D, int64_t
   p.A = A;
   p.B = B;
   p.D = D;
-  if (K == 0) return launch_zero_fill(p, stream);
+  if ((rc = parse_epilogue(epi, N, D, ldd, ctx.device, p)) != GEMM_OK) return rc;
+  if (p.epi_mode != 0 && base == GEMM_VARIANT_SYNC) return GEMM_ERR_INVALID_ARG;
+  if (K == 0)
+    return p.epi_mode != 0 ? launch_epilogue_only(p, ctx.num_sms, stream) : launch_zero_fill(p, stream);
   if (!is_device_pointer(A, ctx.device) || !is_device_pointer(B, ctx.device))
     return GEMM_ERR_INVALID_ARG;
   ctx.timeout_ns = static_cast<unsigned long long>(timeout_ns_for(K));
@@ -266,7 +301,7 @@ static int bf16_impl(int variant, const void* A, const void* B, void* D, int64_t
   p.workspace_bytes = ws_bytes > 0 ? static_cast<uint64_t>(ws_bytes) : 0u;
   if (ws != nullptr && (base == GEMM_VARIANT_SYNC || !is_device_pointer(ws, ctx.device)))
     return GEMM_ERR_INVALID_ARG;
-  const bool tma_store = tma_store_ok(D, N, ldd, direct);
+  const bool tma_store = tma_store_ok(D, N, ldd, direct) && !(p.epi_mode & kEpiOutF32);
   switch (base) {
     case GEMM_VARIANT_SYNC:
       return launch_bf16_sync(p, ctx, stream);
@@ -281,14 +316,22 @@ static int bf16_impl(int variant, const void* A, const void* B, void* D, int64_t
 
 int gemm_bf16_variant(int variant, const void* A, const void* B, void* D, int64_t M, int64_t N,
                       int64_t K, int64_t lda, int64_t ldb, int64_t ldd, cudaStream_t stream) {
-  return bf16_impl(variant, A, B, D, M, N, K, lda, ldb, ldd, nullptr, 0, stream);
+  return bf16_impl(variant, A, B, D, M, N, K, lda, ldb, ldd, nullptr, 0, nullptr, stream);
 }
 
 int gemm_bf16_streamk(int variant, const void* A, const void* B, void* D, int64_t M, int64_t N,
                       int64_t K, int64_t lda, int64_t ldb, int64_t ldd, void* workspace,
                       int64_t workspace_bytes, cudaStream_t stream) {
   if (workspace == nullptr) return GEMM_ERR_INVALID_ARG;
-  return bf16_impl(variant, A, B, D, M, N, K, lda, ldb, ldd, workspace, workspace_bytes, stream);
+  return bf16_impl(variant, A, B, D, M, N, K, lda, ldb, ldd, workspace, workspace_bytes, nullptr,
+                   stream);
+}
+
+int gemm_bf16_fused(int variant, const void* A, const void* B, void* D, int64_t M, int64_t N,
+                    int64_t K, int64_t lda, int64_t ldb, int64_t ldd, const gemm_epilogue_t* epi,
+                    cudaStream_t stream) {
+  if ((variant & 0xFF) == GEMM_VARIANT_SYNC) return GEMM_ERR_INVALID_ARG;
+  return bf16_impl(variant, A, B, D, M, N, K, lda, ldb, ldd, nullptr, 0, epi, stream);
 }
 
 int gemm_bf16(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
@@ -299,7 +342,7 @@ int gemm_bf16(const void* A, const void* B, void* D, int64_t M, int64_t N, int64
 static int mxfp8_impl(int variant, const void* A, const void* B, const void* SFA,
                       const void* SFB, void* D, int64_t M, int64_t N, int64_t K, int64_t lda,
                       int64_t ldb, int64_t ldsfa, int64_t ldsfb, int64_t ldd, void* ws,
-                      int64_t ws_bytes, cudaStream_t stream) {
+                      int64_t ws_bytes, const gemm_epilogue_t* epi, cudaStream_t stream) {
   const int base = variant & 0xFF;
   const bool direct = (variant & GEMM_VARIANT_DIRECT_STORE) != 0;
   if ((variant & ~(0xFF | GEMM_VARIANT_DIRECT_STORE)) != 0 || base > GEMM_VARIANT_2CTA)
@@ -331,7 +374,9 @@ static int mxfp8_impl(int variant, const void* A, const void* B, const void* SFA
   p.SFA = SFA;
   p.SFB = SFB;
   p.D = D;
-  if (K == 0) return launch_zero_fill(p, stream);
+  if ((rc = parse_epilogue(epi, N, D, ldd, ctx.device, p)) != GEMM_OK) return rc;
+  if (K == 0)
+    return p.epi_mode != 0 ? launch_epilogue_only(p, ctx.num_sms, stream) : launch_zero_fill(p, stream);
   if (!is_device_pointer(A, ctx.device) || !is_device_pointer(B, ctx.device) ||
       !is_device_pointer(SFA, ctx.device) || !is_device_pointer(SFB, ctx.device))
     return GEMM_ERR_INVALID_ARG;
@@ -343,7 +388,8 @@ static int mxfp8_impl(int variant, const void* A, const void* B, const void* SFA
   // The automatic MXFP8 choice is the single-CTA kernel with the masked-store
   // epilogue: without TMA-store staging it keeps four operand stages, which
   // measures faster than three stages with TMA stores.
-  const bool tma_store = base != GEMM_VARIANT_AUTO && tma_store_ok(D, N, ldd, direct);
+  const bool tma_store = base != GEMM_VARIANT_AUTO && tma_store_ok(D, N, ldd, direct) &&
+                         !(p.epi_mode & kEpiOutF32);
   return launch_mxf8_ws(base == GEMM_VARIANT_2CTA ? 2 : 1, tma_store, p, ctx, stream);
 }
 
@@ -352,7 +398,15 @@ int gemm_mxfp8_variant(int variant, const void* A, const void* B, const void* SF
                        int64_t ldb, int64_t ldsfa, int64_t ldsfb, int64_t ldd,
                        cudaStream_t stream) {
   return mxfp8_impl(variant, A, B, SFA, SFB, D, M, N, K, lda, ldb, ldsfa, ldsfb, ldd, nullptr, 0,
-                    stream);
+                    nullptr, stream);
+}
+
+int gemm_mxfp8_fused(int variant, const void* A, const void* B, const void* SFA, const void* SFB,
+                     void* D, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                     int64_t ldsfa, int64_t ldsfb, int64_t ldd, const gemm_epilogue_t* epi,
+                     cudaStream_t stream) {
+  return mxfp8_impl(variant, A, B, SFA, SFB, D, M, N, K, lda, ldb, ldsfa, ldsfb, ldd, nullptr, 0,
+                    epi, stream);
 }
 
 int gemm_mxfp8_streamk(int variant, const void* A, const void* B, const void* SFA,
@@ -361,7 +415,7 @@ int gemm_mxfp8_streamk(int variant, const void* A, const void* B, const void* SF
                        int64_t workspace_bytes, cudaStream_t stream) {
   if (workspace == nullptr) return GEMM_ERR_INVALID_ARG;
   return mxfp8_impl(variant, A, B, SFA, SFB, D, M, N, K, lda, ldb, ldsfa, ldsfb, ldd, workspace,
-                    workspace_bytes, stream);
+                    workspace_bytes, nullptr, stream);
 }
 
 int64_t gemm_streamk_workspace_bytes(int mxfp8, int variant) {

@@ -20,6 +20,12 @@ struct Problem {
   uint32_t stall_iter = 0xFFFFFFFFu;   // watchdog test hook (see gemm_debug_stall_next_launch)
   void* workspace = nullptr;           // stream-K partials + flags (nullptr: data-parallel only)
   uint64_t workspace_bytes = 0;
+  // fused epilogue (epi_mode bits in kernel_common.cuh; 0 = plain bf16 store)
+  uint32_t epi_mode = 0;
+  float alpha = 1.0f, beta = 0.0f;
+  const void* C = nullptr;
+  uint64_t ldc = 0;
+  const void* bias = nullptr;
 };
 
 // Stream-K workspace per CTA: 4 epilogue warps x 32 rows x tile_n fp32, plus
@@ -117,6 +123,8 @@ int launch_bf16_sync(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream
 int launch_mxf8_ws(int cg, bool tma_store, const Problem& p, const LaunchCtx& ctx,
                    cudaStream_t stream);
 int launch_zero_fill(const Problem& p, cudaStream_t stream);
+// K == 0 with a fused epilogue: D = act(alpha * 0 + beta * C + bias).
+int launch_epilogue_only(const Problem& p, int num_sms, cudaStream_t stream);
 int launch_mxfp8_quantize(const float* X, uint32_t rows, uint32_t K, uint64_t ldx, uint8_t* Q,
                           uint64_t ldq, uint8_t* SF, uint64_t ldsf, int num_sms,
                           cudaStream_t stream);

@@ -48,6 +48,12 @@ struct GemmArgs {
   float* ws_part;             // stream-K partial accumulators, one slot per cluster
   uint32_t* ws_flag;          // per (slot, CTA, epilogue warp) ready flags
   uint32_t epoch;             // this launch's flag value (never 0)
+  // Fused epilogue: v = alpha acc + beta C + bias[col], act(v) (mode 0: none)
+  uint32_t epi_mode;
+  float alpha, beta;
+  const void* C;
+  uint64_t ldc;
+  const void* bias;
 };
 
 // One piece of work for a cluster: K-tiles [k_begin, k_end) of a tile.
@@ -380,6 +386,112 @@ __device__ __forceinline__ void store_chunk32_staged(uint8_t* buf, uint16_t* D, 
     }
   }
   __syncwarp();
+}
+
+// ------------------------------------------------------------ fused epilogue
+
+__device__ __forceinline__ float epi_act(float x, uint32_t act) {
+  if (act == kActRelu) return x < 0.0f ? 0.0f : x;                        // NaN kept
+  if (act == kActGelu) return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
+  return x;
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t h) { return __uint_as_float(h << 16); }
+
+// 32 consecutive values starting at p (the first n valid, the rest 0) of
+// fp32 or bf16 type, with 16-byte loads where the address allows.
+template <bool F32>
+__device__ __forceinline__ void load_row32(const void* p, uint32_t n, float (&x)[32]) {
+  if constexpr (F32) {
+    const float* q = static_cast<const float*>(p);
+    if (n == 32 && (reinterpret_cast<uintptr_t>(q) & 15u) == 0) {
+#pragma unroll
+      for (uint32_t i = 0; i < 8; ++i) {
+        const float4 t = __ldg(reinterpret_cast<const float4*>(q) + i);
+        x[4 * i] = t.x; x[4 * i + 1] = t.y; x[4 * i + 2] = t.z; x[4 * i + 3] = t.w;
+      }
+    } else {
+#pragma unroll
+      for (uint32_t t = 0; t < 32; ++t) x[t] = t < n ? __ldg(q + t) : 0.0f;
+    }
+  } else {
+    const uint16_t* q = static_cast<const uint16_t*>(p);
+    if (n == 32 && (reinterpret_cast<uintptr_t>(q) & 15u) == 0) {
+#pragma unroll
+      for (uint32_t i = 0; i < 4; ++i) {
+        const uint4 t = __ldg(reinterpret_cast<const uint4*>(q) + i);
+        const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+        for (uint32_t k = 0; k < 4; ++k) {
+          x[8 * i + 2 * k] = bf16_bits_to_f32(w[k] & 0xFFFFu);
+          x[8 * i + 2 * k + 1] = bf16_bits_to_f32(w[k] >> 16);
+        }
+      }
+    } else {
+#pragma unroll
+      for (uint32_t t = 0; t < 32; ++t) x[t] = t < n ? bf16_bits_to_f32(__ldg(q + t)) : 0.0f;
+    }
+  }
+}
+
+// The fused epilogue on one thread's 32 accumulators: row `row`, columns
+// col0 .. col0 + 31 (columns >= N and rows >= M read nothing):
+// v = alpha * acc + beta * C[row, col] + bias[col], then the activation, in fp32.
+__device__ __forceinline__ void epi_apply(uint32_t (&v)[32], const GemmArgs& a, uint32_t row,
+                                          uint32_t col0) {
+  const uint32_t mode = a.epi_mode;
+  const uint32_t n = col0 < a.N ? min(32u, a.N - col0) : 0u;
+  float x[32];
+#pragma unroll
+  for (uint32_t t = 0; t < 32; ++t) x[t] = __uint_as_float(v[t]);
+  if (mode & kEpiAlpha) {
+#pragma unroll
+    for (uint32_t t = 0; t < 32; ++t) x[t] *= a.alpha;
+  }
+  if ((mode & kEpiC) && row < a.M && n > 0) {
+    float c[32];
+    if (mode & kEpiOutF32)
+      load_row32<true>(static_cast<const float*>(a.C) + static_cast<uint64_t>(row) * a.ldc + col0, n, c);
+    else
+      load_row32<false>(static_cast<const uint16_t*>(a.C) + static_cast<uint64_t>(row) * a.ldc + col0, n, c);
+#pragma unroll
+    for (uint32_t t = 0; t < 32; ++t) x[t] = fmaf(a.beta, c[t], x[t]);
+  }
+  if ((mode & kEpiBias) && n > 0) {
+    float b[32];
+    if (mode & kEpiBiasF32)
+      load_row32<true>(static_cast<const float*>(a.bias) + col0, n, b);
+    else
+      load_row32<false>(static_cast<const uint16_t*>(a.bias) + col0, n, b);
+#pragma unroll
+    for (uint32_t t = 0; t < 32; ++t) x[t] += b[t];
+  }
+  const uint32_t act = (mode >> kEpiActShift) & 3u;
+  if (act != 0) {
+#pragma unroll
+    for (uint32_t t = 0; t < 32; ++t) x[t] = epi_act(x[t], act);
+  }
+#pragma unroll
+  for (uint32_t t = 0; t < 32; ++t) v[t] = __float_as_uint(x[t]);
+}
+
+// fp32 output: one thread's row segment of 32 values (one 128-byte line when
+// aligned), masked against M and N.
+__device__ __forceinline__ void store_row32_f32(float* D, uint64_t ldd, uint32_t M, uint32_t N,
+                                                uint32_t row, uint32_t col0, const uint32_t (&v)[32]) {
+  if (row >= M || col0 >= N) return;
+  const uint32_t n = min(32u, N - col0);
+  float* dp = D + static_cast<uint64_t>(row) * ldd + col0;
+  if (n == 32 && (reinterpret_cast<uintptr_t>(dp) & 15u) == 0) {
+#pragma unroll
+    for (uint32_t i = 0; i < 8; ++i)
+      reinterpret_cast<float4*>(dp)[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                                     __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+  } else {
+#pragma unroll
+    for (uint32_t t = 0; t < 32; ++t)
+      if (t < n) dp[t] = __uint_as_float(v[t]);
+  }
 }
 
 template <int CG, Kind KIND, bool TMA_STORE>
@@ -769,6 +881,10 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
               if (!add_partials(v0, 2 * c)) { ok = false; break; }
               if (2 * c + 1 < live && !add_partials(v1, 2 * c + 1)) { ok = false; break; }
             }
+            if (args.epi_mode != 0) {
+              epi_apply(v0, args, row0 + lane, col_base + c * 64);
+              epi_apply(v1, args, row0 + lane, col_base + c * 64 + 32);
+            }
             const uint32_t buf = epi0 + (ew * C::EPI_BUFS + (chunk_ctr % C::EPI_BUFS)) * C::EPI_BUF_BYTES;
             if (lane == 0) bulk_wait_group_read<C::EPI_BUFS - 1>();   // this buffer's last store has read it
             __syncwarp();
@@ -806,9 +922,14 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
             tmem_ld_32x32b_x32(t_addr + c * 32, v);
             tmem_wait_ld();
             if (w.kind == 1 && !add_partials(v, c)) { ok = false; break; }
-            store_chunk32_staged(base_ptr + (epi0 - base) + ew * C::CHUNK_BYTES,
-                                 static_cast<uint16_t*>(args.D), args.ldd, args.M, args.N, row0,
-                                 col_base + c * 32, v, lane);
+            if (args.epi_mode != 0) epi_apply(v, args, row0 + lane, col_base + c * 32);
+            if (args.epi_mode & kEpiOutF32)
+              store_row32_f32(static_cast<float*>(args.D), args.ldd, args.M, args.N, row0 + lane,
+                              col_base + c * 32, v);
+            else
+              store_chunk32_staged(base_ptr + (epi0 - base) + ew * C::CHUNK_BYTES,
+                                   static_cast<uint16_t*>(args.D), args.ldd, args.M, args.N, row0,
+                                   col_base + c * 32, v, lane);
           }
         }
       }

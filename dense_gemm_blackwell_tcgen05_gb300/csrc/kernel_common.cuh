@@ -24,6 +24,16 @@ enum WaitSite : uint32_t {
   kSiteStreamKFlag = 9,     // stream-K owner waiting for a partial accumulator
 };
 
+// Fused-epilogue mode word (0: the plain bf16 store of the accumulator).
+constexpr uint32_t kEpiOutF32 = 1u;    // D (and C) hold fp32
+constexpr uint32_t kEpiC = 2u;         // + beta * C
+constexpr uint32_t kEpiBias = 4u;      // + bias[column]
+constexpr uint32_t kEpiBiasF32 = 8u;   // bias holds fp32 (else bf16)
+constexpr uint32_t kEpiAlpha = 16u;    // alpha != 1
+constexpr uint32_t kEpiActShift = 8u;  // activation code in bits 8..9
+constexpr uint32_t kActRelu = 1u;
+constexpr uint32_t kActGelu = 2u;
+
 struct Watchdog {
   unsigned long long* status;       // library-owned device status word
   unsigned long long timeout_ns;    // per-wait limit

@@ -100,6 +100,12 @@ int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) 
   a.ws_part = nullptr;
   a.ws_flag = nullptr;
   a.epoch = 0;
+  a.epi_mode = p.epi_mode;
+  a.alpha = p.alpha;
+  a.beta = p.beta;
+  a.C = p.C;
+  a.ldc = p.ldc;
+  a.bias = p.bias;
 
   const uint64_t tiles = static_cast<uint64_t>(a.num_m_blocks) * a.num_n_blocks;
   const uint64_t resident = CG == 2 ? static_cast<uint64_t>(max_clusters[ctx.device])

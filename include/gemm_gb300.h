@@ -109,6 +109,55 @@ int gemm_mxfp8_variant(int variant, const void* A, const void* B, const void* SF
                        cudaStream_t stream);
 
 /*
+ * Fused epilogue, applied to the fp32 accumulator on its way from TMEM to
+ * memory (the readback step where "cast/epilogue/store" happen:
+ * b200-tmem-lifecycle-planner, "A1 -- Case 1: dense MMA accumulator";
+ * custom fusion is the reason to own the kernel: b200-gemm-optimization-
+ * ladder, "B -- Boundaries", "Do not use when").  The pages name no
+ * particular epilogue; this is the plain linear-layer one, in fp32:
+ *
+ *     v = alpha * acc + beta * C[i,j] + bias[j]          (terms absent when NULL)
+ *     D[i,j] = act(v), rounded once to the output type (RNE)
+ *
+ * act: GEMM_ACT_NONE; GEMM_ACT_RELU (0 where v < 0, NaN kept); GEMM_ACT_GELU
+ * v * Phi(v) = v (1 + erf(v / sqrt 2)) / 2.
+ * out_dtype: GEMM_DTYPE_BF16 or GEMM_DTYPE_F32; it is also C's type.  C is
+ * [M, N] with pitch ldc >= N elements, any alignment; C may be D itself
+ * (in-place update) only with ldc == ldd, and must not overlap D otherwise.
+ * bias: N values of bias_dtype (GEMM_DTYPE_BF16 or GEMM_DTYPE_F32), any
+ * alignment.  All pointers are device pointers.
+ */
+enum { GEMM_DTYPE_BF16 = 0, GEMM_DTYPE_F32 = 1 };
+enum { GEMM_ACT_NONE = 0, GEMM_ACT_RELU = 1, GEMM_ACT_GELU = 2 };
+typedef struct gemm_epilogue {
+  float alpha;
+  float beta;
+  const void* C;
+  int64_t ldc;
+  const void* bias;
+  int32_t bias_dtype;
+  int32_t activation;
+  int32_t out_dtype;
+  int32_t reserved;  /* must be 0 */
+} gemm_epilogue_t;
+
+/* gemm_bf16_variant / gemm_mxfp8_variant with a fused epilogue (variants 0,
+ * 1, 2, optionally | GEMM_VARIANT_DIRECT_STORE; an fp32 output always uses
+ * the masked-store epilogue).  `epi` NULL means alpha = 1 and nothing else
+ * (the plain entry points).  D holds elements of epi->out_dtype with pitch
+ * ldd.  K == 0 gives D = act(alpha * 0 + beta * C + bias).  Errors as the
+ * plain entry points, plus GEMM_ERR_INVALID_ARG for an unknown dtype or
+ * activation, reserved != 0, ldc < N, a host C or bias, or C == D with
+ * ldc != ldd; GEMM_VARIANT_SYNC is not offered. */
+int gemm_bf16_fused(int variant, const void* A, const void* B, void* D, int64_t M, int64_t N,
+                    int64_t K, int64_t lda, int64_t ldb, int64_t ldd, const gemm_epilogue_t* epi,
+                    cudaStream_t stream);
+int gemm_mxfp8_fused(int variant, const void* A, const void* B, const void* SFA, const void* SFB,
+                     void* D, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                     int64_t ldsfa, int64_t ldsfb, int64_t ldd, const gemm_epilogue_t* epi,
+                     cudaStream_t stream);
+
+/*
  * Stream-K schedule (the scheduler row "dynamic / stream-K scheduling" of the
  * optimisation ladder's persistent level: "check the tail and tile order",
  * b200-gemm-optimization-ladder, "E -- Executable steps", level 6).  Same

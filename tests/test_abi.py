@@ -147,3 +147,42 @@ def test_streamk_workspace_query_without_device():
 def test_noalloc_variant_checked_before_device_setup():
     assert g.gemm_bf16_streamk_noalloc(3, FAKE, FAKE, FAKE, 4, 4, 16, 16, 16, 4, 0) == \
         g.GEMM_ERR_INVALID_ARG
+
+
+def test_epilogue_struct_layout_matches_the_header(tmp_path):
+    """The ctypes mirror of gemm_epilogue_t has the C compiler's layout."""
+    import ctypes
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "layout.c"
+    src.write_text(
+        '#include <stdio.h>\n#include <stddef.h>\n#include "gemm_gb300.h"\n'
+        "int main(void) { printf(\"%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\\n\", sizeof(gemm_epilogue_t),"
+        " offsetof(gemm_epilogue_t, alpha), offsetof(gemm_epilogue_t, beta),"
+        " offsetof(gemm_epilogue_t, C), offsetof(gemm_epilogue_t, ldc),"
+        " offsetof(gemm_epilogue_t, bias), offsetof(gemm_epilogue_t, bias_dtype),"
+        " offsetof(gemm_epilogue_t, activation), offsetof(gemm_epilogue_t, out_dtype),"
+        " offsetof(gemm_epilogue_t, reserved)); return 0; }\n")
+    exe = tmp_path / "layout"
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    subprocess.run(["gcc", "-I", inc, "-o", str(exe), str(src)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    E = g.GemmEpilogue
+    want = [ctypes.sizeof(E)] + [getattr(E, f).offset for f in
+                                 ("alpha", "beta", "C", "ldc", "bias", "bias_dtype", "activation",
+                                  "out_dtype", "reserved")]
+    assert got == want
+
+
+def test_fused_validation_without_device():
+    e = g.GemmEpilogue()
+    e.alpha = 1.0
+    # the synchronous ladder kernels take no epilogue; checked before any device work
+    assert g.gemm_bf16_fused(3, FAKE, FAKE, FAKE, 4, 4, 16, 16, 16, 4, e, 0) == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_bf16_fused(0x40, FAKE, FAKE, FAKE, 4, 4, 16, 16, 16, 4, e, 0) == \
+        g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_bf16_fused(2, FAKE, FAKE, FAKE, -1, 4, 16, 16, 16, 4, e, 0) == \
+        g.GEMM_ERR_INVALID_ARG
