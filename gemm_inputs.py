@@ -19,7 +19,16 @@ square_8192            M=N=K=8192, 0.5*N(0,1) -> bf16          3
 mxfp8_8192             M=N=K=8192, N(0,1) -> MXFP8             4
 quantize_8192          [8192, 8192] float32 N(0,1) (the A       4
                        operand above, before encoding)
+fused_gelu_8192        square_8192's A, B; C [M,N] N(0,1) ->   3 (+100 for C,
+                       bf16, bias [N] N(0,1) -> bf16             bias)
+fused_f32_8192         square_8192's A, B; bias [N] N(0,1)     3 (+100)
+                       float32
+streamk_1024x16384     M=N=1024, K=16384, N(0,1) -> bf16       5
+streamk_mxfp8_1024x32768  M=N=1024, K=32768, N(0,1) -> MXFP8   6
 ===================== ===================================== ==================
+
+Epilogue inputs come from a second generator seeded with seed + 100: C
+first (when the workload has one), then the bias vector.
 
 bf16 rounding is torch's float32 -> bfloat16 cast (round-to-nearest-even).
 MXFP8 encoding of a float32 row: for each block of 32 consecutive k (the
@@ -48,6 +57,11 @@ class Workload:
     dist: str            # "uniform" | "normal"
     scale: float = 1.0
     kind: str = "bf16"   # "bf16" | "mxfp8" | "quant" (MXFP8 encoding of float32 rows [M, K])
+    # fused epilogue: "" (plain bf16 store), or "alpha,beta,act,out,bias" with
+    # act none|relu|gelu, out bf16|f32, bias none|bf16|f32 (beta != 0 adds C)
+    epilogue: str = ""
+    schedule: str = "dp"  # "dp" | "streamk" (caller workspace, automatic split)
+    variant: int = 0      # kernel variant the bench runs it with (0 = automatic)
 
     @property
     def flops(self) -> int:
@@ -63,8 +77,39 @@ WORKLOADS = {
         Workload("square_8192", 8192, 8192, 8192, 3, "normal", 0.5),
         Workload("mxfp8_8192", 8192, 8192, 8192, 4, "normal", 1.0, "mxfp8"),
         Workload("quantize_8192", 8192, 0, 8192, 4, "normal", 1.0, "quant"),
+        Workload("fused_gelu_8192", 8192, 8192, 8192, 3, "normal", 0.5, "bf16",
+                 epilogue="1.0,1.0,gelu,bf16,bf16"),
+        Workload("fused_f32_8192", 8192, 8192, 8192, 3, "normal", 0.5, "bf16",
+                 epilogue="0.5,0.0,relu,f32,f32"),
+        Workload("streamk_1024x16384", 1024, 1024, 16384, 5, "normal", 1.0, "bf16",
+                 schedule="streamk"),
+        Workload("streamk_mxfp8_1024x32768", 1024, 1024, 32768, 6, "normal", 1.0, "mxfp8",
+                 schedule="streamk"),
     ]
 }
+
+
+def epilogue_spec(w: Workload) -> dict | None:
+    """The parsed epilogue string of a workload (None: plain store)."""
+    if not w.epilogue:
+        return None
+    alpha, beta, act, out, bias = w.epilogue.split(",")
+    return {"alpha": float(alpha), "beta": float(beta), "act": act, "out": out, "bias": bias}
+
+
+def epilogue_operands(w: Workload):
+    """(C or None, bias or None) of a fused-epilogue workload: C [M, N] in the
+    output dtype, bias [N] in its dtype, drawn N(0,1) from seed + 100."""
+    spec = epilogue_spec(w)
+    if spec is None:
+        return None, None
+    g = torch.Generator().manual_seed(w.seed + 100)
+    out_dt = torch.float32 if spec["out"] == "f32" else torch.bfloat16
+    C = torch.randn(w.M, w.N, generator=g).to(out_dt) if spec["beta"] != 0.0 else None
+    bias = None
+    if spec["bias"] != "none":
+        bias = torch.randn(w.N, generator=g).to(torch.float32 if spec["bias"] == "f32" else torch.bfloat16)
+    return C, bias
 
 
 def _draw(g: torch.Generator, rows: int, cols: int, dist: str, scale: float) -> torch.Tensor:
