@@ -165,8 +165,9 @@ struct GemmCfg {
   // w0 TMA producer, w1 MMA issuer / TMEM owner, w2..5 epilogue and, for
   // MXFP8, w6: the scale-factor warp.  It re-tiles each stage's scale bytes as
   // soon as they land (their own barrier) and then arrives on the leader's
-  // ready barrier, which keeps that work off the MMA issuer's path.
-  static constexpr uint32_t kThreads = MX ? 224 : 192;
+  // ready barrier, which keeps that work off the MMA issuer's path.  Kernels
+  // with the masked-store epilogue and two accumulator buffers add a second
+  // epilogue warpgroup after those (see EPI_WG).
   static constexpr uint32_t kSfWarp = 6;
   static constexpr uint32_t BLOCK_M = 128;    // D rows owned by one CTA (= TMEM lanes)
   static constexpr uint32_t UMMA_M = 128 * CG;
@@ -216,6 +217,13 @@ struct GemmCfg {
   // TMEM: ACC_STAGES accumulators of UMMA_N fp32 columns, then the scale
   // factors (MXFP8: 4 columns for A, 4 per 128 B rows).  512 = whole TMEM.
   static constexpr uint32_t ACC_STAGES = (MX && CG == 1) ? 1 : 2;
+  // Epilogue warpgroups (the ladder's multi-consumer level): with two, group
+  // g drains accumulator buffer g, so two tiles' epilogues run at once.  Used
+  // where the epilogue is the slow consumer -- the masked-store path, whose
+  // staging costs 2 KB per warp -- when there are two buffers to drain.
+  static constexpr uint32_t EPI_WG = (!TMA_STORE && ACC_STAGES == 2) ? 2 : 1;
+  static constexpr uint32_t kEpiWg1Warp = MX ? 7 : 6;   // first warp of group 1
+  static constexpr uint32_t kThreads = 32 * (kEpiWg1Warp + 4 * (EPI_WG - 1));
   static constexpr uint32_t SF_TMEM_COL = ACC_STAGES * UMMA_N;
   static constexpr uint32_t TMEM_COLS = 512;
   static_assert(SF_TMEM_COL + (MX ? 4 + 4 * SFB_CHUNKS : 0) <= TMEM_COLS, "TMEM column budget");
@@ -229,7 +237,8 @@ struct GemmCfg {
   static constexpr uint32_t EPI_BUF_BYTES = 32 * 128;
   static constexpr uint32_t EPI_BUFS = 2;
   static constexpr uint32_t CHUNK_BYTES = 32 * 64;
-  static constexpr uint32_t EPI_BYTES = TMA_STORE ? 4 * EPI_BUFS * EPI_BUF_BYTES : 4 * CHUNK_BYTES;
+  static constexpr uint32_t EPI_BYTES =
+      TMA_STORE ? 4 * EPI_BUFS * EPI_BUF_BYTES : 4 * EPI_WG * CHUNK_BYTES;
 
   static constexpr uint32_t SMEM_LIMIT = 232448;  // 227 KB opt-in per CTA
   static constexpr uint32_t BAR_BYTES = 512;
@@ -773,10 +782,12 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
     if (lane == 0 && *abort_flag)
       for (uint32_t i = gi; i < issued; ++i)
         drain_wait(raw_full_bar(i % C::RAW_SLOTS), (i / C::RAW_SLOTS) & 1u, wd, kSiteProducerDrain);
-  } else if (warp >= 2 && warp < 6) {
-    // ==================== epilogue: four warps, one TMEM lane quarter each =========
+  } else if ((warp >= 2 && warp < 6) ||
+             (C::EPI_WG == 2 && warp >= C::kEpiWg1Warp && warp < C::kEpiWg1Warp + 4)) {
+    // ==================== epilogue: four warps per group, one TMEM lane quarter each ===
+    const uint32_t eg = warp < 6 ? 0u : 1u;  // epilogue group (drains accumulator buffer eg)
     const uint32_t q = warp & 3u;            // TMEM lanes 32q .. 32q+31
-    const uint32_t ew = warp - 2u;           // staging slot owner
+    const uint32_t ew = eg == 0 ? warp - 2u : 4u + warp - C::kEpiWg1Warp;   // staging slot owner
     constexpr uint32_t NCH = C::UMMA_N / 32;
     uint32_t j = 0, chunk_ctr = 0;
     bool ok = true;
@@ -786,8 +797,10 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
       return args.ws_part + (static_cast<uint64_t>(slot * CG + rank) * 4 + q) * (32u * C::UMMA_N);
     };
     const auto flag_ptr = [&](uint32_t slot) { return args.ws_flag + (slot * CG + rank) * 4 + q; };
-    const auto fix_slot = [&](uint32_t r) { return stage0 + (ew * C::FIX_SLOTS + r) * C::FIX_SLOT_BYTES; };
-    const auto fix_bar = [&](uint32_t r) { return bar0 + 8 * (kFixBar0 + ew * C::FIX_SLOTS + r); };
+    // (the ring is per lane quarter: only one group ever runs a fix-up, on the
+    // CTA's last item)
+    const auto fix_slot = [&](uint32_t r) { return stage0 + (q * C::FIX_SLOTS + r) * C::FIX_SLOT_BYTES; };
+    const auto fix_bar = [&](uint32_t r) { return bar0 + 8 * (kFixBar0 + q * C::FIX_SLOTS + r); };
     // owner-side transfer stream: transfer n = chunk (n / nc) of contributor
     // cluster_id + 1 + (n % nc); issued FIX_SLOTS ahead by lane 0
     uint32_t nc = 0, nfix = 0, fix_issued = 0, fix_done = 0;
@@ -825,6 +838,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
     for (uint32_t wi = 0; ok && work_item(args, cluster_id, num_clusters, KT, wi, w); ++wi, ++j) {
       const uint32_t b = j % C::ACC_STAGES;
       const uint32_t around = j / C::ACC_STAGES;
+      if (C::EPI_WG == 2 && b != eg) continue;   // the other group's buffer
       if (!warp_wait(accf_bar(b), around & 1u, wd, kSiteEpiAccFull, lane)) break;
       tc_fence_after_sync();
       uint32_t mb, nb;
