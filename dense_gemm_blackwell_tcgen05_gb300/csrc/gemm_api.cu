@@ -272,7 +272,9 @@ static int bf16_impl(int variant, const void* A, const void* B, void* D, int64_t
                      const gemm_epilogue_t* epi, cudaStream_t stream) {
   const int base = variant & 0xFF;
   const bool direct = (variant & GEMM_VARIANT_DIRECT_STORE) != 0;
-  if ((variant & ~(0xFF | GEMM_VARIANT_DIRECT_STORE)) != 0 || base > GEMM_VARIANT_SYNC)
+  if ((variant & ~(0xFF | GEMM_VARIANT_DIRECT_STORE)) != 0 || base > GEMM_VARIANT_SMALLK)
+    return GEMM_ERR_INVALID_ARG;
+  if (base == GEMM_VARIANT_SMALLK && (ws != nullptr || epi != nullptr || K > smallk_max_k()))
     return GEMM_ERR_INVALID_ARG;
   int rc = check_shape(A, B, D, M, N, K, lda, ldb, ldd, 2);
   if (rc != GEMM_OK || M == 0 || N == 0) return rc;
@@ -302,7 +304,13 @@ static int bf16_impl(int variant, const void* A, const void* B, void* D, int64_t
   if (ws != nullptr && (base == GEMM_VARIANT_SYNC || !is_device_pointer(ws, ctx.device)))
     return GEMM_ERR_INVALID_ARG;
   const bool tma_store = tma_store_ok(D, N, ldd, direct) && !(p.epi_mode & kEpiOutF32);
+  // Small K is a write of D: the CUDA-core kernel unless the call needs the
+  // persistent kernel's extras (an epilogue, a stream-K workspace).
+  if (base == GEMM_VARIANT_AUTO && K <= smallk_max_k() && p.epi_mode == 0 && ws == nullptr)
+    return launch_bf16_smallk(p, stream);
   switch (base) {
+    case GEMM_VARIANT_SMALLK:
+      return launch_bf16_smallk(p, stream);
     case GEMM_VARIANT_SYNC:
       return launch_bf16_sync(p, ctx, stream);
     case GEMM_VARIANT_1CTA:

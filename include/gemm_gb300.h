@@ -73,13 +73,18 @@ typedef enum {
                                    (ladder level 8)                                */
   GEMM_VARIANT_SYNC = 3,        /* one 128x128 tile per CTA, synchronous copies
                                    (ladder levels 1-3; bf16 only, reference rung)  */
+  GEMM_VARIANT_SMALLK = 4,      /* bf16 only, 1 <= K <= 16: CUDA-core kernel for
+                                   the HBM-bound case (a write of D at about 8
+                                   flops per byte), coalesced row stores; AUTO
+                                   picks it for plain calls with K <= 16           */
   GEMM_VARIANT_DIRECT_STORE = 0x100  /* flag: masked st.global epilogue instead of
                                         TMA stores, even when D is aligned         */
 } gemm_variant_t;
 
 /*
  * bf16 GEMM: D = A * B^T with A, B, D bf16 (IEEE bfloat16 bit patterns).
- * Runs the persistent tcgen05 kernel chosen for the shape (GEMM_VARIANT_AUTO).
+ * Runs the persistent tcgen05 kernel chosen for the shape (GEMM_VARIANT_AUTO),
+ * or, for K <= 16, the small-K CUDA-core kernel (GEMM_VARIANT_SMALLK).
  */
 int gemm_bf16(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
               int64_t lda, int64_t ldb, int64_t ldd, cudaStream_t stream);

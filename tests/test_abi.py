@@ -96,6 +96,18 @@ def test_no_device_is_reported_not_crashed():
     assert g.gemm_bf16(FAKE, FAKE, FAKE, 4, 4, 16, 16, 16, 4, 0) == g.GEMM_ERR_UNSUPPORTED_DEVICE
 
 
+def test_smallk_plan_and_validation():
+    p = g.gemm_kernel_plan(False, g.VARIANT_SMALLK)
+    assert p["tmem_cols"] == 0 and p["threads"] == 256 and p["tile_n"] == 256
+    # K beyond the small-K limit, a workspace or an epilogue: refused before device work
+    assert g.gemm_bf16_variant(4, FAKE, FAKE, FAKE, 4, 4, 17, 24, 24, 4, 0) == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_bf16_streamk(4, FAKE, FAKE, FAKE, 4, 4, 8, 8, 8, 4, FAKE, 1 << 20, 0) == \
+        g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_bf16_fused(4, FAKE, FAKE, FAKE, 4, 4, 8, 8, 8, 4, g.GemmEpilogue(), 0) == \
+        g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_bf16_variant(5, FAKE, FAKE, FAKE, 4, 4, 8, 8, 8, 4, 0) == g.GEMM_ERR_INVALID_ARG
+
+
 @pytest.mark.parametrize("mx, variant", [(0, 1), (0, 2), (0, 3), (0, 0x101), (0, 0x102), (1, 1), (1, 0x101),
                                         (1, 2)])
 def test_kernel_plans_fit_the_sm(mx, variant):

@@ -274,3 +274,58 @@ def test_ragged_n_never_writes_padding(v, N, ldd):
     assert torch.all(host[:, N:] == torch.tensor(-1234.0).to(torch.bfloat16))
     D_ref, S = ref(A, B)
     P.check_within_bound(P.bf16_to_f64(host[:, :N]), D_ref, S, f"N={N} ldd={ldd}/{v}")
+
+
+# --------------------------------------------- small-K CUDA-core kernel (K <= 16)
+
+@pytest.mark.parametrize("v", ["smallk", "auto"])
+@pytest.mark.parametrize("M, N, K, lda, ldd", [(300, 520, 8, 8, 520), (4099, 2053, 8, 8, 2053),
+                                               (129, 257, 1, 8, 264), (257, 300, 16, 16, 301),
+                                               (33, 1031, 3, 8, 1031), (1, 1, 5, 8, 1)])
+def test_smallk_small_integers_bitwise(v, M, N, K, lda, ldd):
+    """Bitwise for both row-store forms: bf16 pairs (4-byte aligned rows) and
+    single values (odd pitch: every other row), ragged M and N, padding left
+    untouched."""
+    variant = g.VARIANT_SMALLK if v == "smallk" else g.VARIANT_AUTO
+    gen = torch.Generator().manual_seed(M + N + K)
+    A = torch.zeros(M, lda, dtype=torch.bfloat16)
+    B = torch.zeros(N, lda, dtype=torch.bfloat16)
+    A[:, :K] = torch.randint(-4, 5, (M, K), generator=gen).to(torch.bfloat16)
+    B[:, :K] = torch.randint(-4, 5, (N, K), generator=gen).to(torch.bfloat16)
+    A[:, K:] = float("nan")        # past K: never read
+    B[:, K:] = float("nan")
+    Ad, Bd = A.cuda(), B.cuda()
+    D = torch.full((M, ldd), float("nan"), dtype=torch.bfloat16, device="cuda")
+    rc = g.gemm_bf16_variant(variant, Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), M, N, K, lda,
+                             lda, ldd, 0)
+    assert rc == g.GEMM_OK, g.gemm_status_string(rc)
+    assert g.gemm_last_status(0) == g.GEMM_OK
+    D = D.cpu()
+    if ldd > N:
+        assert torch.isnan(D[:, N:].float()).all()
+    D_ref, _ = ref(A, B, K)
+    assert_bitwise(D[:, :N], D_ref)
+
+
+def test_smallk_random_within_bound():
+    A, B = gi.bf16_operands(1000, 777, 16, seed=41)
+    D = run(A, B, g.VARIANT_SMALLK)
+    D_ref, S = ref(A, B)
+    P.check_within_bound(P.bf16_to_f64(D), D_ref, S, "smallk random")
+
+
+def test_smallk_nonfinite():
+    M, N, K = 64, 300, 8
+    A = torch.ones(M, K, dtype=torch.bfloat16)
+    B = torch.ones(N, K, dtype=torch.bfloat16)
+    A[3, 2] = float("nan")
+    A[7, 0] = float("inf")
+    B[11, 0] = 0.0                          # inf * 0 = NaN at (7, 11)
+    D = run(A, B, g.VARIANT_SMALLK).float()
+    assert torch.isnan(D[3]).all()
+    assert torch.isnan(D[7, 11]) and torch.isinf(D[7, 12]) and D[7, 12] > 0
+    others = torch.ones(M, dtype=torch.bool)
+    others[[3, 7]] = False
+    cols = torch.ones(N, dtype=torch.bool)
+    cols[11] = False
+    assert torch.all(D[others][:, cols] == 8) and torch.all(D[others][:, 11] == 7)
