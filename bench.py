@@ -75,11 +75,17 @@ def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_gemm_blackwell_tcgen05_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
+        if name in PERSISTENT_KERNEL_SOURCES:
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode())
                 h.update(f.read())
     return h.hexdigest()[:16]
+
+
+# The sources of the persistent tcgen05 kernels and their launcher: the DRAM
+# counters stored under profiles/ hold while these are unchanged.
+PERSISTENT_KERNEL_SOURCES = ("ptx.cuh", "kernel_common.cuh", "gemm_kernels.cuh", "launch_ws.cuh",
+                             "gemm_host.h", "gemm_bf16.cu", "gemm_mxfp8.cu")
 
 
 def stored_traffic(kernel_key: str):
