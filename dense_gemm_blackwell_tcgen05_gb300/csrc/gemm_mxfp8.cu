@@ -1,23 +1,24 @@
 // Block-scaled MXFP8 kernels of the library (E4M3 operands, one UE8M0 scale
 // per 32 k carried into TMEM by tcgen05.cp): the single-CTA kernel and the
-// cta_group::2 pair kernel (masked-store epilogue: its 224-column tiles are
-// not a multiple of the 64-column TMA-store chunk).
+// cta_group::2 pair kernel.  Both use 224-column tiles (two accumulators and
+// the scale columns fit in 512 TMEM columns) and the masked-store epilogue:
+// 224 is not a multiple of the 64-column TMA-store chunk.
 #include "launch_ws.cuh"
 
 namespace gb300 {
 
 int launch_mxf8_ws(int cg, bool tma_store, const Problem& p, const LaunchCtx& ctx,
                    cudaStream_t stream) {
-  if (cg == 1)
-    return tma_store ? launch_ws_impl<1, Kind::MXF8, true>(p, ctx, stream)
-                     : launch_ws_impl<1, Kind::MXF8, false>(p, ctx, stream);
+  (void)tma_store;
+  if (cg == 1) return launch_ws_impl<1, Kind::MXF8, false>(p, ctx, stream);
   if (cg == 2) return launch_ws_impl<2, Kind::MXF8, false>(p, ctx, stream);
   return GEMM_ERR_INVALID_ARG;
 }
 
 bool plan_mxf8(int cg, bool tma_store, KernelPlan* out) {
+  (void)tma_store;
   if (cg == 1) {
-    tma_store ? fill_plan<1, Kind::MXF8, true>(out) : fill_plan<1, Kind::MXF8, false>(out);
+    fill_plan<1, Kind::MXF8, false>(out);
     return true;
   }
   if (cg == 2) {
