@@ -935,12 +935,10 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
             ++chunk_ctr;
           }
         } else {
-#pragma unroll 1
-          for (uint32_t c = 0; c < live; ++c) {
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(t_addr + c * 32, v);
-            tmem_wait_ld();
-            if (w.kind == 1 && !add_partials(v, c)) { ok = false; break; }
+          // One 32-column chunk at a time, software-pipelined: the next chunk's
+          // tcgen05.ld is in flight while this one is converted and stored.
+          const auto finish_chunk = [&](uint32_t (&v)[32], uint32_t c) -> bool {
+            if (w.kind == 1 && !add_partials(v, c)) return false;
             if (args.epi_mode != 0) epi_apply(v, args, row0 + lane, col_base + c * 32);
             if (args.epi_mode & kEpiOutF32)
               store_row32_f32(static_cast<float*>(args.D), args.ldd, args.M, args.N, row0 + lane,
@@ -949,6 +947,23 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
               store_chunk32_staged(base_ptr + (epi0 - base) + ew * C::CHUNK_BYTES,
                                    static_cast<uint16_t*>(args.D), args.ldd, args.M, args.N, row0,
                                    col_base + c * 32, v, lane);
+            return true;
+          };
+          uint32_t va[32], vb[32];
+          tmem_ld_32x32b_x32(t_addr, va);
+          tmem_wait_ld();
+#pragma unroll 1
+          for (uint32_t c = 0; c < live; c += 2) {
+            const bool has1 = c + 1 < live, has2 = c + 2 < live;
+            if (has1) tmem_ld_32x32b_x32(t_addr + (c + 1) * 32, vb);
+            const bool ok0 = finish_chunk(va, c);
+            if (has1) tmem_wait_ld();   // vb landed (before any exit: no load left in flight)
+            if (!ok0) { ok = false; break; }
+            if (!has1) break;
+            if (has2) tmem_ld_32x32b_x32(t_addr + (c + 2) * 32, va);
+            const bool ok1 = finish_chunk(vb, c + 1);
+            if (has2) tmem_wait_ld();
+            if (!ok1) { ok = false; break; }
           }
         }
       }

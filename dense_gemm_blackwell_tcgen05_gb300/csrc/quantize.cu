@@ -24,11 +24,13 @@ struct QuantArgs {
   uint8_t* SF;
   uint32_t rows, K;
   uint64_t ldx, ldq, ldsf;
-  uint32_t units_per_row;   // ceil(K / 512)
+  uint32_t units_per_row;   // ceil(K / kUnit)
   bool vec_in, vec_out;     // 16-byte loads / 4-byte stores are aligned everywhere
 };
 
-constexpr uint32_t kUnit = 512;   // elements per warp iteration (16 blocks of 32)
+// Elements per warp iteration (32 blocks of 32): eight 16-byte loads in flight
+// per lane; 512 measured 5% slower, 2048 slower still.
+constexpr uint32_t kUnit = 1024;
 
 // Smallest e with amax <= 448 * 2^e for a finite amax >= 0, from its bits:
 // amax = (1 + f) 2^(E-127) with 448 = 1.75 * 2^8, so e = E - 135 + (f > 0.75).
@@ -61,13 +63,13 @@ __global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const QuantArgs a) 
     const uint32_t row = static_cast<uint32_t>(u / a.units_per_row);
     const uint32_t k0 = static_cast<uint32_t>(u % a.units_per_row) * kUnit;
     const float* xr = a.X + row * a.ldx;
-    // lane l holds elements k0 + 128 j + 4 l .. +3, j = 0..3 (block 4 j + l / 8)
-    float x[4][4];
+    // lane l holds elements k0 + 128 j + 4 l .. +3, j = 0..7 (block 4 j + l / 8)
+    float x[8][4];
 #pragma unroll
-    for (uint32_t j = 0; j < 4; ++j) {
+    for (uint32_t j = 0; j < 8; ++j) {
       const uint32_t k = k0 + 128 * j + 4 * lane;
       if (a.vec_in && k + 4 <= a.K) {
-        const float4 v = *reinterpret_cast<const float4*>(xr + k);
+        const float4 v = __ldcs(reinterpret_cast<const float4*>(xr + k));   // read once
         x[j][0] = v.x; x[j][1] = v.y; x[j][2] = v.z; x[j][3] = v.w;
       } else {
 #pragma unroll
@@ -75,7 +77,7 @@ __global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const QuantArgs a) 
       }
     }
 #pragma unroll
-    for (uint32_t j = 0; j < 4; ++j) {
+    for (uint32_t j = 0; j < 8; ++j) {
       const uint32_t kb = k0 + 128 * j + 32 * (lane >> 3);   // first k of this lane's block
       float m = 0.0f;
 #pragma unroll
@@ -95,7 +97,7 @@ __global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const QuantArgs a) 
       for (uint32_t t = 0; t < 4; ++t) q |= encode_one(x[j][t], scale) << (8 * t);
       uint8_t* qr = a.Q + row * a.ldq;
       if (a.vec_out && k + 4 <= a.K) {
-        *reinterpret_cast<uint32_t*>(qr + k) = q;
+        __stcs(reinterpret_cast<unsigned int*>(qr + k), q);   // written once
       } else {
 #pragma unroll
         for (uint32_t t = 0; t < 4; ++t)
