@@ -315,8 +315,11 @@ static int bf16_impl(int variant, const void* A, const void* B, void* D, int64_t
       return launch_bf16_sync(p, ctx, stream);
     case GEMM_VARIANT_1CTA:
       return launch_bf16_ws(1, tma_store, p, ctx, stream);
-    case GEMM_VARIANT_2CTA:
     case GEMM_VARIANT_AUTO:
+      // One 128-row block of D: the pair's second CTA would multiply only
+      // zero-filled rows, and the cluster launch costs about 2 us of latency.
+      return launch_bf16_ws(M <= 128 ? 1 : 2, tma_store, p, ctx, stream);
+    case GEMM_VARIANT_2CTA:
     default:
       return launch_bf16_ws(2, tma_store, p, ctx, stream);
   }

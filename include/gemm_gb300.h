@@ -83,8 +83,9 @@ typedef enum {
 
 /*
  * bf16 GEMM: D = A * B^T with A, B, D bf16 (IEEE bfloat16 bit patterns).
- * Runs the persistent tcgen05 kernel chosen for the shape (GEMM_VARIANT_AUTO),
- * or, for K <= 16, the small-K CUDA-core kernel (GEMM_VARIANT_SMALLK).
+ * Runs the persistent tcgen05 kernel chosen for the shape (GEMM_VARIANT_AUTO:
+ * the CTA pair, or one CTA when M <= 128), or, for K <= 16, the small-K
+ * CUDA-core kernel (GEMM_VARIANT_SMALLK).
  */
 int gemm_bf16(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
               int64_t lda, int64_t ldb, int64_t ldd, cudaStream_t stream);
