@@ -331,3 +331,36 @@ def test_matmul_wrappers_take_a_workspace():
     assert g.gemm_last_schedule()["sk_tiles"] > 0
     D_ref, _ = oracle.gemm_bf16(gi.bf16_codes(A), gi.bf16_codes(B))
     assert_bitwise(D.cpu(), D_ref, "matmul_bf16")
+
+
+# ------------------------------------------------------------- watchdog
+
+@pytest.mark.parametrize("v", ["1cta", "2cta"])
+@pytest.mark.parametrize("stall", [0, 3])
+def test_streamk_stall_times_out_then_recovers(v, stall):
+    """A stage that never fills (the watchdog test hook) in a split launch:
+    the kernel gives up on its bounded waits, drains its own copies, returns
+    GEMM_ERR_TIMEOUT; after the workspace is zeroed again the next call is
+    exact."""
+    variant = BF16_VARIANTS[v]
+    M, N, K = 1024, 1024, 4096
+    A, B = int_bf16(M, N, K, seed=77, lo=-1, hi=2)
+    Ad, Bd = A.cuda(), B.cuda()
+    D = torch.zeros(M, N, dtype=torch.bfloat16, device="cuda")
+    ws = workspace(False, variant)
+    s = torch.cuda.current_stream().cuda_stream
+    call = lambda: g.gemm_bf16_streamk(variant, Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), M, N,
+                                       K, K, K, N, ws.data_ptr(), ws.numel(), s)
+    old_ms = g.gemm_set_watchdog_ms(100)
+    try:
+        assert g.gemm_debug_stall_next_launch(stall) == g.GEMM_OK
+        assert call() == g.GEMM_OK
+        assert g.gemm_last_schedule()["sk_tiles"] > 0
+        assert g.gemm_last_status(s) == g.GEMM_ERR_TIMEOUT
+    finally:
+        g.gemm_set_watchdog_ms(old_ms)
+    ws.zero_()
+    assert call() == g.GEMM_OK
+    assert g.gemm_last_status(s) == g.GEMM_OK
+    D_ref, _ = oracle.gemm_bf16(gi.bf16_codes(A), gi.bf16_codes(B))
+    assert_bitwise(D.cpu(), D_ref, f"after recovery {v}")
