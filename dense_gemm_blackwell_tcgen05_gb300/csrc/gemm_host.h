@@ -28,10 +28,12 @@ struct Problem {
   const void* bias = nullptr;
 };
 
-// Stream-K workspace per CTA: 4 epilogue warps x 32 rows x tile_n fp32, plus
-// 4 flags; the library sizes it for every SM of the device.
+// Stream-K workspace per CTA: 4 lane quarters x 32 rows x tile_n fp32, plus
+// 8 flags (one per lane quarter and epilogue group); the library sizes it for
+// every SM of the device.
+constexpr uint64_t kStreamKFlagBytes = 8ull * 4ull;
 inline uint64_t streamk_bytes_per_cta(uint32_t tile_n) {
-  return 4ull * 32ull * tile_n * 4ull + 4ull * 4ull;
+  return 4ull * 32ull * tile_n * 4ull + kStreamKFlagBytes;
 }
 
 // Stream-K schedule choice (host only).  Units are K-tiles of the kernel's

@@ -221,11 +221,12 @@ struct GemmCfg {
   // TMEM: ACC_STAGES accumulators of UMMA_N fp32 columns, then the scale
   // factors (MXFP8: 4 columns for A, 4 per 128 B rows).  512 = whole TMEM.
   static constexpr uint32_t ACC_STAGES = 2;
-  // Epilogue warpgroups (the ladder's multi-consumer level): with two, group
-  // g drains accumulator buffer g, so two tiles' epilogues run at once.  Used
-  // where the epilogue is the slow consumer -- the bf16 masked-store path,
-  // whose staging costs 2 KB per warp and no operand stage.  (In the MXFP8
-  // pair the extra staging would cost a stage: 6 -> 5, measured 3% slower.)
+  // Epilogue warpgroups (the ladder's multi-consumer level): with two, both
+  // groups drain every tile, group g taking the 32-column chunks c with
+  // c % 2 == g, so a tile's epilogue takes half as long.  Used where the
+  // epilogue is the slow consumer -- the bf16 masked-store path, whose staging
+  // costs 2 KB per warp and no operand stage.  (In the MXFP8 pair the extra
+  // staging would cost a stage: 6 -> 5, measured 3% slower.)
   static constexpr uint32_t EPI_WG = (!TMA_STORE && ACC_STAGES == 2 && !MX) ? 2 : 1;
   static constexpr uint32_t kEpiWg1Warp = MX ? 7 : 6;   // first warp of group 1
   static constexpr uint32_t kThreads = 32 * (kEpiWg1Warp + 4 * (EPI_WG - 1));
@@ -256,12 +257,15 @@ struct GemmCfg {
       ALIGN_SLACK + STAGES * STAGE_BYTES + SF_BYTES + EPI_BYTES + BAR_BYTES;
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
   // Stream-K owner: each epilogue warp streams its contributors' partial
-  // chunks (32 rows x 32 fp32 columns, 4 KB) through FIX_SLOTS slots placed in
-  // the operand stages, which are idle once the CTA's last MMA has completed.
-  static constexpr uint32_t FIX_SLOTS = 8;
+  // chunks (32 rows x 32 fp32 columns, 4 KB) through FIX_SLOTS slots of its
+  // own, placed in the operand stages, which are idle once the CTA's last MMA
+  // has completed.  32 slots in all (4 or 8 per warp: the depth measured the
+  // same).
+  static constexpr uint32_t FIX_SLOTS = 8 / EPI_WG;
   static constexpr uint32_t FIX_SLOT_BYTES = 32 * 32 * 4;
-  static_assert(4 * FIX_SLOTS * FIX_SLOT_BYTES <= STAGES * STAGE_BYTES, "partial ring fits the stages");
-  static_assert((2 * STAGES + RAW_SLOTS + 2 * T_SLOTS + 5) * 8 + 8 + 4 * FIX_SLOTS * 8 <= BAR_BYTES,
+  static constexpr uint32_t FIX_TOTAL = 4 * EPI_WG * FIX_SLOTS;
+  static_assert(FIX_TOTAL * FIX_SLOT_BYTES <= STAGES * STAGE_BYTES, "partial ring fits the stages");
+  static_assert((2 * STAGES + RAW_SLOTS + 2 * T_SLOTS + 5) * 8 + 8 + FIX_TOTAL * 8 <= BAR_BYTES,
                 "barrier area");
 };
 
@@ -563,10 +567,10 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
     }
     for (uint32_t b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);        // MMA issuer's commit after the last K-tile
-      mbar_init(acce_bar(b), 4 * CG);   // every epilogue warp of the pair
+      mbar_init(acce_bar(b), 4 * CG * C::EPI_WG);   // every epilogue warp of the pair
     }
     mbar_init(drain_bar, 1);
-    for (uint32_t i = 0; i < 4 * C::FIX_SLOTS; ++i) mbar_init(bar0 + 8 * (kFixBar0 + i), 1);
+    for (uint32_t i = 0; i < C::FIX_TOTAL; ++i) mbar_init(bar0 + 8 * (kFixBar0 + i), 1);
     *abort_flag = 0u;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
@@ -790,35 +794,39 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
   } else if ((warp >= 2 && warp < 6) ||
              (C::EPI_WG == 2 && warp >= C::kEpiWg1Warp && warp < C::kEpiWg1Warp + 4)) {
     // ==================== epilogue: four warps per group, one TMEM lane quarter each ===
-    const uint32_t eg = warp < 6 ? 0u : 1u;  // epilogue group (drains accumulator buffer eg)
+    constexpr uint32_t NG = C::EPI_WG;
+    const uint32_t eg = warp < 6 ? 0u : 1u;  // epilogue group: the chunks c with c % NG == eg
     const uint32_t q = warp & 3u;            // TMEM lanes 32q .. 32q+31
     const uint32_t ew = eg == 0 ? warp - 2u : 4u + warp - C::kEpiWg1Warp;   // staging slot owner
     constexpr uint32_t NCH = C::UMMA_N / 32;
     uint32_t j = 0, chunk_ctr = 0;
     bool ok = true;
-    // this warp's 32 x UMMA_N fp32 slice of a stream-K partial slot (chunk c
-    // of 32 columns at float offset 1024 c), and its flag
+    // the 32 x UMMA_N fp32 slice of a stream-K partial slot for this lane
+    // quarter (chunk c of 32 columns at float offset 1024 c), and this warp's
+    // flag in it (one per lane quarter and group: 8 words per CTA slot)
     const auto part_ptr = [&](uint32_t slot) {
       return args.ws_part + (static_cast<uint64_t>(slot * CG + rank) * 4 + q) * (32u * C::UMMA_N);
     };
-    const auto flag_ptr = [&](uint32_t slot) { return args.ws_flag + (slot * CG + rank) * 4 + q; };
-    // (the ring is per lane quarter: only one group ever runs a fix-up, on the
-    // CTA's last item)
-    const auto fix_slot = [&](uint32_t r) { return stage0 + (q * C::FIX_SLOTS + r) * C::FIX_SLOT_BYTES; };
-    const auto fix_bar = [&](uint32_t r) { return bar0 + 8 * (kFixBar0 + q * C::FIX_SLOTS + r); };
-    // owner-side transfer stream: transfer n = chunk (n / nc) of contributor
-    // cluster_id + 1 + (n % nc); issued FIX_SLOTS ahead by lane 0
+    const auto flag_ptr = [&](uint32_t slot) {
+      return args.ws_flag + ((slot * CG + rank) * 4 + q) * 2 + eg;
+    };
+    const uint32_t ring = (q * NG + eg) * C::FIX_SLOTS;   // this warp's fix-up slots
+    const auto fix_slot = [&](uint32_t r) { return stage0 + (ring + r) * C::FIX_SLOT_BYTES; };
+    const auto fix_bar = [&](uint32_t r) { return bar0 + 8 * (kFixBar0 + ring + r); };
+    // owner-side transfer stream: transfer n = this warp's (n / nc)-th chunk
+    // (chunk (n / nc) NG + eg) of contributor cluster_id + 1 + (n % nc);
+    // issued FIX_SLOTS ahead by lane 0
     uint32_t nc = 0, nfix = 0, fix_issued = 0, fix_done = 0;
     const auto issue_fix = [&](uint32_t n) {
       const uint32_t r = n % C::FIX_SLOTS;
       mbar_arrive_expect_tx(fix_bar(r), C::FIX_SLOT_BYTES);
-      bulk_load_1d(fix_slot(r), part_ptr(cluster_id + 1 + n % nc) + (n / nc) * 1024u, C::FIX_SLOT_BYTES,
-                   fix_bar(r));
+      bulk_load_1d(fix_slot(r), part_ptr(cluster_id + 1 + n % nc) + ((n / nc) * NG + eg) * 1024u,
+                   C::FIX_SLOT_BYTES, fix_bar(r));
     };
-    // v += every contributor's partial of chunk c (in contributor order)
+    // v += every contributor's partial of chunk c (c % NG == eg; contributor order)
     const auto add_partials = [&](uint32_t (&v)[32], uint32_t c) -> bool {
       for (uint32_t i = 0; i < nc; ++i) {
-        const uint32_t n = c * nc + i;
+        const uint32_t n = (c / NG) * nc + i;
         const uint32_t r = n % C::FIX_SLOTS;
         if (!warp_wait(fix_bar(r), (n / C::FIX_SLOTS) & 1u, wd, kSiteStreamKFlag, lane)) return false;
         const float4* src = reinterpret_cast<const float4*>(base_ptr + (fix_slot(r) - base));
@@ -843,7 +851,6 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
     for (uint32_t wi = 0; ok && work_item(args, cluster_id, num_clusters, KT, wi, w); ++wi, ++j) {
       const uint32_t b = j % C::ACC_STAGES;
       const uint32_t around = j / C::ACC_STAGES;
-      if (C::EPI_WG == 2 && b != eg) continue;   // the other group's buffer
       if (!warp_wait(accf_bar(b), around & 1u, wd, kSiteEpiAccFull, lane)) break;
       tc_fence_after_sync();
       uint32_t mb, nb;
@@ -859,7 +866,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
         // store instruction writes 512 contiguous bytes), then raise the flag
         float* const part = part_ptr(cluster_id);
 #pragma unroll 1
-        for (uint32_t c = 0; c < live; ++c) {
+        for (uint32_t c = eg; c < live; c += NG) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(t_addr + c * 32, v);
           tmem_wait_ld();
@@ -878,7 +885,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
         nc = num_contributors(args, cluster_id, num_clusters, KT, w.tile);
         for (uint32_t i = 0; ok && i < nc; ++i) ok = wait_flag(flag_ptr(cluster_id + 1 + i), args.epoch, wd, lane);
         if (ok && row0 < args.M) {
-          nfix = live * nc;
+          nfix = (live > eg ? (live - eg + NG - 1) / NG : 0u) * nc;
           const uint32_t first = min(nfix, C::FIX_SLOTS);
           if (lane == 0) {
             fence_proxy_async_global();
@@ -935,8 +942,11 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
             ++chunk_ctr;
           }
         } else {
-          // One 32-column chunk at a time, software-pipelined: the next chunk's
-          // tcgen05.ld is in flight while this one is converted and stored.
+          // One 32-column chunk at a time (this group's chunks eg, eg + NG, ...).
+          // Each tcgen05.ld is followed at once by its tcgen05.wait::ld: the
+          // load writes its destination registers asynchronously while the
+          // compiler takes them as written by the asm statement, so no other
+          // code may sit between the two.
           const auto finish_chunk = [&](uint32_t (&v)[32], uint32_t c) -> bool {
             if (w.kind == 1 && !add_partials(v, c)) return false;
             if (args.epi_mode != 0) epi_apply(v, args, row0 + lane, col_base + c * 32);
@@ -949,21 +959,12 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
                                    col_base + c * 32, v, lane);
             return true;
           };
-          uint32_t va[32], vb[32];
-          tmem_ld_32x32b_x32(t_addr, va);
-          tmem_wait_ld();
 #pragma unroll 1
-          for (uint32_t c = 0; c < live; c += 2) {
-            const bool has1 = c + 1 < live, has2 = c + 2 < live;
-            if (has1) tmem_ld_32x32b_x32(t_addr + (c + 1) * 32, vb);
-            const bool ok0 = finish_chunk(va, c);
-            if (has1) tmem_wait_ld();   // vb landed (before any exit: no load left in flight)
-            if (!ok0) { ok = false; break; }
-            if (!has1) break;
-            if (has2) tmem_ld_32x32b_x32(t_addr + (c + 2) * 32, va);
-            const bool ok1 = finish_chunk(vb, c + 1);
-            if (has2) tmem_wait_ld();
-            if (!ok1) { ok = false; break; }
+          for (uint32_t c = eg; c < live; c += NG) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(t_addr + c * 32, v);
+            tmem_wait_ld();
+            if (!finish_chunk(v, c)) { ok = false; break; }
           }
         }
       }

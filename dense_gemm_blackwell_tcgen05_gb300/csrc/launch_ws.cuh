@@ -129,9 +129,10 @@ int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) 
       a.dp_tiles = sp.dp_tiles;
       a.sk_tiles = sp.sk_tiles;
       clusters = sp.clusters;
-      // flags first (16 bytes per CTA slot), then the partial slots
+      // flags first (kStreamKFlagBytes per CTA slot), then the partial slots
       a.ws_flag = static_cast<uint32_t*>(p.workspace);
-      a.ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(p.workspace) + resident * CG * 16);
+      a.ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(p.workspace) +
+                                           resident * CG * kStreamKFlagBytes);
       uint32_t e = epoch_counter.fetch_add(1) + 1;
       if (e == 0) e = epoch_counter.fetch_add(1) + 1;
       a.epoch = e;

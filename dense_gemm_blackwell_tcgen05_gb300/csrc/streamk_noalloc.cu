@@ -23,7 +23,7 @@
 namespace {
 
 // 24 MiB: partial tiles and flags for up to 191 resident CTAs of the bf16
-// kernels (128 rows x 256 fp32 columns + 16 flag bytes per CTA); a GB300 runs
+// kernels (128 rows x 256 fp32 columns + 32 flag bytes per CTA); a GB300 runs
 // at most 152.
 constexpr uint64_t kScratchBytes = 24ull << 20;
 

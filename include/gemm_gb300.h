@@ -178,7 +178,7 @@ int gemm_mxfp8_fused(int variant, const void* A, const void* B, const void* SFA,
  * workspace) in K order before storing D, so results are deterministic.
  * Otherwise the call behaves like the data-parallel entry point.
  * workspace: 16-byte aligned device memory of at least
- * gemm_streamk_workspace_bytes() bytes: 16 bytes of flags per CTA, then the
+ * gemm_streamk_workspace_bytes() bytes: 32 bytes of flags per CTA, then the
  * partial slots.  ZERO IT ONCE before its first use (every completed call
  * leaves its flag words zero again; after a call that ended in
  * GEMM_ERR_TIMEOUT, zero it again).  Calls that share a workspace

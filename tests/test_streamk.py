@@ -52,12 +52,12 @@ def workspace(mx, variant):
 
 
 def flags_are_zero(ws, mx, variant, sched):
-    """The flag words (16 bytes per launched CTA at the start of the
+    """The flag words (32 bytes per launched CTA at the start of the
     workspace) are back at zero.  Only a split launch uses the workspace."""
     if sched["sk_tiles"] == 0:
         return True
     ctas = sched["clusters"] * sched["ctas_per_cluster"]
-    return bool(torch.all(ws[:ctas * 16] == 0).item())
+    return bool(torch.all(ws[:ctas * 32] == 0).item())
 
 
 def expected_split(sched, M, N, tile_m, tile_n, kt, unit):
