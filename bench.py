@@ -577,6 +577,8 @@ def run_ours(args, rank, world, local):
             "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
             "gpu_launches": args.steps * len(probs),   # in the timed region (value)
+            "device": {"name": torch.cuda.get_device_name(device),
+                       "sm_count": torch.cuda.get_device_properties(device).multi_processor_count},
             "clocks": clk,
         }
         print(json.dumps(line), flush=True)
