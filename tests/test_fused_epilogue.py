@@ -272,3 +272,41 @@ def test_matmul_fused_wrapper():
     P_, S = oracle.gemm_bf16(gi.bf16_codes(A), gi.bf16_codes(B))
     D_ref, _, _ = reference(P_, S, 2.0, 0.0, None, bias, "relu")
     assert_bitwise(D.cpu(), D_ref, "matmul_fused")
+
+
+# ------------------------------------------- the fused workloads, full size
+
+def _workload_sampled(name, n=3000):
+    """The bench's configuration of a fused workload (automatic variant),
+    checked on sampled outputs: oracle sums there, then the oracle epilogue."""
+    w = gi.WORKLOADS[name]
+    sp = gi.epilogue_spec(w)
+    A, B = gi.workload_operands(name)
+    C, bias = gi.epilogue_operands(w)
+    out_dtype = torch.float32 if sp["out"] == "f32" else torch.bfloat16
+    D = g.matmul_fused(A.cuda(), B.cuda(), alpha=sp["alpha"], beta=sp["beta"],
+                       C=None if C is None else C.cuda(), bias=None if bias is None else bias.cuda(),
+                       activation=sp["act"], out_dtype=out_dtype)
+    assert g.gemm_last_status(0) == g.GEMM_OK
+    rows, cols = P.sample_positions(w.M, w.N, n, seed=w.seed)
+    P_, S = oracle.gemm_bf16_entries(gi.bf16_codes(A), gi.bf16_codes(B), rows, cols)
+    Cs = None if C is None else f64(C)[rows, cols][None, :]
+    bs = None if bias is None else f64(bias)[cols]
+    D_ref = oracle.epilogue(np.asarray(P_).reshape(1, -1), sp["alpha"], sp["beta"], Cs, bs,
+                            ACT[sp["act"]])[0]
+    scale = np.abs(sp["alpha"] * np.asarray(P_))
+    if Cs is not None:
+        scale = scale + np.abs(sp["beta"] * Cs[0])
+    if bs is not None:
+        scale = scale + np.abs(bs)
+    got = f64(D.cpu())[rows, cols]
+    r = 2.0 ** -7 if out_dtype == torch.bfloat16 else 2.0 ** -20
+    L = 1.13 if sp["act"] == "gelu" else 1.0
+    bound = r * np.abs(D_ref) + L * (abs(sp["alpha"]) * 1e-3 * np.asarray(S) + 2.0 ** -18 * scale)
+    assert np.all(np.abs(got - D_ref) <= bound), name
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["fused_gelu_8192", "fused_f32_8192"])
+def test_fused_workloads_full_size(name):
+    _workload_sampled(name)

@@ -364,3 +364,28 @@ def test_streamk_stall_times_out_then_recovers(v, stall):
     assert g.gemm_last_status(s) == g.GEMM_OK
     D_ref, _ = oracle.gemm_bf16(gi.bf16_codes(A), gi.bf16_codes(B))
     assert_bitwise(D.cpu(), D_ref, f"after recovery {v}")
+
+
+# ---------------------------------------- the stream-K workloads, full size
+
+@pytest.mark.parametrize("name", ["streamk_1024x16384", "streamk_mxfp8_1024x32768"])
+def test_streamk_workloads_full_size(name):
+    """The bench's configuration (automatic split decision, automatic
+    variant) on sampled outputs; the split must have been taken."""
+    g.gemm_set_streamk_mode(g.STREAMK_AUTO)
+    w = gi.WORKLOADS[name]
+    ops = gi.workload_operands(name)
+    rows, cols = P.sample_positions(w.M, w.N, 3000, seed=w.seed)
+    if w.kind == "bf16":
+        A, B = ops
+        D = g.matmul_bf16(A.cuda(), B.cuda(), workspace=workspace(False, g.VARIANT_AUTO))
+        D_ref, S = oracle.gemm_bf16_entries(gi.bf16_codes(A), gi.bf16_codes(B), rows, cols)
+    else:
+        A, SFA, B, SFB = ops
+        D = g.matmul_mxfp8(A.cuda(), SFA.cuda(), B.cuda(), SFB.cuda(),
+                           workspace=workspace(True, g.VARIANT_AUTO))
+        D_ref, S = oracle.gemm_mxfp8_entries(A.numpy(), B.numpy(), SFA.numpy(), SFB.numpy(), rows,
+                                             cols, w.K)
+    assert g.gemm_last_schedule()["sk_tiles"] > 0
+    assert g.gemm_last_status(0) == g.GEMM_OK
+    P.check_within_bound(P.bf16_to_f64(D.cpu())[rows, cols], D_ref, S, name)
