@@ -53,7 +53,7 @@ def parse_args():
     ap.add_argument("--workload", default="headline",
                     help="headline (bf16 8192^3 + MXFP8 8192^3) or one named workload")
     ap.add_argument("--variant", type=int, default=0, help="kernel variant (0 = auto)")
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work budget of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
