@@ -57,6 +57,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work budget of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-library-context", action="store_true",
+                    help="skip the cuBLAS context figures measured after the timed region")
     return ap.parse_args()
 
 
@@ -412,6 +414,87 @@ def run_reference(args, rank, world):
     return 0
 
 
+def blocked_scales(sf, rows: int, K: int):
+    """UE8M0 scales [rows, >= K/32] rearranged into cuBLASLt's block-scaled layout (128-row x
+    4-block tiles of 512 bytes; inside a tile, row r's byte for block c sits at
+    16*(r % 32) + 4*(r // 32) + c), as torch._scaled_mm takes them.  Context leg only."""
+    import torch
+    nb = (K + 31) // 32
+    R, C = (rows + 127) // 128 * 128, (nb + 3) // 4 * 4
+    p = torch.zeros(R, C, dtype=torch.uint8, device=sf.device)
+    p[:rows, :nb] = sf[:rows, :nb]
+    t = p.view(R // 128, 128, C // 4, 4).permute(0, 2, 1, 3).reshape(-1, 4, 32, 4).transpose(1, 2)
+    return t.reshape(R, C).contiguous().view(torch.float8_e8m0fnu)
+
+
+def library_context(probs, stream, n: int, flush_buf, flush_each):
+    """cuBLAS on the same device operands, for context: torch.matmul for plain bf16 and
+    torch._scaled_mm (block-scaled E4M3) for plain MXFP8 workloads.  Measured after the
+    timed region, alternating with our own kernel (two rounds of n launches each, same
+    flush policy), so both see the same clocks.  No step of the path calls these."""
+    import torch
+
+    import dense_gemm_blackwell_tcgen05_gb300 as g
+    out = {}
+    for j, p in enumerate(probs):
+        w = p.w
+        if w.kind not in ("bf16", "mxfp8") or p.spec or p.ws is not None:
+            continue
+        try:
+            if w.kind == "bf16":
+                A, B = p.dev[:2]
+                lib_name = "torch.matmul (cuBLAS)"
+                lib = lambda A=A, B=B: torch.matmul(A, B.t())
+            else:
+                A, SFA, B, SFB = p.dev[:4]
+                sa, sb = blocked_scales(SFA, w.M, w.K), blocked_scales(SFB, w.N, w.K)
+                a8, b8 = A.view(torch.float8_e4m3fn), B.view(torch.float8_e4m3fn)
+                lib_name = "torch._scaled_mm (cuBLASLt, block-scaled E4M3)"
+                lib = lambda a8=a8, b8=b8, sa=sa, sb=sb: torch._scaled_mm(
+                    a8, b8.t(), scale_a=sa, scale_b=sb, out_dtype=torch.bfloat16)
+            with torch.cuda.stream(stream):
+                rc = p.launch(stream.cuda_stream)
+                if rc != g.GEMM_OK:
+                    raise g.GemmError(rc, w.name)
+                ref = lib()
+            torch.cuda.synchronize()
+            same = bool(torch.equal(ref.view(torch.int16), p.D.view(torch.int16)))
+
+            def timed(f):
+                s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                total = 0.0
+                with torch.cuda.stream(stream):
+                    if flush_each[j]:
+                        for _ in range(n):
+                            flush_buf.zero_()
+                            s.record(stream)
+                            f()
+                            e.record(stream)
+                            e.synchronize()
+                            total += s.elapsed_time(e)
+                    else:
+                        s.record(stream)
+                        for _ in range(n):
+                            f()
+                        e.record(stream)
+                        e.synchronize()
+                        total = s.elapsed_time(e)
+                return total / n
+
+            ours_f = lambda: p.launch(stream.cuda_stream)
+            t_ours, t_lib = [], []
+            for _ in range(2):
+                t_ours.append(timed(ours_f))
+                t_lib.append(timed(lib))
+            out[w.name] = {"library": lib_name,
+                           "library_tflops": w.flops / (min(t_lib) / 1e3) / 1e12,
+                           "ours_tflops": w.flops / (min(t_ours) / 1e3) / 1e12,
+                           "launches": 2 * n, "bitwise_equal_to_ours": same}
+        except Exception as exc:   # a torch without block-scaled _scaled_mm, for instance
+            out[w.name] = {"unavailable": repr(exc)[:200]}
+    return out
+
+
 def run_ours(args, rank, world, local):
     import torch
 
@@ -590,6 +673,14 @@ def run_ours(args, rank, world, local):
         roof["peak_source"] = f"{peak_src} ({'bf16_tflops_sustained' if peak_src == 'measured' else 'fallback sustained'}" \
                               f"{' x2 for FP8' if works[dom].kind == 'mxfp8' else ''})"
 
+    # ---- cuBLAS on the same operands, for context (after the timed region) ----
+    libctx = None
+    if rank == 0 and not args.no_library_context:
+        libctx = library_context(probs, stream, min(args.steps, 100), flush_buf, flush_each)
+        st = g.gemm_last_status(sh)
+        if st != g.GEMM_OK:
+            raise g.GemmError(st, "library context")
+
     # ---- CPU baseline: the oracle as it stands, bounded sample, rank 0 at N=1 ----
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -616,6 +707,7 @@ def run_ours(args, rank, world, local):
             "roofline": roof,
             "kernels": kernels,
             "cpu_baseline": cpu,
+            "library_context": libctx,
             "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
             "gpu_launches": args.steps * len(probs),   # in the timed region (value)

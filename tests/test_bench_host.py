@@ -1,0 +1,24 @@
+"""Host-side helpers of bench.py that need no GPU."""
+import torch
+
+import bench
+
+
+def test_blocked_scales_layout():
+    # cuBLASLt's block-scaled layout, written out element by element: a 128-row x
+    # 4-block tile is 512 bytes, tiles ordered row-block major; inside a tile, row
+    # r's byte for block c sits at 16*(r % 32) + 4*(r // 32) + c.
+    rows, K = 200, 8 * 32 * 3          # ragged rows, 24 blocks: 6 groups of 4
+    nb = K // 32
+    g = torch.Generator().manual_seed(0)
+    sf = torch.randint(0, 255, (rows, 32), dtype=torch.uint8, generator=g)
+    out = bench.blocked_scales(sf, rows, K).view(torch.uint8).flatten()
+    R, C = 256, (nb + 3) // 4 * 4
+    assert out.numel() == R * C
+    for r in range(R):
+        for b in range(C):
+            tile = (r // 128) * (C // 4) + b // 4
+            rr = r % 128
+            off = tile * 512 + 16 * (rr % 32) + 4 * (rr // 32) + b % 4
+            want = int(sf[r, b]) if r < rows and b < nb else 0
+            assert int(out[off]) == want, (r, b)
