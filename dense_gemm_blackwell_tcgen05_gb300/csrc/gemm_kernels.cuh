@@ -280,20 +280,22 @@ struct GemmCfg {
 template <uint32_t CHUNKS>
 __device__ __forceinline__ void retile_scales(const uint8_t* raw, uint8_t* t_base, uint32_t t_stride,
                                               uint32_t t_off, uint32_t rows, uint32_t lane) {
-  const uint4* rw = reinterpret_cast<const uint4*>(raw);
+  if constexpr (CHUNKS > 0) {   // (bf16 instantiations have no scales)
+    const uint4* rw = reinterpret_cast<const uint4*>(raw);
 #pragma unroll
-  for (uint32_t h = 0; h < CHUNKS; ++h) {
-    uint4 v[4];
+    for (uint32_t h = 0; h < CHUNKS; ++h) {
+      uint4 v[4];
 #pragma unroll
-    for (uint32_t q = 0; q < 4; ++q) {
-      const uint32_t r = h * 128 + 32 * q + lane;
-      v[q] = r < rows ? rw[r] : make_uint4(0, 0, 0, 0);
+      for (uint32_t q = 0; q < 4; ++q) {
+        const uint32_t r = h * 128 + 32 * q + lane;
+        v[q] = r < rows ? rw[r] : make_uint4(0, 0, 0, 0);
+      }
+      uint8_t* d0 = t_base + t_off + h * 512 + 16 * lane;
+      *reinterpret_cast<uint4*>(d0) = make_uint4(v[0].x, v[1].x, v[2].x, v[3].x);
+      *reinterpret_cast<uint4*>(d0 + t_stride) = make_uint4(v[0].y, v[1].y, v[2].y, v[3].y);
+      *reinterpret_cast<uint4*>(d0 + 2 * t_stride) = make_uint4(v[0].z, v[1].z, v[2].z, v[3].z);
+      *reinterpret_cast<uint4*>(d0 + 3 * t_stride) = make_uint4(v[0].w, v[1].w, v[2].w, v[3].w);
     }
-    uint4* d0 = reinterpret_cast<uint4*>(t_base + t_off + h * 512) + lane;
-    *d0 = make_uint4(v[0].x, v[1].x, v[2].x, v[3].x);
-    *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(d0) + t_stride) = make_uint4(v[0].y, v[1].y, v[2].y, v[3].y);
-    *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(d0) + 2 * t_stride) = make_uint4(v[0].z, v[1].z, v[2].z, v[3].z);
-    *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(d0) + 3 * t_stride) = make_uint4(v[0].w, v[1].w, v[2].w, v[3].w);
   }
 }
 
