@@ -303,7 +303,17 @@ static int bf16_impl(int variant, const void* A, const void* B, void* D, int64_t
   p.workspace_bytes = ws_bytes > 0 ? static_cast<uint64_t>(ws_bytes) : 0u;
   if (ws != nullptr && (base == GEMM_VARIANT_SYNC || !is_device_pointer(ws, ctx.device)))
     return GEMM_ERR_INVALID_ARG;
-  const bool tma_store = tma_store_ok(D, N, ldd, direct) && !(p.epi_mode & kEpiOutF32);
+  bool tma_store = tma_store_ok(D, N, ldd, direct) && !(p.epi_mode & kEpiOutF32);
+  // A launch that splits tiles along K sums the partial tiles in its epilogue
+  // warps; the masked-store kernels have two epilogue groups against the
+  // TMA-store kernels' one, which measured 11% faster on 1024x1024x16384.
+  if (tma_store && ws != nullptr &&
+      (base == GEMM_VARIANT_AUTO || base == GEMM_VARIANT_1CTA || base == GEMM_VARIANT_2CTA)) {
+    const int cg = base == GEMM_VARIANT_1CTA ? 1 : base == GEMM_VARIANT_2CTA ? 2 : (M <= 128 ? 1 : 2);
+    uint32_t sk_tiles = 0;
+    if ((rc = bf16_streamk_split_tiles(cg, p, ctx, &sk_tiles)) != GEMM_OK) return rc;
+    if (sk_tiles != 0) tma_store = false;
+  }
   // Small K is a write of D: the CUDA-core kernel unless the call needs the
   // persistent kernel's extras (an epilogue, a stream-K workspace).
   if (base == GEMM_VARIANT_AUTO && K <= smallk_max_k() && p.epi_mode == 0 && ws == nullptr)

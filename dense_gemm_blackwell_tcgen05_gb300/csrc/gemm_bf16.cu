@@ -17,6 +17,12 @@ int launch_bf16_ws(int cg, bool tma_store, const Problem& p, const LaunchCtx& ct
   return GEMM_ERR_INVALID_ARG;
 }
 
+int bf16_streamk_split_tiles(int cg, const Problem& p, const LaunchCtx& ctx, uint32_t* sk_tiles) {
+  if (cg == 1) return ws_streamk_split_tiles<1, Kind::BF16, false>(p, ctx, sk_tiles);
+  if (cg == 2) return ws_streamk_split_tiles<2, Kind::BF16, false>(p, ctx, sk_tiles);
+  return GEMM_ERR_INVALID_ARG;
+}
+
 bool plan_bf16(int cg, bool tma_store, KernelPlan* out) {
   if (cg == 1) {
     tma_store ? fill_plan<1, Kind::BF16, true>(out) : fill_plan<1, Kind::BF16, false>(out);

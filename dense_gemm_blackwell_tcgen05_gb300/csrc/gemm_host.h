@@ -122,6 +122,9 @@ bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base
 int launch_bf16_ws(int cg, bool tma_store, const Problem& p, const LaunchCtx& ctx,
                    cudaStream_t stream);
 int launch_bf16_sync(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream);
+// Tiles a bf16 launch on `p` (one CTA or a pair) would split along K with its
+// workspace under the current stream-K mode; 0 for the data-parallel schedule.
+int bf16_streamk_split_tiles(int cg, const Problem& p, const LaunchCtx& ctx, uint32_t* sk_tiles);
 int launch_mxf8_ws(int cg, bool tma_store, const Problem& p, const LaunchCtx& ctx,
                    cudaStream_t stream);
 int launch_zero_fill(const Problem& p, cudaStream_t stream);

@@ -13,13 +13,13 @@
 
 namespace gb300 {
 
+// One-time, per device: opt gemm_ws_kernel<CG, KIND, TMA_STORE> into the large
+// shared-memory carve-out and (pairs) find how many clusters can be resident at
+// once.  *resident: the clusters a launch may use.
 template <int CG, Kind KIND, bool TMA_STORE>
-int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) {
+int ws_resident(const LaunchCtx& ctx, uint64_t* resident) {
   using C = GemmCfg<CG, KIND, TMA_STORE>;
   auto kern = gemm_ws_kernel<CG, KIND, TMA_STORE>;
-
-  // Per-device, one-time: opt into the large shared-memory carve-out and
-  // (pairs) find how many clusters can be resident at once.
   static std::mutex mu;
   static int prepared[128] = {0};
   static int max_clusters[128] = {0};
@@ -59,6 +59,33 @@ int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) 
       prepared[ctx.device] = 1;
     }
   }
+  *resident = CG == 2 ? static_cast<uint64_t>(max_clusters[ctx.device])
+                      : static_cast<uint64_t>(ctx.num_sms);
+  return GEMM_OK;
+}
+
+// The number of tiles a launch of gemm_ws_kernel<CG, KIND, TMA_STORE> on `p`
+// would split along K (0: the data-parallel schedule).
+template <int CG, Kind KIND, bool TMA_STORE>
+int ws_streamk_split_tiles(const Problem& p, const LaunchCtx& ctx, uint32_t* sk_tiles) {
+  using C = GemmCfg<CG, KIND, TMA_STORE>;
+  *sk_tiles = 0;
+  if (p.workspace == nullptr) return GEMM_OK;
+  uint64_t resident = 0;
+  if (const int rc = ws_resident<CG, KIND, TMA_STORE>(ctx, &resident); rc != GEMM_OK) return rc;
+  const uint64_t tiles = static_cast<uint64_t>((p.M + C::UMMA_M - 1) / C::UMMA_M) *
+                         ((p.N + C::UMMA_N - 1) / C::UMMA_N);
+  const uint32_t kt = (p.K + C::BK - 1) / C::BK;
+  *sk_tiles = plan_streamk(tiles, resident, kt, C::MX ? C::SF_GROUP : 1u, streamk_mode()).sk_tiles;
+  return GEMM_OK;
+}
+
+template <int CG, Kind KIND, bool TMA_STORE>
+int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) {
+  using C = GemmCfg<CG, KIND, TMA_STORE>;
+  auto kern = gemm_ws_kernel<CG, KIND, TMA_STORE>;
+  uint64_t resident = 0;
+  if (const int rc = ws_resident<CG, KIND, TMA_STORE>(ctx, &resident); rc != GEMM_OK) return rc;
 
   Maps maps;
   std::memset(&maps, 0, sizeof maps);
@@ -108,8 +135,6 @@ int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) 
   a.bias = p.bias;
 
   const uint64_t tiles = static_cast<uint64_t>(a.num_m_blocks) * a.num_n_blocks;
-  const uint64_t resident = CG == 2 ? static_cast<uint64_t>(max_clusters[ctx.device])
-                                    : static_cast<uint64_t>(ctx.num_sms);
   // Schedule.  Data-parallel: whole tiles round-robin over min(tiles, resident)
   // clusters.  Stream-K (only with a caller workspace, and only where the
   // cost model in plan_streamk predicts a gain, unless forced): the tiles of

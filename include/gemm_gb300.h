@@ -78,7 +78,12 @@ typedef enum {
                                    flops per byte), coalesced row stores; AUTO
                                    picks it for plain calls with K <= 16           */
   GEMM_VARIANT_DIRECT_STORE = 0x100  /* flag: masked st.global epilogue instead of
-                                        TMA stores, even when D is aligned         */
+                                        TMA stores, even when D is aligned.  Without
+                                        it the library picks: TMA stores where D is
+                                        aligned, except that a bf16 stream-K launch
+                                        that splits tiles takes the masked kernel,
+                                        whose two epilogue warpgroups share the
+                                        partial sums                               */
 } gemm_variant_t;
 
 /*
