@@ -157,7 +157,7 @@ __host__ __device__ constexpr uint32_t align_up_u32(uint32_t x, uint32_t a) {
 //   MXFP8, 1 CTA : 128 x 256 tiles, one accumulator + scale columns
 //   MXFP8, pair  : 256 x 224 cluster tiles, two 224-column accumulators +
 //                  scale columns (2 x 224 + 12 <= 512)
-template <int CG, Kind KIND, bool TMA_STORE>
+template <int CG, Kind KIND, bool TMA_STORE, bool EPI2 = false>
 struct GemmCfg {
   static_assert(CG == 1 || CG == 2, "cta_group is 1 or 2");
   static constexpr bool MX = KIND == Kind::MXF8;
@@ -229,7 +229,9 @@ struct GemmCfg {
   // epilogue is the slow consumer -- the bf16 masked-store path, whose staging
   // costs 2 KB per warp and no operand stage.  (In the MXFP8 pair the extra
   // staging would cost a stage: 6 -> 5, measured 3% slower.)
-  static constexpr uint32_t EPI_WG = (!TMA_STORE && ACC_STAGES == 2 && !MX) ? 2 : 1;
+  // EPI2 asks for the second group in an MXFP8 kernel as well (used for
+  // launches that split tiles along K, whose epilogue also sums partial tiles).
+  static constexpr uint32_t EPI_WG = (!TMA_STORE && ACC_STAGES == 2 && (!MX || EPI2)) ? 2 : 1;
   static constexpr uint32_t kEpiWg1Warp = MX ? 7 : 6;   // first warp of group 1
   static constexpr uint32_t kThreads = 32 * (kEpiWg1Warp + 4 * (EPI_WG - 1));
   static constexpr uint32_t SF_TMEM_COL = ACC_STAGES * UMMA_N;
@@ -516,13 +518,13 @@ __device__ __forceinline__ void store_row32_f32(float* D, uint64_t ldd, uint32_t
   }
 }
 
-template <int CG, Kind KIND, bool TMA_STORE>
-__global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE>::kThreads, 1)
+template <int CG, Kind KIND, bool TMA_STORE, bool EPI2 = false>
+__global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 1)
     gemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD,
                    const __grid_constant__ CUtensorMap tmSFA,
                    const __grid_constant__ CUtensorMap tmSFB, const GemmArgs args) {
-  using C = GemmCfg<CG, KIND, TMA_STORE>;
+  using C = GemmCfg<CG, KIND, TMA_STORE, EPI2>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;

@@ -16,10 +16,10 @@ namespace gb300 {
 // One-time, per device: opt gemm_ws_kernel<CG, KIND, TMA_STORE> into the large
 // shared-memory carve-out and (pairs) find how many clusters can be resident at
 // once.  *resident: the clusters a launch may use.
-template <int CG, Kind KIND, bool TMA_STORE>
+template <int CG, Kind KIND, bool TMA_STORE, bool EPI2 = false>
 int ws_resident(const LaunchCtx& ctx, uint64_t* resident) {
-  using C = GemmCfg<CG, KIND, TMA_STORE>;
-  auto kern = gemm_ws_kernel<CG, KIND, TMA_STORE>;
+  using C = GemmCfg<CG, KIND, TMA_STORE, EPI2>;
+  auto kern = gemm_ws_kernel<CG, KIND, TMA_STORE, EPI2>;
   static std::mutex mu;
   static int prepared[128] = {0};
   static int max_clusters[128] = {0};
@@ -66,13 +66,13 @@ int ws_resident(const LaunchCtx& ctx, uint64_t* resident) {
 
 // The number of tiles a launch of gemm_ws_kernel<CG, KIND, TMA_STORE> on `p`
 // would split along K (0: the data-parallel schedule).
-template <int CG, Kind KIND, bool TMA_STORE>
+template <int CG, Kind KIND, bool TMA_STORE, bool EPI2 = false>
 int ws_streamk_split_tiles(const Problem& p, const LaunchCtx& ctx, uint32_t* sk_tiles) {
-  using C = GemmCfg<CG, KIND, TMA_STORE>;
+  using C = GemmCfg<CG, KIND, TMA_STORE, EPI2>;
   *sk_tiles = 0;
   if (p.workspace == nullptr) return GEMM_OK;
   uint64_t resident = 0;
-  if (const int rc = ws_resident<CG, KIND, TMA_STORE>(ctx, &resident); rc != GEMM_OK) return rc;
+  if (const int rc = ws_resident<CG, KIND, TMA_STORE, EPI2>(ctx, &resident); rc != GEMM_OK) return rc;
   const uint64_t tiles = static_cast<uint64_t>((p.M + C::UMMA_M - 1) / C::UMMA_M) *
                          ((p.N + C::UMMA_N - 1) / C::UMMA_N);
   const uint32_t kt = (p.K + C::BK - 1) / C::BK;
@@ -80,12 +80,12 @@ int ws_streamk_split_tiles(const Problem& p, const LaunchCtx& ctx, uint32_t* sk_
   return GEMM_OK;
 }
 
-template <int CG, Kind KIND, bool TMA_STORE>
+template <int CG, Kind KIND, bool TMA_STORE, bool EPI2 = false>
 int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) {
-  using C = GemmCfg<CG, KIND, TMA_STORE>;
-  auto kern = gemm_ws_kernel<CG, KIND, TMA_STORE>;
+  using C = GemmCfg<CG, KIND, TMA_STORE, EPI2>;
+  auto kern = gemm_ws_kernel<CG, KIND, TMA_STORE, EPI2>;
   uint64_t resident = 0;
-  if (const int rc = ws_resident<CG, KIND, TMA_STORE>(ctx, &resident); rc != GEMM_OK) return rc;
+  if (const int rc = ws_resident<CG, KIND, TMA_STORE, EPI2>(ctx, &resident); rc != GEMM_OK) return rc;
 
   Maps maps;
   std::memset(&maps, 0, sizeof maps);
@@ -189,9 +189,9 @@ int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) 
   return GEMM_OK;
 }
 
-template <int CG, Kind KIND, bool TMA_STORE>
+template <int CG, Kind KIND, bool TMA_STORE, bool EPI2 = false>
 void fill_plan(KernelPlan* out) {
-  using C = GemmCfg<CG, KIND, TMA_STORE>;
+  using C = GemmCfg<CG, KIND, TMA_STORE, EPI2>;
   out->stages = C::STAGES;
   out->smem_bytes = C::SMEM_BYTES;
   out->tmem_cols = C::TMEM_COLS;
