@@ -34,6 +34,7 @@ DeviceState g_devices[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::atomic<int64_t> g_watchdog_ms{-1};
 std::atomic<int> g_streamk_mode{kStreamKAuto};
+std::atomic<uint32_t> g_streamk_epoch{0};
 thread_local int t_last_cuda_error = 0;
 thread_local int64_t t_stall_next = -1;   // one-shot watchdog test hook
 thread_local int64_t t_schedule[5] = {0, 0, 0, 0, 0};
@@ -192,6 +193,12 @@ int parse_epilogue(const gemm_epilogue_t* e, int64_t N, const void* D, int64_t l
 void note_cuda_error(cudaError_t e) { t_last_cuda_error = static_cast<int>(e); }
 
 int streamk_mode() { return g_streamk_mode.load(); }
+
+uint32_t next_streamk_epoch() {
+  uint32_t e = g_streamk_epoch.fetch_add(1) + 1;
+  if (e == 0) e = g_streamk_epoch.fetch_add(1) + 1;   // 0 means "no partial yet"
+  return e;
+}
 
 void note_schedule(uint32_t clusters, uint32_t cg, uint32_t dp_tiles, uint32_t sk_tiles,
                    uint32_t sk_unit) {
@@ -372,11 +379,11 @@ static int mxfp8_impl(int variant, const void* A, const void* B, const void* SFA
   if (rc != GEMM_OK || M == 0 || N == 0) return rc;
   if (K > 0) {
     const int64_t nblk = (K + 31) / 32;
+    // Any pitch >= ceil(K/32) and any alignment: the launcher picks TMA or a
+    // plain-load gather for the scale bytes.
     if (SFA == nullptr || SFB == nullptr || ldsfa < nblk || ldsfb < nblk ||
         ldsfa > (int64_t(1) << 36) || ldsfb > (int64_t(1) << 36))
       return GEMM_ERR_INVALID_ARG;
-    if (!aligned16(SFA) || !aligned16(SFB) || ldsfa % 16 != 0 || ldsfb % 16 != 0)
-      return GEMM_ERR_ALIGNMENT;
   }
   LaunchCtx ctx;
   if ((rc = current_device(&ctx)) != GEMM_OK) return rc;

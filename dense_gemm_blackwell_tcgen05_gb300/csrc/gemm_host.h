@@ -51,6 +51,13 @@ struct StreamKPlan {
 enum StreamKMode { kStreamKAuto = 0, kStreamKAlways = 1, kStreamKNever = 2 };
 int streamk_mode();
 
+// The flag value of the next split launch: one process-wide sequence shared by
+// every kernel configuration, never 0.  A flag word left behind by a launch
+// that gave up (watchdog timeout) holds an earlier launch's value, which no
+// later launch waits for, so a workspace needs zeroing only once, before its
+// first use.
+uint32_t next_streamk_epoch();
+
 inline StreamKPlan plan_streamk(uint64_t tiles, uint64_t resident, uint32_t kt, uint32_t unit,
                                 int mode) {
   constexpr double kFixed = 30.0, kPerContributor = 8.0, kMinGain = 0.05;

@@ -2,10 +2,11 @@
 // TMEM, bf16 output.
 //
 //  * gemm_ws_kernel   -- persistent, warp-specialised kernel (TMA producer
-//                        warp, single-thread MMA issuer, four epilogue warps),
-//                        one CTA (cta_group::1, 128x256 tiles) or a CTA pair
-//                        (cta_group::2, 256x256 cluster tiles); bf16 operands
-//                        or block-scaled MXFP8 operands.
+//                        warp, single-thread MMA issuer, one or two groups of
+//                        four epilogue warps, a scale-factor warp for MXFP8),
+//                        one CTA (cta_group::1) or a CTA pair (cta_group::2);
+//                        bf16 operands (128x256 / 256x256 tiles) or
+//                        block-scaled MXFP8 operands (128x224 / 256x224).
 //  * gemm_sync_kernel -- (gemm_sync.cuh) one 128x128 tile per CTA with synchronous thread
 //                        copies into shared memory and one MMA batch per
 //                        K-tile: the first rungs of the optimisation ladder,
@@ -54,6 +55,12 @@ struct GemmArgs {
   const void* C;
   uint64_t ldc;
   const void* bias;
+  // MXFP8 scale bytes read with plain loads (sf_gather != 0: a pitch or base
+  // that TMA cannot take) instead of through the tmSFA / tmSFB tensor maps
+  uint32_t sf_gather;
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  uint64_t ldsfa, ldsfb;
 };
 
 // One piece of work for a cluster: K-tiles [k_begin, k_end) of a tile.
@@ -154,7 +161,8 @@ __host__ __device__ constexpr uint32_t align_up_u32(uint32_t x, uint32_t a) {
 //
 //   bf16,  1 CTA : 128 x 256 tiles, two 256-column accumulators
 //   bf16,  pair  : 256 x 256 cluster tiles, two 256-column accumulators
-//   MXFP8, 1 CTA : 128 x 256 tiles, one accumulator + scale columns
+//   MXFP8, 1 CTA : 128 x 224 tiles, two 224-column accumulators + scale
+//                  columns (2 x 224 + 12 <= 512)
 //   MXFP8, pair  : 256 x 224 cluster tiles, two 224-column accumulators +
 //                  scale columns (2 x 224 + 12 <= 512)
 template <int CG, Kind KIND, bool TMA_STORE, bool EPI2 = false>
@@ -297,6 +305,45 @@ __device__ __forceinline__ void retile_scales(const uint8_t* raw, uint8_t* t_bas
       *reinterpret_cast<uint4*>(d0 + t_stride) = make_uint4(v[0].y, v[1].y, v[2].y, v[3].y);
       *reinterpret_cast<uint4*>(d0 + 2 * t_stride) = make_uint4(v[0].z, v[1].z, v[2].z, v[3].z);
       *reinterpret_cast<uint4*>(d0 + 3 * t_stride) = make_uint4(v[0].w, v[1].w, v[2].w, v[3].w);
+    }
+  }
+}
+
+// Plain-load gather of one scale-factor group for scale pitches and bases
+// that TMA cannot take: rows row0 .. row0 + ROWS - 1 of an R-row byte matrix
+// with pitch ld, bytes kb0 .. kb0 + 15 of each row (one UE8M0 byte per 32 k,
+// 4 K-tiles), written to `dst` in the layout the TMA box would give (16 bytes
+// per row).  Rows >= R and bytes >= nblk are written as zero and never read.
+// Lane l takes rows l, l + 32, ...; four rows' 64 byte loads are in flight at
+// once (the scale bytes are small and L2-resident).
+template <uint32_t ROWS>
+__device__ __forceinline__ void gather_scale_rows(uint8_t* dst, const uint8_t* src, uint64_t ld,
+                                                  uint32_t row0, uint32_t R, uint32_t kb0,
+                                                  uint32_t nblk, uint32_t lane) {
+  constexpr uint32_t PER_LANE = (ROWS + 31) / 32;
+  const uint32_t nb = kb0 < nblk ? min(16u, nblk - kb0) : 0u;
+#pragma unroll
+  for (uint32_t i0 = 0; i0 < PER_LANE; i0 += 4) {
+    uint32_t w[4][4];
+#pragma unroll
+    for (uint32_t j = 0; j < 4; ++j) {
+      const uint32_t r = (i0 + j) * 32 + lane;
+      const bool live = i0 + j < PER_LANE && r < ROWS && row0 + r < R;
+      const uint8_t* p = src + static_cast<uint64_t>(row0 + r) * ld + kb0;
+#pragma unroll
+      for (uint32_t q = 0; q < 4; ++q) {
+        uint32_t x = 0;
+#pragma unroll
+        for (uint32_t b = 0; b < 4; ++b)
+          if (live && 4 * q + b < nb) x |= static_cast<uint32_t>(__ldg(p + 4 * q + b)) << (8 * b);
+        w[j][q] = x;
+      }
+    }
+#pragma unroll
+    for (uint32_t j = 0; j < 4; ++j) {
+      const uint32_t r = (i0 + j) * 32 + lane;
+      if (i0 + j < PER_LANE && r < ROWS)
+        *reinterpret_cast<uint4*>(dst + 16 * r) = make_uint4(w[j][0], w[j][1], w[j][2], w[j][3]);
     }
   }
 }
@@ -582,7 +629,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     if constexpr (TMA_STORE) tma_prefetch_desc(&tmD);
-    if constexpr (C::MX) {
+    if (C::MX && !args.sf_gather) {
       tma_prefetch_desc(&tmSFA);
       tma_prefetch_desc(&tmSFB);
     }
@@ -747,25 +794,43 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
       g.valid = work_item(args, cluster_id, num_clusters, KT, g.wi, g.w);
     };
     const uint64_t pol = l2_policy_evict_last();
-    // TMA loads of one group into raw slot gi % RAW_SLOTS (lane 0 only)
+    const uint32_t nblk = (args.K + 31u) / 32u;
+    // Loads of one group into raw slot gi % RAW_SLOTS (called by the whole
+    // warp): two TMA boxes issued by lane 0, or, for scale pitches TMA cannot
+    // take, a plain-load gather by every lane into the same layout followed by
+    // lane 0's arrival (the slot is then full when the barrier's phase ends,
+    // as after the TMA bytes).
     const auto load_group = [&](const GroupCursor& g, uint32_t gi) {
       uint32_t mb, nb;
       tile_coords(g.w.tile, args.num_m_blocks, args.num_n_blocks, args.group_m, mb, nb);
       const uint32_t r = gi % C::RAW_SLOTS;
       const uint32_t slot = raw0 + r * C::RAW_SLOT_BYTES;
-      const int32_t sx = static_cast<int32_t>((g.w.k_begin / C::SF_GROUP + g.q) * 16);
-      mbar_arrive_expect_tx(raw_full_bar(r), C::SF_TX);
-      tma_load_2d(slot + C::OFF_SFA_RAW, &tmSFA, raw_full_bar(r), sx,
-                  static_cast<int32_t>(mb * C::UMMA_M + rank * C::BLOCK_M), pol);
-      tma_load_2d(slot + C::OFF_SFB_RAW, &tmSFB, raw_full_bar(r), sx,
-                  static_cast<int32_t>(nb * C::UMMA_N), pol);
+      const uint32_t kb0 = (g.w.k_begin / C::SF_GROUP + g.q) * 16;
+      const uint32_t a_row = mb * C::UMMA_M + rank * C::BLOCK_M;
+      const uint32_t b_row = nb * C::UMMA_N;
+      if (!args.sf_gather) {
+        if (lane == 0) {
+          mbar_arrive_expect_tx(raw_full_bar(r), C::SF_TX);
+          tma_load_2d(slot + C::OFF_SFA_RAW, &tmSFA, raw_full_bar(r), static_cast<int32_t>(kb0),
+                      static_cast<int32_t>(a_row), pol);
+          tma_load_2d(slot + C::OFF_SFB_RAW, &tmSFB, raw_full_bar(r), static_cast<int32_t>(kb0),
+                      static_cast<int32_t>(b_row), pol);
+        }
+      } else {
+        uint8_t* const sp = base_ptr + (slot - base);
+        gather_scale_rows<C::BLOCK_M>(sp + C::OFF_SFA_RAW, args.sfa, args.ldsfa, a_row, args.M,
+                                      kb0, nblk, lane);
+        gather_scale_rows<C::SFB_ROWS>(sp + C::OFF_SFB_RAW, args.sfb, args.ldsfb, b_row, args.N,
+                                       kb0, nblk, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(raw_full_bar(r));
+      }
     };
     GroupCursor lc, pc;   // load cursor (RAW_SLOTS ahead) and processing cursor
     cur_first(lc);
     cur_first(pc);
     uint32_t issued = 0;
-    for (; issued < C::RAW_SLOTS && lc.valid; ++issued, cur_next(lc))
-      if (lane == 0) load_group(lc, issued);
+    for (; issued < C::RAW_SLOTS && lc.valid; ++issued, cur_next(lc)) load_group(lc, issued);
     __syncwarp();
     uint32_t gi = 0;
     for (; pc.valid; ++gi, cur_next(pc)) {
@@ -790,14 +855,15 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
           mbar_arrive_cluster(mapa_shared(t_ready_bar(gt), 0));
       }
       if (lc.valid) {   // refill this raw slot with the next group to load
-        if (lane == 0) load_group(lc, issued);
+        load_group(lc, issued);
         ++issued;
         cur_next(lc);
       }
       __syncwarp();
     }
-    // Exit path after a give-up: let this warp's scale loads still in flight land.
-    if (lane == 0 && *abort_flag)
+    // Exit path after a give-up: let this warp's scale loads still in flight
+    // land (a gathered slot's phase has already completed).
+    if (lane == 0 && *abort_flag && !args.sf_gather)
       for (uint32_t i = gi; i < issued; ++i)
         drain_wait(raw_full_bar(i % C::RAW_SLOTS), (i / C::RAW_SLOTS) & 1u, wd, kSiteProducerDrain);
   } else if ((warp >= 2 && warp < 6) ||

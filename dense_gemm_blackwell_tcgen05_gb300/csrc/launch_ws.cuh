@@ -101,7 +101,13 @@ int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) 
                        CU_TENSOR_MAP_SWIZZLE_128B))
       return GEMM_ERR_LAUNCH;
   }
-  if constexpr (C::MX) {
+  // Scale bytes travel by TMA when both matrices are 16-byte aligned with
+  // pitches that are multiples of 16 bytes (TMA's rules); otherwise the
+  // scale-factor warp gathers them with plain loads.
+  const bool sf_gather =
+      C::MX && (((reinterpret_cast<uintptr_t>(p.SFA) | reinterpret_cast<uintptr_t>(p.SFB)) & 15u) != 0 ||
+                p.ldsfa % 16 != 0 || p.ldsfb % 16 != 0);
+  if (C::MX && !sf_gather) {
     const uint64_t nblk = (p.K + 31) / 32;
     if (!encode_map_2d(&maps.SFA, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.SFA, nblk, p.M, p.ldsfa, 16,
                        C::BLOCK_M, CU_TENSOR_MAP_SWIZZLE_NONE) ||
@@ -110,7 +116,6 @@ int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) 
       return GEMM_ERR_LAUNCH;
   }
 
-  static std::atomic<uint32_t> epoch_counter{0};
   GemmArgs a;
   a.M = p.M;
   a.N = p.N;
@@ -133,6 +138,11 @@ int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) 
   a.C = p.C;
   a.ldc = p.ldc;
   a.bias = p.bias;
+  a.sf_gather = sf_gather ? 1u : 0u;
+  a.sfa = static_cast<const uint8_t*>(p.SFA);
+  a.sfb = static_cast<const uint8_t*>(p.SFB);
+  a.ldsfa = p.ldsfa;
+  a.ldsfb = p.ldsfb;
 
   const uint64_t tiles = static_cast<uint64_t>(a.num_m_blocks) * a.num_n_blocks;
   // Schedule.  Data-parallel: whole tiles round-robin over min(tiles, resident)
@@ -158,9 +168,7 @@ int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) 
       a.ws_flag = static_cast<uint32_t*>(p.workspace);
       a.ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(p.workspace) +
                                            resident * CG * kStreamKFlagBytes);
-      uint32_t e = epoch_counter.fetch_add(1) + 1;
-      if (e == 0) e = epoch_counter.fetch_add(1) + 1;
-      a.epoch = e;
+      a.epoch = next_streamk_epoch();
     }
   }
   cudaLaunchConfig_t cfg = {};

@@ -10,8 +10,13 @@
 //
 // Nothing here allocates: the scratch is a file-scope __device__ array that
 // the CUDA loader places with the module.  Its device address is fetched once
-// per device (cudaGetSymbolAddress) and its flag words are cleared once; both
-// happen on the first call for a device, with that device current.
+// per device (cudaGetSymbolAddress, with that device current) on the first
+// call for the device, and that call also clears the buffer with a
+// cudaMemsetAsync on the caller's stream, ordered before its own kernel.
+// Later calls need no clearing: a completed split launch leaves its flag words
+// at zero, and one that gave up on a watchdog timeout leaves flag values of
+// its own launch, which no later launch waits for (the flag value is a
+// process-wide launch sequence number).
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -34,10 +39,12 @@ std::mutex g_mu;
 void* g_ptr[kMaxDevices] = {};
 
 // Device address of the scratch for the current device, set up on first use:
-// the symbol lookup and a synchronous clear of the whole buffer (the stream-K
+// the symbol lookup and a clear of the whole buffer on `stream` (the stream-K
 // flags must start at zero; the partial slots need no initial value but
-// clearing all of it is as cheap).  Returns a gemm_status_t.
-int scratch_for_current_device(void** out) {
+// clearing all of it is as cheap).  The clear is queued on the caller's
+// stream, so the kernel that follows on that stream runs after it whatever the
+// stream's flags.  Returns a gemm_status_t.
+int scratch_for_current_device(cudaStream_t stream, void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     cudaGetLastError();
@@ -47,7 +54,7 @@ int scratch_for_current_device(void** out) {
   if (g_ptr[dev] == nullptr) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_streamk_scratch);
-    if (e == cudaSuccess) e = cudaMemset(p, 0, kScratchBytes);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p, 0, kScratchBytes, stream);
     if (e != cudaSuccess) {
       gb300::note_cuda_error(e);
       cudaGetLastError();
@@ -72,7 +79,7 @@ extern "C" int gemm_bf16_streamk_noalloc(int variant, const void* A, const void*
   if (need < 0) return static_cast<int>(need);
   if (static_cast<uint64_t>(need) > kScratchBytes) return GEMM_ERR_INVALID_ARG;
   void* scratch = nullptr;
-  if (const int rc = scratch_for_current_device(&scratch); rc != GEMM_OK) return rc;
+  if (const int rc = scratch_for_current_device(stream, &scratch); rc != GEMM_OK) return rc;
   return gemm_bf16_streamk(variant, A, B, D, M, N, K, lda, ldb, ldd, scratch,
                            static_cast<int64_t>(kScratchBytes), stream);
 }

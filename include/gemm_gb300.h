@@ -28,10 +28,11 @@
  *   GEMM_ERR_INVALID_ARG  M, N or K negative or >= 2^31, a NULL pointer,
  *                         lda < K, ldb < K, ldd < N, a pointer that is not
  *                         device memory, an unknown variant
- *   GEMM_ERR_ALIGNMENT    A or B (or SFA/SFB) not 16-byte aligned, or a row
- *                         pitch whose byte size is not a multiple of 16
- *                         (the TMA engine's rule): bf16 needs lda, ldb
- *                         multiples of 8, E4M3 multiples of 16
+ *   GEMM_ERR_ALIGNMENT    A or B not 16-byte aligned, or an A/B row pitch
+ *                         whose byte size is not a multiple of 16 (the TMA
+ *                         engine's rule): bf16 needs lda, ldb multiples of
+ *                         8, E4M3 multiples of 16 (MXFP8 scale matrices
+ *                         take any pitch and alignment)
  *   GEMM_ERR_UNSUPPORTED_DEVICE  the current device is not compute
  *                         capability 10.3 (sm_103); there is no fallback
  *   GEMM_ERR_LAUNCH       the CUDA launch (or tensor-map encoding) failed
@@ -66,7 +67,8 @@ typedef enum {
 typedef enum {
   GEMM_VARIANT_AUTO = 0,        /* the fastest path for the arguments              */
   GEMM_VARIANT_1CTA = 1,        /* persistent warp-specialised, cta_group::1,
-                                   128x256 tiles (ladder levels 4-7)               */
+                                   128x256 tiles (bf16) or 128x224 tiles (MXFP8)
+                                   (ladder levels 4-7)                             */
   GEMM_VARIANT_2CTA = 2,        /* persistent warp-specialised CTA pair,
                                    cta_group::2, 256x256 tiles (bf16) or 256x224
                                    tiles (MXFP8, masked-store epilogue)
@@ -106,9 +108,13 @@ int gemm_bf16_variant(int variant, const void* A, const void* B, void* D, int64_
  *   b(j,k) = 2^(SFB[j*ldsfb + k/32] - 127) * e4m3(B[j*ldb + k])
  * A [M, K], B [N, K]: E4M3 ("e4m3fn") bytes, lda/ldb multiples of 16.
  * SFA [M, ldsfa], SFB [N, ldsfb]: UE8M0 scale bytes (2^(e-127), 255 = NaN), one
- * per 32 consecutive k (the last block may be partial); ldsfa, ldsfb are
- * row pitches in bytes, >= ceil(K/32) and multiples of 16; SFA/SFB 16-byte
- * aligned.  D bf16 as above.
+ * per 32 consecutive k (the last block may be partial), row-major; ldsfa,
+ * ldsfb are row pitches in bytes, any value >= ceil(K/32) (the dense layout
+ * ld = ceil(K/32) included), with any alignment of SFA/SFB.  When both are
+ * 16-byte aligned with pitches that are multiples of 16, the scale bytes
+ * travel by TMA; otherwise the kernel's scale-factor warp gathers them with
+ * plain loads (same results; slower for large K).  Bytes at k-blocks
+ * >= ceil(K/32) are never read.  D bf16 as above.
  */
 int gemm_mxfp8(const void* A, const void* B, const void* SFA, const void* SFB, void* D,
                int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldsfa,
@@ -184,10 +190,11 @@ int gemm_mxfp8_fused(int variant, const void* A, const void* B, const void* SFA,
  * Otherwise the call behaves like the data-parallel entry point.
  * workspace: 16-byte aligned device memory of at least
  * gemm_streamk_workspace_bytes() bytes: 32 bytes of flags per CTA, then the
- * partial slots.  ZERO IT ONCE before its first use (every completed call
- * leaves its flag words zero again; after a call that ended in
- * GEMM_ERR_TIMEOUT, zero it again).  Calls that share a workspace
- * must not overlap on the GPU.  Errors as the data-parallel entry points,
+ * partial slots.  ZERO IT ONCE before its first use.  Later calls need no
+ * clearing: a completed call leaves its flag words zero again, and a call
+ * that ended in GEMM_ERR_TIMEOUT leaves flag values that identify its own
+ * launch (a process-wide launch sequence number), which no later launch
+ * waits for.  Calls that share a workspace must not overlap on the GPU.  Errors as the data-parallel entry points,
  * plus GEMM_ERR_INVALID_ARG for a NULL, short or misaligned workspace.
  */
 int gemm_bf16_streamk(int variant, const void* A, const void* B, void* D, int64_t M, int64_t N,
@@ -211,11 +218,16 @@ int gemm_mxfp8_streamk(int variant, const void* A, const void* B, const void* SF
  * minus the workspace, plus GEMM_ERR_INVALID_ARG when the device would need
  * more scratch than the buffer holds.
  * First call per device: with that device current, it looks up the buffer's
- * address and clears it synchronously (cudaMemset), so make the first call
- * for each device before any stream capture begins.
+ * address (cudaGetSymbolAddress) and clears the buffer with a
+ * cudaMemsetAsync queued on `stream` ahead of its own kernel, so make the
+ * first call for each device before any stream capture begins.  Later calls
+ * do not clear it (nothing needs clearing, also after a GEMM_ERR_TIMEOUT).
  * Every call on a device shares the one buffer: calls that overlap on the GPU
  * (other streams, other host threads) race and give wrong results; order
- * them on one stream or synchronise between them.
+ * them on one stream or synchronise between them.  The buffer's address is
+ * kept for the life of the process: calling cudaDeviceReset() and then this
+ * entry point is not supported (nor, for the same reason, any other entry
+ * point of the library, which keeps its status word's address the same way).
  */
 int gemm_bf16_streamk_noalloc(int variant, const void* A, const void* B, void* D, int64_t M,
                               int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldd,

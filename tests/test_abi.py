@@ -82,10 +82,16 @@ def test_mxfp8_validation():
     f = lambda **k: g.gemm_mxfp8(k.get("A", FAKE), FAKE, k.get("SFA", FAKE), FAKE, FAKE, 4, 4,
                                  k.get("K", 64), k.get("lda", 64), 64, k.get("ldsfa", 16), 16, 4, 0)
     assert f(lda=40, K=40) == g.GEMM_ERR_ALIGNMENT          # E4M3 pitch must be 16-byte multiple
-    assert f(ldsfa=8) == g.GEMM_ERR_ALIGNMENT               # scale pitch multiple of 16
     assert f(K=1024, lda=1024, ldsfa=16) == g.GEMM_ERR_INVALID_ARG   # ldsfa < ceil(K/32)
     assert f(SFA=NULL) == g.GEMM_ERR_INVALID_ARG
-    assert f(SFA=FAKE + 4) == g.GEMM_ERR_ALIGNMENT
+    # scale matrices take any pitch >= ceil(K/32) and any alignment (plain-load
+    # gather where TMA cannot read them): past validation, these reach the
+    # device checks (no device here; the fake pointers on a GPU machine)
+    past = (g.GEMM_ERR_UNSUPPORTED_DEVICE, g.GEMM_ERR_INVALID_ARG)
+    assert f(ldsfa=2) in past
+    assert f(ldsfa=8) in past
+    assert f(SFA=FAKE + 4) in past
+    assert f(SFA=FAKE + 1, ldsfa=3) in past
 
 
 def test_no_device_is_reported_not_crashed():

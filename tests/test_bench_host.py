@@ -22,3 +22,14 @@ def test_blocked_scales_layout():
             off = tile * 512 + 16 * (rr % 32) + 4 * (rr // 32) + b % 4
             want = int(sf[r, b]) if r < rows and b < nb else 0
             assert int(out[off]) == want, (r, b)
+
+
+def test_tensor_peak_choice():
+    # the sustained (power-capped, seconds-long) peak only for a region that
+    # is itself seconds long and saw the power cap; a short burst otherwise
+    capped = {"reasons": ["sw_power_cap"]}
+    assert bench.tensor_peak_choice(0.019, {"reasons": []})[0] == "burst"
+    assert bench.tensor_peak_choice(0.019, capped)[0] == "burst"
+    assert bench.tensor_peak_choice(5.0, {"reasons": []})[0] == "burst"
+    assert bench.tensor_peak_choice(5.0, None)[0] == "burst"
+    assert bench.tensor_peak_choice(1.2, capped)[0] == "sustained"

@@ -122,7 +122,9 @@ def test_workload_mxfp8_8192():
     w = gi.WORKLOADS["mxfp8_8192"]
     A, SFA, B, SFB = gi.workload_operands("mxfp8_8192")
     D = run(A, SFA, B, SFB, g.VARIANT_AUTO)
-    rows, cols = P.sample_positions(w.M, w.N, 3000, seed=w.seed)
+    # every 224-column tile edge of the MXFP8 kernels and every 128-row edge
+    rows, cols = P.sample_positions(w.M, w.N, 3000, seed=w.seed, tile_m=128, tile_n=224)
+    assert {223, 224, 8063, 8064} <= set(cols.tolist())
     D_ref, S = oracle.gemm_mxfp8_entries(A.numpy(), B.numpy(), SFA.numpy(), SFB.numpy(), rows, cols)
     P.check_within_bound(P.bf16_to_f64(D)[rows, cols], D_ref, S, "mxfp8_8192")
 
@@ -145,3 +147,156 @@ def test_k_tail_reads_nothing_past_k(v, K, lda):
     D = run(A, SFA, B, SFB, VARIANTS[v], K=K)
     D_ref, _ = ref(A, SFA, B, SFB, K)
     assert np.array_equal(gi.bf16_codes(D), oracle.f64_to_bf16_rne(D_ref))
+
+
+# ----------------------------------------------------- non-finite and extreme scales
+
+def assert_matches_oracle(D, D_ref, what):
+    """NaN exactly where the oracle has NaN, +-Inf where it has +-Inf, and the
+    bf16 RNE of the oracle's value everywhere else, bit for bit (a zero of
+    either sign where the oracle's value rounds to zero)."""
+    d = P.bf16_to_f64(D)
+    nan_ref = np.isnan(D_ref)
+    assert np.array_equal(np.isnan(d), nan_ref), f"{what}: NaN pattern differs"
+    inf_ref = np.isinf(D_ref)
+    assert np.array_equal(d[inf_ref], D_ref[inf_ref]), f"{what}: Inf differs"
+    fin = np.isfinite(D_ref)
+    want = oracle.bf16_to_f64(oracle.f64_to_bf16_rne(D_ref[fin]))
+    if not np.array_equal(d[fin], want):        # -0 == +0 here
+        bad = np.flatnonzero(d[fin] != want)
+        raise AssertionError(f"{what}: {bad.size} finite mismatches; first got {d[fin][bad[0]]} "
+                             f"want {want[bad[0]]}")
+
+
+MX_VARIANTS = ["1cta", "2cta", "auto"]
+
+
+@pytest.mark.parametrize("v", MX_VARIANTS)
+def test_nan_code_inside_k(v):
+    """E4M3 NaN codes (0x7F, 0xFF) inside K: row r of D (from A) and column j
+    (from B) are NaN, every other element is exact."""
+    M, N, K = 260, 470, 256
+    A, SFA, B, SFB = int_operands(M, N, K, seed=31)
+    A[5, 100] = 0x7F
+    A[200, 0] = 0xFF
+    B[300, 255] = 0x7F
+    D = run(A, SFA, B, SFB, VARIANTS[v])
+    D_ref, _ = ref(A, SFA, B, SFB)
+    assert np.isnan(D_ref[5]).all() and np.isnan(D_ref[:, 300]).all()
+    assert_matches_oracle(D, D_ref, f"nan code/{v}")
+
+
+@pytest.mark.parametrize("v", MX_VARIANTS)
+def test_nan_scale_on_live_block(v):
+    """A UE8M0 NaN scale (0xFF) on a block whose elements are live (inside K,
+    nonzero): every product of that block is NaN, so row r of D (scale of A)
+    and column j (scale of B) are NaN, the rest exact."""
+    M, N, K = 300, 450, 192
+    A, SFA, B, SFB = int_operands(M, N, K, seed=32)
+    A[7, 64:96] = P.e4m3_from_ints(np.full(32, 3))         # live, nonzero block 2 of row 7
+    B[250, 160:192] = P.e4m3_from_ints(np.full(32, -2))    # live block 5 (the last) of row 250
+    SFA[7, 2] = 0xFF
+    SFB[250, 5] = 0xFF
+    D = run(A, SFA, B, SFB, VARIANTS[v])
+    D_ref, _ = ref(A, SFA, B, SFB)
+    assert np.isnan(D_ref[7]).all() and np.isnan(D_ref[:, 250]).all()
+    assert_matches_oracle(D, D_ref, f"nan scale/{v}")
+
+
+def e4m3_subnormal_codes(rng, shape):
+    """Random E4M3 subnormal codes: sign, exponent field 0, mantissa 1..7
+    (values +-m 2^-9)."""
+    m = rng.integers(1, 8, size=shape)
+    sign = rng.integers(0, 2, size=shape) << 7
+    return torch.from_numpy((sign | m).astype(np.uint8))
+
+
+@pytest.mark.parametrize("v", MX_VARIANTS)
+def test_zero_scale_byte_is_two_to_minus_127(v):
+    """Scale byte 0 means 2^-127, not zero: A holds subnormal E4M3 codes
+    (+-m 2^-9) scaled by 2^-127 and B small integers scaled by 2^127 (byte
+    254), so every product is +-m v 2^-9 exactly and the sums are exact in
+    fp32; then the same with normal codes in A."""
+    M, N, K = 200, 300, 256
+    rng = np.random.default_rng(33)
+    _, _, B, SFB = int_operands(M, N, K, seed=34)
+    nblk = K // 32
+    SFB[:, :nblk] = 254
+    SFA = torch.zeros(M, gi.sf_pitch(K), dtype=torch.uint8)      # byte 0 everywhere
+    A = e4m3_subnormal_codes(rng, (M, K))
+    D = run(A, SFA, B, SFB, VARIANTS[v])
+    D_ref, _ = ref(A, SFA, B, SFB)
+    assert np.all(np.abs(D_ref[np.nonzero(D_ref)]) >= 2.0 ** -9)   # far from underflow
+    assert_matches_oracle(D, D_ref, f"scale 0 subnormal/{v}")
+    A2, _, _, _ = int_operands(M, N, K, seed=35)
+    D = run(A2, SFA, B, SFB, VARIANTS[v])
+    D_ref, _ = ref(A2, SFA, B, SFB)
+    assert_matches_oracle(D, D_ref, f"scale 0 normal/{v}")
+
+
+@pytest.mark.parametrize("v", MX_VARIANTS)
+def test_zero_scales_underflow_to_zero(v):
+    """Both scales 2^-127 (byte 0): every product is below 2^-248, far under
+    the smallest bf16 (and fp32) subnormal, so the oracle's value rounds to
+    zero and D must be zero everywhere."""
+    M, N, K = 130, 260, 128
+    A, _, B, _ = int_operands(M, N, K, seed=36)
+    A[:, :K] = P.e4m3_from_ints(np.random.default_rng(37).integers(1, 5, size=(M, K)))
+    SFA = torch.zeros(M, gi.sf_pitch(K), dtype=torch.uint8)
+    SFB = torch.zeros(N, gi.sf_pitch(K), dtype=torch.uint8)
+    D = run(A, SFA, B, SFB, VARIANTS[v])
+    D_ref, _ = ref(A, SFA, B, SFB)
+    assert np.all(np.abs(D_ref) < 2.0 ** -240) and np.any(D_ref != 0)
+    assert_matches_oracle(D, D_ref, f"underflow/{v}")
+
+
+# ------------------------------------------- scale matrices in any layout (gathered)
+
+def run_sf_layout(A, SFA_rows, B, SFB_rows, variant, K, ldsf, offset):
+    """The scale rows stored at pitch `ldsf` bytes, `offset` bytes into a
+    device buffer (so the base may be misaligned)."""
+    M, N = A.shape[0], B.shape[0]
+    nblk = (K + 31) // 32
+
+    def place(sf_rows):
+        R = sf_rows.shape[0]
+        buf = torch.full((offset + R * ldsf + 64,), 0xFF, dtype=torch.uint8)   # NaN scales around
+        view = buf[offset:offset + R * ldsf].view(R, ldsf)
+        view[:, :nblk] = sf_rows[:, :nblk]
+        return buf.cuda(), view
+
+    sa_dev, sa = place(SFA_rows)
+    sb_dev, sb = place(SFB_rows)
+    Ad, Bd = A.cuda(), B.cuda()
+    D = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    rc = g.gemm_mxfp8_variant(variant, Ad.data_ptr(), Bd.data_ptr(), sa_dev.data_ptr() + offset,
+                              sb_dev.data_ptr() + offset, D.data_ptr(), M, N, K, A.shape[1],
+                              B.shape[1], ldsf, ldsf, N, s)
+    assert rc == g.GEMM_OK, g.gemm_status_string(rc)
+    st = g.gemm_last_status(s)
+    assert st == g.GEMM_OK, g.gemm_status_string(st)
+    return D.cpu(), sa, sb
+
+
+@pytest.mark.parametrize("v", MX_VARIANTS)
+@pytest.mark.parametrize("ldsf, offset", [(33, 0), (33, 1), (40, 4), (48, 3)])
+def test_dense_scale_layout_k1040(v, ldsf, offset):
+    """K = 1040 (33 scale blocks, a partial K-tile) with the scale matrices
+    in the dense layout ld = ceil(K/32) = 33, and at other pitches and base
+    offsets that TMA cannot read; bytes around the rows hold NaN scales that
+    must not be read.  Exact integer operands: bitwise against the oracle."""
+    M, N, K = 300, 470, 1040
+    A, SFA, B, SFB = int_operands(M, N, K, seed=38, lda=1040)
+    D, sa, sb = run_sf_layout(A, SFA, B, SFB, VARIANTS[v], K, ldsf, offset)
+    D_ref, _ = ref(A, sa, B, sb, K)
+    assert_matches_oracle(D, D_ref, f"dense scales ld={ldsf} off={offset}/{v}")
+
+
+def test_dense_scale_layout_quantised_normal():
+    """Quantised N(0,1) operands, dense scale layout, several waves of tiles."""
+    M, N, K = 1100, 1500, 1040
+    A, SFA, B, SFB = gi.mxfp8_operands(M, N, K, seed=39)
+    D, sa, sb = run_sf_layout(A, SFA, B, SFB, g.VARIANT_AUTO, K, 33, 0)
+    D_ref, S = ref(A, sa, B, sb, K)
+    P.check_within_bound(P.bf16_to_f64(D), D_ref, S, "dense scales, quantised")
