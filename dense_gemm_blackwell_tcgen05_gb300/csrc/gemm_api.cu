@@ -133,6 +133,7 @@ int check_shape(const void* A, const void* B, void* D, int64_t M, int64_t N, int
     return GEMM_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return GEMM_OK;
   if (D == nullptr || ldd < N || ldd > (int64_t(1) << 36)) return GEMM_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(D) & 1u) != 0) return GEMM_ERR_ALIGNMENT;   // bf16 elements
   if (K == 0) return GEMM_OK;
   if (A == nullptr || B == nullptr || lda < K || ldb < K || lda > (int64_t(1) << 36) ||
       ldb > (int64_t(1) << 36))
@@ -154,6 +155,20 @@ int64_t timeout_ns_for(int64_t K) {
   // The longest legitimate wait is about one tile's main loop; allow 64 ns per
   // k on top of the fixed limit (eight times a pessimistic per-SM rate).
   return watchdog_ms() * 1000000ll + K * 64ll;
+}
+
+// Every element of D, C and bias is accessed at its own alignment: the
+// pointers must be multiples of their element sizes.  (Checked before any
+// device work, like the shape.)
+int check_epilogue_alignment(const gemm_epilogue_t* e, const void* D) {
+  if (e == nullptr) return GEMM_OK;
+  const uintptr_t osz = e->out_dtype == GEMM_DTYPE_F32 ? 4u : 2u;
+  if ((reinterpret_cast<uintptr_t>(D) & (osz - 1)) != 0 ||
+      (e->C != nullptr && (reinterpret_cast<uintptr_t>(e->C) & (osz - 1)) != 0) ||
+      (e->bias != nullptr &&
+       (reinterpret_cast<uintptr_t>(e->bias) & (e->bias_dtype == GEMM_DTYPE_F32 ? 3u : 1u)) != 0))
+    return GEMM_ERR_ALIGNMENT;
+  return GEMM_OK;
 }
 
 // Fills the fused-epilogue fields of `p` from `e` (NULL: the plain store).
@@ -284,6 +299,7 @@ static int bf16_impl(int variant, const void* A, const void* B, void* D, int64_t
   if (base == GEMM_VARIANT_SMALLK && (ws != nullptr || epi != nullptr || K > smallk_max_k()))
     return GEMM_ERR_INVALID_ARG;
   int rc = check_shape(A, B, D, M, N, K, lda, ldb, ldd, 2);
+  if (rc == GEMM_OK && M != 0 && N != 0) rc = check_epilogue_alignment(epi, D);
   if (rc != GEMM_OK || M == 0 || N == 0) return rc;
   LaunchCtx ctx;
   if ((rc = current_device(&ctx)) != GEMM_OK) return rc;
@@ -324,10 +340,10 @@ static int bf16_impl(int variant, const void* A, const void* B, void* D, int64_t
   // Small K is a write of D: the CUDA-core kernel unless the call needs the
   // persistent kernel's extras (an epilogue, a stream-K workspace).
   if (base == GEMM_VARIANT_AUTO && K <= smallk_max_k() && p.epi_mode == 0 && ws == nullptr)
-    return launch_bf16_smallk(p, stream);
+    return launch_bf16_smallk(p, ctx.num_sms, stream);
   switch (base) {
     case GEMM_VARIANT_SMALLK:
-      return launch_bf16_smallk(p, stream);
+      return launch_bf16_smallk(p, ctx.num_sms, stream);
     case GEMM_VARIANT_SYNC:
       return launch_bf16_sync(p, ctx, stream);
     case GEMM_VARIANT_1CTA:
@@ -376,6 +392,7 @@ static int mxfp8_impl(int variant, const void* A, const void* B, const void* SFA
   if ((variant & ~(0xFF | GEMM_VARIANT_DIRECT_STORE)) != 0 || base > GEMM_VARIANT_2CTA)
     return GEMM_ERR_INVALID_ARG;
   int rc = check_shape(A, B, D, M, N, K, lda, ldb, ldd, 1);
+  if (rc == GEMM_OK && M != 0 && N != 0) rc = check_epilogue_alignment(epi, D);
   if (rc != GEMM_OK || M == 0 || N == 0) return rc;
   if (K > 0) {
     const int64_t nblk = (K + 31) / 32;

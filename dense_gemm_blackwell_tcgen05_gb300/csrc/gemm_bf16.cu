@@ -36,8 +36,8 @@ bool plan_bf16(int cg, bool tma_store, KernelPlan* out) {
     *out = KernelPlan{1, 0, 128, 128, 1, 128, 128};
     return true;
   }
-  if (cg == 4) {   // small-K CUDA-core kernel: 64 rows of A (fp32) in shared memory
-    *out = KernelPlan{0, 64 * 16 * 4, 0, 256, 1, 64, 256};
+  if (cg == 4) {   // small-K CUDA-core kernel: 128-row tiles of A (fp32) in shared memory
+    *out = KernelPlan{0, 128 * 16 * 4, 0, 256, 1, 128, 256};
     return true;
   }
   return false;

@@ -136,7 +136,7 @@ int launch_mxf8_ws(int cg, bool tma_store, const Problem& p, const LaunchCtx& ct
                    cudaStream_t stream);
 int launch_zero_fill(const Problem& p, cudaStream_t stream);
 // CUDA-core kernel for 1 <= K <= smallk_max_k() (plain bf16 store only).
-int launch_bf16_smallk(const Problem& p, cudaStream_t stream);
+int launch_bf16_smallk(const Problem& p, int num_sms, cudaStream_t stream);
 uint32_t smallk_max_k();
 // K == 0 with a fused epilogue: D = act(alpha * 0 + beta * C + bias).
 int launch_epilogue_only(const Problem& p, int num_sms, cudaStream_t stream);

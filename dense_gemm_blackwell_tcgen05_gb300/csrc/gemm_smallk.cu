@@ -1,21 +1,27 @@
 // Small-K bf16 GEMM on the CUDA cores (GEMM_VARIANT_SMALLK; the automatic
 // choice for K <= 16).  With so few products per output the operation is a
-// write of D, HBM-bound at about 8 flops per byte: the tensor-core path would
-// move a mostly zero-filled 64-wide K box per tile for 16 or fewer real
-// columns and wait on it, so this kernel skips staging through TMEM and
-// spends its time on coalesced stores instead.
+// write of D at about K flops per output byte: the tensor-core path would move
+// a mostly zero-filled 64-wide K box per tile for 16 or fewer real columns and
+// then drain a whole TMEM accumulator per tile, so this kernel keeps
+// everything in registers and spends its time on wide, aligned stores.
 //
-// A block covers 64 rows x 256 columns of D with 8 warps.  A lane owns CPL = 4
-// consecutive columns (8 measured slower: fewer resident blocks and, on odd
-// pitches, twice the 2-byte stores) and keeps their K values
-// of B in registers for the whole block; a warp covers 32 CPL columns and
-// walks its share of the block's rows.  A's rows are staged in shared memory
-// (fp32) and read as broadcasts.  Per row a warp writes 32 CPL * 2 contiguous
-// bytes, in 16-, 8-, 4- or 2-byte pieces as the row's address allows.  K is
-// rounded up to a compile-time 4, 8 or 16 (zero-padded).  Sums are fp32 FMAs
-// in k order, rounded once to bf16 (RNE).  The kernel is bound by instruction
-// issue rather than HBM on the ragged shapes: per output about K FMAs plus a
-// share of a row's broadcast loads, conversion and store.
+// Layout of the work.  A block of 8 warps owns one strip of 32 * CPL columns
+// of D (CPL = 8 consecutive columns per lane, 4 for K > 8) and row tiles of
+// kTileRows rows (grid-stride over the tiles).  A row tile's A values are
+// staged once in shared memory as fp32 pairs (a, a) and read back as
+// broadcasts.  Warp w computes rows w, w + 8, ... of the tile: per row a lane
+// forms its CPL sums with packed fp32 FMAs (two columns per instruction) in
+// k order, rounds them once to bf16 (RNE) and stores them as one 2*CPL-byte
+// piece.
+//
+// Stores.  A warp's rows all start the same number e of elements past a
+// 2*CPL-byte boundary (the rows are 8 apart and CPL divides 8), whatever the
+// pitch.  So each warp's strip is shifted back by its own e columns: every
+// lane's CPL columns then sit on one aligned 2*CPL-byte piece in every row
+// it writes, and the only narrower stores are at the matrix's left and right
+// edges (2 bytes per column there).  Each lane keeps the K values of B for
+// its columns in registers for the whole block.  Nothing outside row x
+// [0, N) is written and nothing at k >= K is read.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -27,8 +33,7 @@
 namespace gb300 {
 namespace {
 
-constexpr uint32_t kRows = 64;        // D rows per block
-constexpr uint32_t kCols = 256;       // D columns per block
+constexpr uint32_t kTileRows = 128;   // rows of A staged per tile
 constexpr uint32_t kMaxK = 16;
 constexpr uint32_t kThreadsSmallK = 256;
 
@@ -51,7 +56,7 @@ __device__ __forceinline__ void load_row(const uint16_t* p, uint32_t K, float (&
 #pragma unroll
   for (uint32_t h = 0; h < (KK + 7) / 8; ++h) {
     if (8 * (h + 1) <= KK && K >= 8 * (h + 1)) {
-      const uint4 w = *reinterpret_cast<const uint4*>(p + 8 * h);
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(p + 8 * h));
       const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
       for (uint32_t i = 0; i < 4; ++i) {
@@ -62,95 +67,94 @@ __device__ __forceinline__ void load_row(const uint16_t* p, uint32_t K, float (&
 #pragma unroll
       for (uint32_t i = 0; i < 8; ++i) {
         const uint32_t k = 8 * h + i;
-        if (k < KK) x[k] = k < K ? bf16f(p[k]) : 0.0f;
+        if (k < KK) x[k] = k < K ? bf16f(__ldg(p + k)) : 0.0f;
       }
     }
-  }
-}
-
-// Four consecutive outputs (packed bf16 pairs p01, p23) at dp, n of them
-// valid, in the widest pieces the address allows.
-__device__ __forceinline__ void store4(uint16_t* dp, uint32_t p01, uint32_t p23, uint32_t n) {
-  const uintptr_t al = reinterpret_cast<uintptr_t>(dp);
-  if (n == 4 && (al & 7u) == 0) {
-    *reinterpret_cast<uint2*>(dp) = make_uint2(p01, p23);
-  } else if ((al & 3u) == 0) {
-    if (n >= 2) *reinterpret_cast<uint32_t*>(dp) = p01;
-    else dp[0] = static_cast<uint16_t>(p01 & 0xFFFFu);
-    if (n == 4) *reinterpret_cast<uint32_t*>(dp + 2) = p23;
-    else if (n == 3) dp[2] = static_cast<uint16_t>(p23 & 0xFFFFu);
-  } else {
-    dp[0] = static_cast<uint16_t>(p01 & 0xFFFFu);
-    if (n > 1) dp[1] = static_cast<uint16_t>(p01 >> 16);
-    if (n > 2) dp[2] = static_cast<uint16_t>(p23 & 0xFFFFu);
-    if (n > 3) dp[3] = static_cast<uint16_t>(p23 >> 16);
   }
 }
 
 template <uint32_t KK, uint32_t CPL>
-__global__ void __launch_bounds__(kThreadsSmallK) gemm_smallk_kernel(const SmallKArgs a) {
-  constexpr uint32_t kWarpCols = 32 * CPL;
-  constexpr uint32_t kWarpsPerRow = kCols / kWarpCols;           // 2 (CPL 4) or 1 (CPL 8)
-  constexpr uint32_t kRowsPerWarp = kRows * kWarpsPerRow / 8;    // 16 or 8
-  __shared__ __align__(16) float sA[kRows][KK];
+__global__ void __launch_bounds__(kThreadsSmallK, 2) gemm_smallk_kernel(const SmallKArgs a) {
+  constexpr uint32_t W = CPL / 2;            // packed words per lane and row
+  constexpr uint32_t kStrip = 32 * CPL;      // columns of a warp's strip
+  // A row tile as fp32 pairs (a, a): one 16-byte broadcast load feeds two
+  // packed FMAs
+  __shared__ __align__(16) float2 sA[kTileRows][KK];
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
-  const uint32_t c = blockIdx.x * kCols + kWarpCols * (warp % kWarpsPerRow) + CPL * lane;
-  const uint32_t r_base = kRowsPerWarp * (warp / kWarpsPerRow);
-  // B values of columns c .. c + CPL - 1, kept in registers (zero past N)
-  float b[CPL][KK];
+  // This warp's rows (warp, warp + 8, ... of every tile) all start the same
+  // number e of elements past a 2*CPL-byte boundary: tiles start at multiples
+  // of 8 rows, and CPL divides 8.  Shifting the warp's strip back by e
+  // columns puts every lane's CPL columns on such a boundary in every row.
+  const uint32_t e = static_cast<uint32_t>(
+      (reinterpret_cast<uintptr_t>(a.D + static_cast<uint64_t>(warp) * a.ldd) >> 1) & (CPL - 1u));
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kStrip - e + CPL * lane;   // first column
+  const bool lane_full = c0 >= 0 && c0 + CPL <= a.N;
+  const bool lane_any = c0 + CPL > 0 && c0 < static_cast<int64_t>(a.N);
+  // B values of columns c0 .. c0 + CPL - 1 in registers as column pairs
+  // (zero outside [0, N))
+  float2 b[W][KK];
 #pragma unroll
-  for (uint32_t t = 0; t < CPL; ++t) {
-    if (c + t < a.N) {
-      load_row<KK>(a.B + static_cast<uint64_t>(c + t) * a.ldb, a.K, b[t]);
+  for (uint32_t p = 0; p < W; ++p) {
+    float lo[KK], hi[KK];
+    const int64_t cl = c0 + 2 * p, ch = cl + 1;
+    if (cl >= 0 && cl < a.N) {
+      load_row<KK>(a.B + static_cast<uint64_t>(cl) * a.ldb, a.K, lo);
     } else {
 #pragma unroll
-      for (uint32_t k = 0; k < KK; ++k) b[t][k] = 0.0f;
+      for (uint32_t k = 0; k < KK; ++k) lo[k] = 0.0f;
     }
+    if (ch >= 0 && ch < a.N) {
+      load_row<KK>(a.B + static_cast<uint64_t>(ch) * a.ldb, a.K, hi);
+    } else {
+#pragma unroll
+      for (uint32_t k = 0; k < KK; ++k) hi[k] = 0.0f;
+    }
+#pragma unroll
+    for (uint32_t k = 0; k < KK; ++k) b[p][k] = make_float2(lo[k], hi[k]);
   }
-  for (uint32_t rt = blockIdx.y; rt * kRows < a.M; rt += gridDim.y) {
-    const uint32_t row0 = rt * kRows;
+  for (uint32_t rt = blockIdx.y; rt * kTileRows < a.M; rt += gridDim.y) {
+    const uint32_t row0 = rt * kTileRows;
+    const uint32_t nrows = min(kTileRows, a.M - row0);
     __syncthreads();   // the previous row tile's reads of sA are done
-    if (threadIdx.x < kRows) {
+    if (threadIdx.x < nrows) {
       float x[KK];
-      const uint32_t row = row0 + threadIdx.x;
-      if (row < a.M) {
-        load_row<KK>(a.A + static_cast<uint64_t>(row) * a.lda, a.K, x);
-      } else {
+      load_row<KK>(a.A + static_cast<uint64_t>(row0 + threadIdx.x) * a.lda, a.K, x);
 #pragma unroll
-        for (uint32_t k = 0; k < KK; ++k) x[k] = 0.0f;
-      }
-#pragma unroll
-      for (uint32_t k = 0; k < KK; k += 4)
-        *reinterpret_cast<float4*>(&sA[threadIdx.x][k]) = make_float4(x[k], x[k + 1], x[k + 2], x[k + 3]);
+      for (uint32_t k = 0; k < KK; k += 2)
+        *reinterpret_cast<float4*>(&sA[threadIdx.x][k]) = make_float4(x[k], x[k], x[k + 1], x[k + 1]);
     }
     __syncthreads();
-    if (c >= a.N || row0 + r_base >= a.M) continue;
-    const uint32_t nvalid = min(CPL, a.N - c);
-    const uint32_t nrows = min(kRowsPerWarp, a.M - (row0 + r_base));
-    uint16_t* dp = a.D + static_cast<uint64_t>(row0 + r_base) * a.ldd + c;
 #pragma unroll 2
-    for (uint32_t r = 0; r < nrows; ++r, dp += a.ldd) {
-      float x[CPL];
+    for (uint32_t r = warp; r < nrows; r += 8) {
+      float2 acc[W];
 #pragma unroll
-      for (uint32_t t = 0; t < CPL; ++t) x[t] = 0.0f;
+      for (uint32_t p = 0; p < W; ++p) acc[p] = make_float2(0.0f, 0.0f);
 #pragma unroll
-      for (uint32_t k = 0; k < KK; k += 4) {
-        const float4 av = *reinterpret_cast<const float4*>(&sA[r_base + r][k]);   // broadcast
-        const float ak[4] = {av.x, av.y, av.z, av.w};
+      for (uint32_t k = 0; k < KK; k += 2) {
+        const float4 av = *reinterpret_cast<const float4*>(&sA[r][k]);   // (a_k, a_k, a_k+1, a_k+1)
 #pragma unroll
-        for (uint32_t i = 0; i < 4; ++i)
+        for (uint32_t p = 0; p < W; ++p)
+          acc[p] = __ffma2_rn(make_float2(av.x, av.y), b[p][k], acc[p]);
 #pragma unroll
-          for (uint32_t t = 0; t < CPL; ++t) x[t] = fmaf(ak[i], b[t][k + i], x[t]);
+        for (uint32_t p = 0; p < W; ++p)
+          acc[p] = __ffma2_rn(make_float2(av.z, av.w), b[p][k + 1], acc[p]);
       }
-      uint32_t pk[CPL / 2];
+      uint32_t v[W];
 #pragma unroll
-      for (uint32_t t = 0; t < CPL / 2; ++t) pk[t] = pack_bf16x2(x[2 * t], x[2 * t + 1]);
-      if (CPL == 8 && nvalid == 8 && (reinterpret_cast<uintptr_t>(dp) & 15u) == 0) {
-        *reinterpret_cast<uint4*>(dp) = make_uint4(pk[0], pk[1], pk[2 % (CPL / 2)], pk[3 % (CPL / 2)]);
-      } else {
+      for (uint32_t p = 0; p < W; ++p) v[p] = pack_bf16x2(acc[p].x, acc[p].y);
+      // 2*CPL-byte aligned: the row's start is e elements past a boundary
+      uint16_t* const dst = a.D + static_cast<int64_t>(row0 + r) * static_cast<int64_t>(a.ldd) + c0;
+      if (lane_full) {
+        if constexpr (W == 4)
+          *reinterpret_cast<uint4*>(dst) = make_uint4(v[0], v[1], v[2], v[3]);
+        else
+          *reinterpret_cast<uint2*>(dst) = make_uint2(v[0], v[1]);
+      } else if (lane_any) {
+        // the matrix's left or right edge: one 2-byte store per column inside
 #pragma unroll
-        for (uint32_t g = 0; g < CPL / 4; ++g)
-          if (4 * g < nvalid) store4(dp + 4 * g, pk[2 * g], pk[2 * g + 1], min(4u, nvalid - 4 * g));
+        for (uint32_t t = 0; t < CPL; ++t)
+          if (c0 + t >= 0 && c0 + t < a.N)
+            dst[t] = static_cast<uint16_t>(t % 2 ? v[t / 2] >> 16 : v[t / 2] & 0xFFFFu);
       }
     }
   }
@@ -160,7 +164,7 @@ __global__ void __launch_bounds__(kThreadsSmallK) gemm_smallk_kernel(const Small
 
 uint32_t smallk_max_k() { return kMaxK; }
 
-int launch_bf16_smallk(const Problem& p, cudaStream_t stream) {
+int launch_bf16_smallk(const Problem& p, int num_sms, cudaStream_t stream) {
   if (p.K == 0 || p.K > kMaxK) return GEMM_ERR_INVALID_ARG;
   SmallKArgs a;
   a.A = static_cast<const uint16_t*>(p.A);
@@ -172,15 +176,23 @@ int launch_bf16_smallk(const Problem& p, cudaStream_t stream) {
   a.lda = p.lda;
   a.ldb = p.ldb;
   a.ldd = p.ldd;
-  const uint64_t col_tiles = (static_cast<uint64_t>(p.N) + kCols - 1) / kCols;
-  const uint64_t row_tiles = (static_cast<uint64_t>(p.M) + kRows - 1) / kRows;
-  if (col_tiles > 0x7FFFFFFFull) return GEMM_ERR_INVALID_ARG;
-  const dim3 grid(static_cast<unsigned>(col_tiles),
-                  static_cast<unsigned>(row_tiles < 65535 ? row_tiles : 65535));
+  const uint32_t cpl = p.K <= 8 ? 8u : 4u;
+  // a warp's strip starts up to cpl - 1 columns before the block's, so the
+  // strips must cover N + cpl - 1 columns
+  const uint64_t strips = (static_cast<uint64_t>(p.N) + cpl - 1 + 32 * cpl - 1) / (32 * cpl);
+  const uint64_t row_tiles = (static_cast<uint64_t>(p.M) + kTileRows - 1) / kTileRows;
+  if (strips > 0x7FFFFFFFull) return GEMM_ERR_INVALID_ARG;
+  // one wave of two blocks per SM; each block walks its strip's row tiles
+  const uint64_t target = 2ull * static_cast<uint64_t>(num_sms > 0 ? num_sms : 1);
+  uint64_t gy = (target + strips - 1) / strips;
+  if (gy > row_tiles) gy = row_tiles;
+  if (gy > 65535) gy = 65535;
+  if (gy < 1) gy = 1;
+  const dim3 grid(static_cast<unsigned>(strips), static_cast<unsigned>(gy));
   if (p.K <= 4)
-    gemm_smallk_kernel<4, 4><<<grid, kThreadsSmallK, 0, stream>>>(a);
+    gemm_smallk_kernel<4, 8><<<grid, kThreadsSmallK, 0, stream>>>(a);
   else if (p.K <= 8)
-    gemm_smallk_kernel<8, 4><<<grid, kThreadsSmallK, 0, stream>>>(a);
+    gemm_smallk_kernel<8, 8><<<grid, kThreadsSmallK, 0, stream>>>(a);
   else
     gemm_smallk_kernel<16, 4><<<grid, kThreadsSmallK, 0, stream>>>(a);
   if (const cudaError_t e = cudaGetLastError(); e != cudaSuccess) {

@@ -32,13 +32,15 @@
  *                         whose byte size is not a multiple of 16 (the TMA
  *                         engine's rule): bf16 needs lda, ldb multiples of
  *                         8, E4M3 multiples of 16 (MXFP8 scale matrices
- *                         take any pitch and alignment)
+ *                         take any pitch and alignment); or D (C, bias of a
+ *                         fused epilogue) not aligned to its element size
  *   GEMM_ERR_UNSUPPORTED_DEVICE  the current device is not compute
  *                         capability 10.3 (sm_103); there is no fallback
  *   GEMM_ERR_LAUNCH       the CUDA launch (or tensor-map encoding) failed
  * M == 0 or N == 0 is a no-op that returns GEMM_OK.  K == 0 writes D = 0
- * (the empty sum).  D may have any pitch and alignment: when its rows are not
- * 16-byte aligned the epilogue uses masked stores instead of TMA stores.
+ * (the empty sum).  D may have any pitch (ldd >= N) and any element-aligned
+ * base: when its rows are not 16-byte aligned the epilogue uses masked stores
+ * instead of TMA stores.
  */
 #ifndef GEMM_GB300_H
 #define GEMM_GB300_H

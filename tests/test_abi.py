@@ -69,6 +69,13 @@ def test_bf16_null_and_misaligned_pointers():
     assert g.gemm_bf16(NULL, FAKE, FAKE, 4, 4, 16, 16, 16, 4, 0) == g.GEMM_ERR_INVALID_ARG
     assert g.gemm_bf16(FAKE, FAKE, NULL, 4, 4, 16, 16, 16, 4, 0) == g.GEMM_ERR_INVALID_ARG
     assert g.gemm_bf16(FAKE + 8, FAKE, FAKE, 4, 4, 16, 16, 16, 4, 0) == g.GEMM_ERR_ALIGNMENT
+    # D's elements must sit at their own alignment (2 bytes for bf16)
+    assert g.gemm_bf16(FAKE, FAKE, FAKE + 1, 4, 4, 16, 16, 16, 4, 0) == g.GEMM_ERR_ALIGNMENT
+    e = g.GemmEpilogue()
+    e.alpha, e.out_dtype = 1.0, g.DTYPE_F32
+    assert g.gemm_bf16_fused(0, FAKE, FAKE, FAKE + 2, 4, 4, 16, 16, 16, 4, e, 0) == g.GEMM_ERR_ALIGNMENT
+    e.out_dtype, e.bias, e.bias_dtype = g.DTYPE_BF16, FAKE + 1, g.DTYPE_BF16
+    assert g.gemm_bf16_fused(0, FAKE, FAKE, FAKE, 4, 4, 16, 16, 16, 4, e, 0) == g.GEMM_ERR_ALIGNMENT
 
 
 def test_variant_validation():

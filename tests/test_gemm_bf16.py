@@ -307,6 +307,44 @@ def test_smallk_small_integers_bitwise(v, M, N, K, lda, ldd):
     assert_bitwise(D[:, :N], D_ref)
 
 
+@pytest.mark.parametrize("M, N, K, ldd, offset", [
+    (64, 2053, 8, 2053, 0), (64, 2053, 8, 2053, 3), (40, 257, 5, 261, 1), (40, 255, 8, 255, 7),
+    (48, 513, 12, 515, 2), (48, 127, 16, 133, 5), (70000, 40, 4, 41, 1), (300, 1, 8, 1, 1)])
+def test_smallk_any_row_alignment(M, N, K, ldd, offset):
+    """Rows that start at every element offset within a 16-byte line (odd
+    pitches, D placed `offset` elements into its buffer), ragged column strips
+    and a grid that walks several row tiles per block: bitwise, and nothing
+    written before D, between rows or after the last row."""
+    gen = torch.Generator().manual_seed(M + N + K + ldd)
+    lda = (K + 7) // 8 * 8
+    A = torch.zeros(M, lda, dtype=torch.bfloat16)
+    B = torch.zeros(N, lda, dtype=torch.bfloat16)
+    A[:, :K] = torch.randint(-4, 5, (M, K), generator=gen).to(torch.bfloat16)
+    B[:, :K] = torch.randint(-4, 5, (N, K), generator=gen).to(torch.bfloat16)
+    Ad, Bd = A.cuda(), B.cuda()
+    buf = torch.full((offset + M * ldd + 64,), -1234.0, dtype=torch.bfloat16, device="cuda")
+    dptr = buf.data_ptr() + 2 * offset
+    rc = g.gemm_bf16_variant(g.VARIANT_SMALLK, Ad.data_ptr(), Bd.data_ptr(), dptr, M, N, K, lda,
+                             lda, ldd, 0)
+    assert rc == g.GEMM_OK, g.gemm_status_string(rc)
+    assert g.gemm_last_status(0) == g.GEMM_OK
+    host = buf.cpu()
+    sentinel = torch.tensor(-1234.0).to(torch.bfloat16)
+    assert torch.all(host[:offset] == sentinel) and torch.all(host[offset + M * ldd:] == sentinel)
+    D = host[offset:offset + M * ldd].view(M, ldd)
+    assert torch.all(D[:, N:] == sentinel)
+    D_ref, _ = ref(A, B, K)
+    assert_bitwise(D[:, :N], D_ref)
+
+
+def test_smallk_rejects_an_odd_byte_address():
+    A = torch.zeros(8, 8, dtype=torch.bfloat16, device="cuda")
+    buf = torch.zeros(100, dtype=torch.uint8, device="cuda")
+    rc = g.gemm_bf16_variant(g.VARIANT_SMALLK, A.data_ptr(), A.data_ptr(), buf.data_ptr() + 1, 8,
+                             8, 8, 8, 8, 8, 0)
+    assert rc == g.GEMM_ERR_ALIGNMENT
+
+
 def test_smallk_random_within_bound():
     A, B = gi.bf16_operands(1000, 777, 16, seed=41)
     D = run(A, B, g.VARIANT_SMALLK)
