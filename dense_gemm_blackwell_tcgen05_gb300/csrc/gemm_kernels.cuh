@@ -246,13 +246,16 @@ struct GemmCfg {
   static constexpr uint32_t TMEM_COLS = 512;
   static_assert(SF_TMEM_COL + (MX ? 4 + 4 * SFB_CHUNKS : 0) <= TMEM_COLS, "TMEM column budget");
 
-  // Epilogue staging for TMA stores: per epilogue warp, two 32x64 bf16
-  // buffers (32 rows of 128 bytes, 128-byte swizzled).
-  static_assert(!TMA_STORE || UMMA_N % 64 == 0, "TMA-store epilogue works in 64-column chunks");
+  // Epilogue staging for TMA stores: per epilogue warp, two buffers of 32
+  // rows x TS_COLS bf16 columns -- 64 columns (128-byte rows, 128-byte
+  // swizzle) where the tile width allows, else 32 (64-byte rows, 64-byte
+  // swizzle: the MXFP8 tiles are 224 = 7 x 32 columns wide).
+  static constexpr uint32_t TS_COLS = UMMA_N % 64 == 0 ? 64 : 32;
+  static_assert(!TMA_STORE || UMMA_N % TS_COLS == 0, "TMA-store chunks tile the accumulator");
   // The masked-store epilogue instead stages one 32x32 chunk per warp (2 KB)
   // and writes it back row by row, lanes across columns, so its global stores
   // are coalesced whatever the pitch.
-  static constexpr uint32_t EPI_BUF_BYTES = 32 * 128;
+  static constexpr uint32_t EPI_BUF_BYTES = 32 * TS_COLS * 2;
   static constexpr uint32_t EPI_BUFS = 2;
   static constexpr uint32_t CHUNK_BYTES = 32 * 64;
   static constexpr uint32_t EPI_BYTES =
@@ -970,7 +973,38 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
         }
       }
       if (w.kind != 2 && ok && row0 < args.M) {
-        if constexpr (TMA_STORE) {
+        if constexpr (TMA_STORE && C::TS_COLS == 32) {
+          // 32-column chunks: one tcgen05.ld, one 32x32 box per chunk
+#pragma unroll 1
+          for (uint32_t c = 0; c < C::UMMA_N / 32; ++c) {
+            if (col_base + c * 32 >= args.N) break;
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(t_addr + c * 32, v);
+            tmem_wait_ld();
+            if (w.kind == 1 && !add_partials(v, c)) { ok = false; break; }
+            if (args.epi_mode != 0) epi_apply(v, args, row0 + lane, col_base + c * 32);
+            const uint32_t buf = epi0 + (ew * C::EPI_BUFS + (chunk_ctr % C::EPI_BUFS)) * C::EPI_BUF_BYTES;
+            if (lane == 0) bulk_wait_group_read<C::EPI_BUFS - 1>();   // this buffer's last store has read it
+            __syncwarp();
+            uint8_t* rowp = base_ptr + (buf - base) + lane * 64;
+#pragma unroll
+            for (uint32_t i = 0; i < 4; ++i) {
+              const uint4 val = make_uint4(pack_bf16x2(__uint_as_float(v[8 * i + 0]), __uint_as_float(v[8 * i + 1])),
+                                           pack_bf16x2(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3])),
+                                           pack_bf16x2(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5])),
+                                           pack_bf16x2(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7])));
+              // 64-byte swizzle: 16-byte chunk i of row r sits at chunk i ^ ((r / 2) % 4)
+              *reinterpret_cast<uint4*>(rowp + ((i ^ ((lane >> 1) & 3u)) << 4)) = val;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmD, buf, static_cast<int32_t>(col_base + c * 32), static_cast<int32_t>(row0));
+              bulk_commit_group();
+            }
+            ++chunk_ctr;
+          }
+        } else if constexpr (TMA_STORE) {
 #pragma unroll 1
           for (uint32_t c = 0; c < C::UMMA_N / 64; ++c) {
             if (col_base + c * 64 >= args.N) break;

@@ -97,8 +97,8 @@ int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) 
                      CU_TENSOR_MAP_SWIZZLE_128B))
     return GEMM_ERR_LAUNCH;
   if constexpr (TMA_STORE) {
-    if (!encode_map_2d(&maps.D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.D, p.N, p.M, p.ldd * 2, 64, 32,
-                       CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!encode_map_2d(&maps.D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.D, p.N, p.M, p.ldd * 2, C::TS_COLS,
+                       32, C::TS_COLS == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
       return GEMM_ERR_LAUNCH;
   }
   // Scale bytes travel by TMA when both matrices are 16-byte aligned with

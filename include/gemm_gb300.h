@@ -73,8 +73,7 @@ typedef enum {
                                    (ladder levels 4-7)                             */
   GEMM_VARIANT_2CTA = 2,        /* persistent warp-specialised CTA pair,
                                    cta_group::2, 256x256 tiles (bf16) or 256x224
-                                   tiles (MXFP8, masked-store epilogue)
-                                   (ladder level 8)                                */
+                                   tiles (MXFP8) (ladder level 8)                  */
   GEMM_VARIANT_SYNC = 3,        /* one 128x128 tile per CTA, synchronous copies
                                    (ladder levels 1-3; bf16 only, reference rung)  */
   GEMM_VARIANT_SMALLK = 4,      /* bf16 only, 1 <= K <= 16: CUDA-core kernel for
@@ -84,10 +83,12 @@ typedef enum {
   GEMM_VARIANT_DIRECT_STORE = 0x100  /* flag: masked st.global epilogue instead of
                                         TMA stores, even when D is aligned.  Without
                                         it the library picks: TMA stores where D is
-                                        aligned, except that a bf16 stream-K launch
-                                        that splits tiles takes the masked kernel,
-                                        whose two epilogue warpgroups share the
-                                        partial sums                               */
+                                        16-byte aligned with ldd and N multiples of
+                                        8 (64-column boxes for bf16, 32-column for
+                                        MXFP8), except that a stream-K launch that
+                                        splits tiles (bf16, or MXFP8 on one CTA)
+                                        takes the masked kernel, whose two epilogue
+                                        warpgroups share the partial sums          */
 } gemm_variant_t;
 
 /*

@@ -300,3 +300,26 @@ def test_dense_scale_layout_quantised_normal():
     D, sa, sb = run_sf_layout(A, SFA, B, SFB, g.VARIANT_AUTO, K, 33, 0)
     D_ref, S = ref(A, sa, B, sb, K)
     P.check_within_bound(P.bf16_to_f64(D), D_ref, S, "dense scales, quantised")
+
+
+@pytest.mark.parametrize("v", ["1cta", "2cta"])
+@pytest.mark.parametrize("M, N, ldd", [(300, 520, 536), (129, 456, 456), (257, 1000, 1008)])
+def test_tma_store_epilogue_guard_band(v, M, N, ldd):
+    """The 32-column TMA-store epilogue of the MXFP8 kernels (aligned D, N * 2
+    a multiple of 16): ragged M and N against the 224-column tiles, exact,
+    and the pitch padding never written."""
+    K = 256
+    A, SFA, B, SFB = int_operands(M, N, K, seed=M + N)
+    plan = g.gemm_kernel_plan(True, VARIANTS[v])
+    assert plan["tile_n"] == 224
+    Ad, Bd, SAd, SBd = (t.cuda() for t in (A, B, SFA, SFB))
+    D = torch.full((M, ldd), float("nan"), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    rc = g.gemm_mxfp8_variant(VARIANTS[v], Ad.data_ptr(), Bd.data_ptr(), SAd.data_ptr(),
+                              SBd.data_ptr(), D.data_ptr(), M, N, K, K, K, SFA.shape[1],
+                              SFB.shape[1], ldd, s)
+    assert rc == g.GEMM_OK and g.gemm_last_status(s) == g.GEMM_OK
+    D = D.cpu()
+    assert torch.isnan(D[:, N:].float()).all(), "padding columns written"
+    D_ref, _ = ref(A, SFA, B, SFB)
+    assert np.array_equal(gi.bf16_codes(D[:, :N]), oracle.f64_to_bf16_rne(D_ref))
