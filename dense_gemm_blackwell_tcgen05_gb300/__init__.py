@@ -21,8 +21,8 @@ __all__ = [
     "VARIANT_AUTO", "VARIANT_1CTA", "VARIANT_2CTA", "VARIANT_SYNC", "VARIANT_SMALLK",
     "VARIANT_DIRECT_STORE",
     "GemmError", "load", "library_path", "EXPORTED_SYMBOLS",
-    "gemm_bf16", "gemm_bf16_variant", "gemm_mxfp8", "gemm_mxfp8_variant",
-    "gemm_last_status", "gemm_last_status_word", "gemm_status_string", "gemm_set_watchdog_ms",
+    "gemm_bf16", "gemm_bf16_variant", "gemm_mxfp8", "gemm_mxfp8_variant", "gemm_mxfp8_tiled",
+    "matmul_mxfp8_tiled", "gemm_last_status", "gemm_last_status_word", "gemm_status_string", "gemm_set_watchdog_ms",
     "gemm_kernel_plan", "gemm_last_cuda_error", "gemm_debug_stall_next_launch",
     "gemm_mxfp8_quantize", "quantize_mxfp8", "gemm_bf16_streamk", "gemm_mxfp8_streamk",
     "gemm_streamk_workspace_bytes", "gemm_last_schedule", "streamk_workspace",
@@ -54,7 +54,7 @@ EXPORTED_SYMBOLS = (
     "gemm_last_cuda_error", "gemm_debug_stall_next_launch", "gemm_mxfp8_quantize",
     "gemm_bf16_streamk", "gemm_mxfp8_streamk", "gemm_streamk_workspace_bytes",
     "gemm_last_schedule", "gemm_bf16_streamk_noalloc", "gemm_set_streamk_mode",
-    "gemm_streamk_plan", "gemm_bf16_fused", "gemm_mxfp8_fused",
+    "gemm_streamk_plan", "gemm_bf16_fused", "gemm_mxfp8_fused", "gemm_mxfp8_tiled",
 )
 
 _lock = threading.Lock()
@@ -103,7 +103,10 @@ def load() -> ctypes.CDLL:
                                      _i64, _i64, _vp]
             L.gemm_mxfp8_variant.argtypes = [ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _i64, _i64,
                                              _i64, _i64, _i64, _i64, _i64, _i64, _vp]
-            for name in ("gemm_bf16", "gemm_bf16_variant", "gemm_mxfp8", "gemm_mxfp8_variant"):
+            L.gemm_mxfp8_tiled.argtypes = [ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64,
+                                           _i64, _i64, _i64, _vp]
+            for name in ("gemm_bf16", "gemm_bf16_variant", "gemm_mxfp8", "gemm_mxfp8_variant",
+                         "gemm_mxfp8_tiled"):
                 getattr(L, name).restype = ctypes.c_int
             L.gemm_bf16_streamk.argtypes = [ctypes.c_int, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
                                             _i64, _i64, _vp, _i64, _vp]
@@ -173,6 +176,11 @@ def gemm_mxfp8_variant(variant: int, A: int, B: int, SFA: int, SFB: int, D: int,
                        stream: int = 0) -> int:
     return load().gemm_mxfp8_variant(variant, A, B, SFA, SFB, D, M, N, K, lda, ldb, ldsfa, ldsfb,
                                      ldd, stream)
+
+
+def gemm_mxfp8_tiled(variant: int, A: int, B: int, SFA: int, SFB: int, D: int, M: int, N: int,
+                     K: int, lda: int, ldb: int, ldd: int, stream: int = 0) -> int:
+    return load().gemm_mxfp8_tiled(variant, A, B, SFA, SFB, D, M, N, K, lda, ldb, ldd, stream)
 
 
 def gemm_bf16_streamk(variant: int, A: int, B: int, D: int, M: int, N: int, K: int, lda: int,
@@ -338,9 +346,10 @@ def gemm_set_watchdog_ms(ms: int) -> int:
     return int(load().gemm_set_watchdog_ms(ms))
 
 
-def gemm_kernel_plan(mxfp8: bool, variant: int) -> dict:
+def gemm_kernel_plan(mxfp8, variant: int) -> dict:
+    """mxfp8: False/0 bf16, True/1 MXFP8, 2 MXFP8 with tiled scales."""
     vals = [ctypes.c_int32() for _ in range(7)]
-    rc = load().gemm_kernel_plan(int(bool(mxfp8)), variant, *[ctypes.byref(v) for v in vals])
+    rc = load().gemm_kernel_plan(int(mxfp8), variant, *[ctypes.byref(v) for v in vals])
     if rc != GEMM_OK:
         raise GemmError(rc, "gemm_kernel_plan")
     keys = ("stages", "smem_bytes", "tmem_cols", "threads", "cluster", "tile_m", "tile_n")
@@ -420,6 +429,36 @@ def matmul_mxfp8(A, SFA, B, SFB, out=None, variant: int = VARIANT_AUTO, stream=N
                                 _stream_handle(stream))
     if rc != GEMM_OK:
         raise GemmError(rc, "gemm_mxfp8")
+    return out
+
+
+def matmul_mxfp8_tiled(A, SFA, B, SFB, out=None, variant: int = VARIANT_AUTO, stream=None):
+    """Block-scaled D = A @ B.T with the scale matrices in the tiled layout of
+    gemm_mxfp8_tiled (1-D byte tensors, e.g. from gemm_inputs.tile_scales)."""
+    import torch
+    for t, n in ((A, "A"), (B, "B")):
+        _check_2d(t, n)
+        if t.element_size() != 1:
+            raise TypeError(f"{n} must hold one byte per element")
+    for t, n in ((SFA, "SFA"), (SFB, "SFB")):
+        if not t.is_cuda or t.element_size() != 1 or not t.is_contiguous():
+            raise TypeError(f"{n} must be a contiguous CUDA byte tensor")
+    M, K = A.shape
+    N = B.shape[0]
+    if B.shape[1] != K:
+        raise ValueError("A and B disagree on K")
+    kt = (K + 127) // 128
+    for t, n, R in ((SFA, "SFA", M), (SFB, "SFB", N)):
+        if t.numel() < (R + 127) // 128 * kt * 512:
+            raise ValueError(f"{n} is smaller than the tiled layout of {R} rows")
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=A.device)
+    _check_2d(out, "out")
+    rc = gemm_mxfp8_tiled(variant, A.data_ptr(), B.data_ptr(), SFA.data_ptr(), SFB.data_ptr(),
+                          out.data_ptr(), M, N, K, A.stride(0), B.stride(0), out.stride(0),
+                          _stream_handle(stream))
+    if rc != GEMM_OK:
+        raise GemmError(rc, "gemm_mxfp8_tiled")
     return out
 
 

@@ -383,10 +383,13 @@ int gemm_bf16(const void* A, const void* B, void* D, int64_t M, int64_t N, int64
   return gemm_bf16_variant(GEMM_VARIANT_AUTO, A, B, D, M, N, K, lda, ldb, ldd, stream);
 }
 
+// sf_tiled: SFA/SFB hold the scale matrices in the tiled layout of
+// gemm_mxfp8_tiled (ldsfa/ldsfb unused); else row-major with those pitches.
 static int mxfp8_impl(int variant, const void* A, const void* B, const void* SFA,
                       const void* SFB, void* D, int64_t M, int64_t N, int64_t K, int64_t lda,
                       int64_t ldb, int64_t ldsfa, int64_t ldsfb, int64_t ldd, void* ws,
-                      int64_t ws_bytes, const gemm_epilogue_t* epi, cudaStream_t stream) {
+                      int64_t ws_bytes, const gemm_epilogue_t* epi, cudaStream_t stream,
+                      bool sf_tiled = false) {
   const int base = variant & 0xFF;
   const bool direct = (variant & GEMM_VARIANT_DIRECT_STORE) != 0;
   if ((variant & ~(0xFF | GEMM_VARIANT_DIRECT_STORE)) != 0 || base > GEMM_VARIANT_2CTA)
@@ -394,7 +397,15 @@ static int mxfp8_impl(int variant, const void* A, const void* B, const void* SFA
   int rc = check_shape(A, B, D, M, N, K, lda, ldb, ldd, 1);
   if (rc == GEMM_OK && M != 0 && N != 0) rc = check_epilogue_alignment(epi, D);
   if (rc != GEMM_OK || M == 0 || N == 0) return rc;
-  if (K > 0) {
+  if (K > 0 && sf_tiled) {
+    // 512-byte chunks read by TMA: 16-byte aligned bases, and the 16-byte-row
+    // view (32 rows per chunk) addressable with 32-bit coordinates
+    const int64_t kt = (K + 127) / 128;
+    if (SFA == nullptr || SFB == nullptr || (M + 127) / 128 * kt * 32 > INT32_MAX ||
+        (N + 127) / 128 * kt * 32 > INT32_MAX)
+      return GEMM_ERR_INVALID_ARG;
+    if (!aligned16(SFA) || !aligned16(SFB)) return GEMM_ERR_ALIGNMENT;
+  } else if (K > 0) {
     const int64_t nblk = (K + 31) / 32;
     // Any pitch >= ceil(K/32) and any alignment: the launcher picks TMA or a
     // plain-load gather for the scale bytes.
@@ -434,6 +445,8 @@ static int mxfp8_impl(int variant, const void* A, const void* B, const void* SFA
   // slower), with the 32-column TMA-store epilogue where D allows it (same
   // four operand stages as the masked-store kernel; 0.5% faster at 8192^3).
   const bool tma_store = tma_store_ok(D, N, ldd, direct) && !(p.epi_mode & kEpiOutF32);
+  // Tiled scales: the CTA pair unless one CTA is asked for.
+  if (sf_tiled) return launch_mxf8t_ws(base == GEMM_VARIANT_1CTA ? 1 : 2, tma_store, p, ctx, stream);
   return launch_mxf8_ws(base == GEMM_VARIANT_2CTA ? 2 : 1, tma_store, p, ctx, stream);
 }
 
@@ -460,6 +473,13 @@ int gemm_mxfp8_streamk(int variant, const void* A, const void* B, const void* SF
   if (workspace == nullptr) return GEMM_ERR_INVALID_ARG;
   return mxfp8_impl(variant, A, B, SFA, SFB, D, M, N, K, lda, ldb, ldsfa, ldsfb, ldd, workspace,
                     workspace_bytes, nullptr, stream);
+}
+
+int gemm_mxfp8_tiled(int variant, const void* A, const void* B, const void* SFA, const void* SFB,
+                     void* D, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                     int64_t ldd, cudaStream_t stream) {
+  return mxfp8_impl(variant, A, B, SFA, SFB, D, M, N, K, lda, ldb, 0, 0, ldd, nullptr, 0, nullptr,
+                    stream, true);
 }
 
 int64_t gemm_streamk_workspace_bytes(int mxfp8, int variant) {
@@ -606,7 +626,9 @@ int gemm_kernel_plan(int mxfp8, int variant, int32_t* stages, int32_t* smem_byte
   const bool tma_store = (variant & GEMM_VARIANT_DIRECT_STORE) == 0;
   KernelPlan k;
   bool ok;
-  if (mxfp8)
+  if (mxfp8 == 2)
+    ok = base <= GEMM_VARIANT_2CTA && plan_mxf8t(base == GEMM_VARIANT_1CTA ? 1 : 2, tma_store, &k);
+  else if (mxfp8)
     ok = base <= GEMM_VARIANT_2CTA && plan_mxf8(base == GEMM_VARIANT_2CTA ? 2 : 1, tma_store, &k);
   else
     ok = plan_bf16(base == GEMM_VARIANT_AUTO ? 2 : base, tma_store, &k);

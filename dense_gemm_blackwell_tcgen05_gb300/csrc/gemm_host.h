@@ -134,6 +134,9 @@ int launch_bf16_sync(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream
 int bf16_streamk_split_tiles(int cg, const Problem& p, const LaunchCtx& ctx, uint32_t* sk_tiles);
 int launch_mxf8_ws(int cg, bool tma_store, const Problem& p, const LaunchCtx& ctx,
                    cudaStream_t stream);
+// MXFP8 with scale matrices in the tiled layout (gemm_mxfp8_tiled).
+int launch_mxf8t_ws(int cg, bool tma_store, const Problem& p, const LaunchCtx& ctx,
+                    cudaStream_t stream);
 int launch_zero_fill(const Problem& p, cudaStream_t stream);
 // CUDA-core kernel for 1 <= K <= smallk_max_k() (plain bf16 store only).
 int launch_bf16_smallk(const Problem& p, int num_sms, cudaStream_t stream);
@@ -150,5 +153,6 @@ struct KernelPlan {
 };
 bool plan_bf16(int cg, bool tma_store, KernelPlan* out);
 bool plan_mxf8(int cg, bool tma_store, KernelPlan* out);
+bool plan_mxf8t(int cg, bool tma_store, KernelPlan* out);
 
 }  // namespace gb300

@@ -26,7 +26,12 @@
 
 namespace gb300 {
 
-enum class Kind { BF16, MXF8 };
+// BF16: bf16 operands.  MXF8: block-scaled E4M3 operands with row-major
+// scale matrices, re-tiled on chip by a scale-factor warp.  MXF8T: the same
+// with the scale matrices already in the tensor core's chunk layout in
+// global memory ("tiled": 512-byte chunks of 128 rows x 4 scale blocks),
+// loaded by TMA into each operand stage like A and B.
+enum class Kind { BF16, MXF8, MXF8T };
 
 struct GemmArgs {
   uint32_t M, N, K;
@@ -165,10 +170,14 @@ __host__ __device__ constexpr uint32_t align_up_u32(uint32_t x, uint32_t a) {
 //                  columns (2 x 224 + 12 <= 512)
 //   MXFP8, pair  : 256 x 224 cluster tiles, two 224-column accumulators +
 //                  scale columns (2 x 224 + 12 <= 512)
+//   MXFP8 with tiled scales, 1 CTA / pair : 128 x 256 / 256 x 256 tiles, one
+//                  256-column accumulator + scale columns (256 + 12 <= 512)
 template <int CG, Kind KIND, bool TMA_STORE, bool EPI2 = false>
 struct GemmCfg {
   static_assert(CG == 1 || CG == 2, "cta_group is 1 or 2");
-  static constexpr bool MX = KIND == Kind::MXF8;
+  static constexpr bool MX = KIND != Kind::BF16;          // block-scaled E4M3
+  static constexpr bool SF_TILED = KIND == Kind::MXF8T;   // scales by TMA, in the stages
+  static constexpr bool SF_WARP = MX && !SF_TILED;        // scales re-tiled on chip
 
   // w0 TMA producer, w1 MMA issuer / TMEM owner, w2..5 epilogue and, for
   // MXFP8, w6: the scale-factor warp.  It re-tiles each stage's scale bytes as
@@ -183,7 +192,9 @@ struct GemmCfg {
   // columns fit in 512 TMEM columns (2 x 224 + 12): the epilogue of one tile
   // then overlaps the next tile's MMAs (measured +4% at 8192^3, +16% at
   // 8192x8192x4096 against one 256-column accumulator).
-  static constexpr uint32_t UMMA_N = MX ? 224 : 256;
+  // Tiled scales need no on-chip scale rings, and tile at N = 256: their
+  // 128-row chunks then line up with whole tiles.
+  static constexpr uint32_t UMMA_N = SF_WARP ? 224 : 256;
   static constexpr uint32_t B_ROWS = UMMA_N / CG;  // B rows staged by one CTA
   static constexpr uint32_t ELEM = MX ? 1 : 2;
   static constexpr uint32_t BK = 128 / ELEM;  // K elements per stage: one 128-byte row
@@ -191,9 +202,15 @@ struct GemmCfg {
   static constexpr uint32_t K_STEPS = BK / UMMA_K;
   static constexpr uint32_t A_BYTES = BLOCK_M * 128;
   static constexpr uint32_t B_BYTES = B_ROWS * 128;
-  static constexpr uint32_t STAGE_BYTES = align_up_u32(A_BYTES + B_BYTES, 1024);
+  // Tiled scales: the K-tile's 512-byte chunk of this CTA's 128 A rows, then
+  // one chunk per 128 B rows of the tile (every CTA holds the scales of all
+  // the tile's B rows), behind A and B in the same stage.
+  static constexpr uint32_t SFB_TILE_CHUNKS = SF_TILED ? UMMA_N / 128 : 0;
+  static constexpr uint32_t SF_STAGE_BYTES = SF_TILED ? 512 * (1 + SFB_TILE_CHUNKS) : 0;
   static constexpr uint32_t OFF_B = A_BYTES;
-  static constexpr uint32_t AB_TX = A_BYTES + B_BYTES;            // per CTA
+  static constexpr uint32_t OFF_SF = A_BYTES + B_BYTES;
+  static constexpr uint32_t STAGE_BYTES = align_up_u32(A_BYTES + B_BYTES + SF_STAGE_BYTES, 1024);
+  static constexpr uint32_t AB_TX = A_BYTES + B_BYTES + SF_STAGE_BYTES;   // per CTA
   static constexpr uint32_t FULL_ARRIVALS = 1;                    // the producer's expect_tx
 
   // MXFP8 scale factors travel in two rings of their own, one slot per group
@@ -214,21 +231,23 @@ struct GemmCfg {
   static constexpr uint32_t T_SLOTS = CG == 2 ? 4 : 2;
   static constexpr uint32_t SFB_ROWS = MX ? UMMA_N : 0;
   static constexpr uint32_t SFB_CHUNKS = (SFB_ROWS + 127) / 128;
-  static constexpr uint32_t SFA_RAW = MX ? BLOCK_M * 16 : 0;
-  static constexpr uint32_t SFB_RAW = SFB_ROWS * 16;
-  static constexpr uint32_t SFA_T = MX ? 512 : 0;                 // one chunk per K-tile
-  static constexpr uint32_t SFB_T = SFB_CHUNKS * 512;
+  static constexpr uint32_t SFA_RAW = SF_WARP ? BLOCK_M * 16 : 0;
+  static constexpr uint32_t SFB_RAW = SF_WARP ? SFB_ROWS * 16 : 0;
+  static constexpr uint32_t SFA_T = SF_WARP ? 512 : 0;            // one chunk per K-tile
+  static constexpr uint32_t SFB_T = SF_WARP ? SFB_CHUNKS * 512 : 0;
   static constexpr uint32_t T_PER_KT = SFA_T + SFB_T;
   static constexpr uint32_t OFF_SFA_RAW = 0;                      // within a raw slot
   static constexpr uint32_t OFF_SFB_RAW = SFA_RAW;
-  static constexpr uint32_t RAW_SLOT_BYTES = MX ? align_up_u32(SFA_RAW + SFB_RAW, 1024) : 0;
-  static constexpr uint32_t T_SLOT_BYTES = MX ? align_up_u32(SF_GROUP * T_PER_KT, 1024) : 0;
+  static constexpr uint32_t RAW_SLOT_BYTES = SF_WARP ? align_up_u32(SFA_RAW + SFB_RAW, 1024) : 0;
+  static constexpr uint32_t T_SLOT_BYTES = SF_WARP ? align_up_u32(SF_GROUP * T_PER_KT, 1024) : 0;
   static constexpr uint32_t SF_BYTES = RAW_SLOTS * RAW_SLOT_BYTES + T_SLOTS * T_SLOT_BYTES;
   static constexpr uint32_t SF_TX = SFA_RAW + SFB_RAW;            // per CTA and raw slot
 
   // TMEM: ACC_STAGES accumulators of UMMA_N fp32 columns, then the scale
   // factors (MXFP8: 4 columns for A, 4 per 128 B rows).  512 = whole TMEM.
-  static constexpr uint32_t ACC_STAGES = 2;
+  // Two 256-column accumulators leave no columns for scales, so the tiled-
+  // scale kernels (N = 256) keep one.
+  static constexpr uint32_t ACC_STAGES = SF_TILED ? 1 : 2;
   // Unroll factor of the MMA issuer's K-tile loop.
   static constexpr int MMA_UNROLL = CG == 2 ? (MX ? 2 : 4) : 1;
   // Epilogue warpgroups (the ladder's multi-consumer level): with two, both
@@ -240,7 +259,7 @@ struct GemmCfg {
   // EPI2 asks for the second group in an MXFP8 kernel as well (used for
   // launches that split tiles along K, whose epilogue also sums partial tiles).
   static constexpr uint32_t EPI_WG = (!TMA_STORE && ACC_STAGES == 2 && (!MX || EPI2)) ? 2 : 1;
-  static constexpr uint32_t kEpiWg1Warp = MX ? 7 : 6;   // first warp of group 1
+  static constexpr uint32_t kEpiWg1Warp = SF_WARP ? 7 : 6;   // first warp of group 1
   static constexpr uint32_t kThreads = 32 * (kEpiWg1Warp + 4 * (EPI_WG - 1));
   static constexpr uint32_t SF_TMEM_COL = ACC_STAGES * UMMA_N;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -672,16 +691,35 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
           }
           const uint32_t sb = stage0 + s * C::STAGE_BYTES;
           const int32_t kx = static_cast<int32_t>(kt * C::BK);
+          // Tiled scales: chunk (row block, K-tile) sits at chunk row
+          // (row block * KT + kt) * 32 of the 16-byte-row view; this CTA's A
+          // row block, then the tile's B row blocks.
+          const int32_t sfa_y = static_cast<int32_t>(((static_cast<uint32_t>(a_row) / 128u) * KT + kt) * 32u);
+          const uint32_t sfb_blk = (nb * C::UMMA_N) / 128u;
           if constexpr (CG == 1) {
             mbar_arrive_expect_tx(full_bar(s), C::AB_TX);
             tma_load_2d(sb, &tmA, full_bar(s), kx, a_row, pol);
             tma_load_2d(sb + C::OFF_B, &tmB, full_bar(s), kx, b_row, pol);
+            if constexpr (C::SF_TILED) {
+              tma_load_2d(sb + C::OFF_SF, &tmSFA, full_bar(s), 0, sfa_y, pol);
+#pragma unroll
+              for (uint32_t h = 0; h < C::SFB_TILE_CHUNKS; ++h)
+                tma_load_2d(sb + C::OFF_SF + 512 * (1 + h), &tmSFB, full_bar(s), 0,
+                            static_cast<int32_t>(((sfb_blk + h) * KT + kt) * 32u), pol);
+            }
           } else {
             // both CTAs' operand bytes land on the leader's ready barrier
             const uint32_t leader_full = mapa_shared(full_bar(s), 0);
             if (leader) mbar_arrive_expect_tx(full_bar(s), CG * C::AB_TX);
             tma_load_2d_pair(sb, &tmA, leader_full, kx, a_row, pol);
             tma_load_2d_pair(sb + C::OFF_B, &tmB, leader_full, kx, b_row, pol);
+            if constexpr (C::SF_TILED) {
+              tma_load_2d_pair(sb + C::OFF_SF, &tmSFA, leader_full, 0, sfa_y, pol);
+#pragma unroll
+              for (uint32_t h = 0; h < C::SFB_TILE_CHUNKS; ++h)
+                tma_load_2d_pair(sb + C::OFF_SF + 512 * (1 + h), &tmSFB, leader_full, 0,
+                                 static_cast<int32_t>(((sfb_blk + h) * KT + kt) * 32u), pol);
+            }
           }
         }
       }
@@ -717,7 +755,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
           const uint32_t s = it % C::STAGES;
           const uint32_t round = it / C::STAGES;
           const uint32_t g = gi % C::T_SLOTS;
-          if constexpr (C::MX) {
+          if constexpr (C::SF_WARP) {
             // first K-tile of a scale-factor group: every CTA filled the slot
             if (kt % C::SF_GROUP == 0 &&
                 !wait_bounded(t_ready_bar(g), (gi / C::T_SLOTS) & 1u, wd, kSiteMmaFull)) {
@@ -736,11 +774,14 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
           if constexpr (C::MX) {
             const uint32_t sfa_t = tmem_base + C::SF_TMEM_COL;
             const uint32_t sfb_t = sfa_t + 4;
-            const uint32_t tsrc = t0 + g * C::T_SLOT_BYTES + (kt % C::SF_GROUP) * C::T_PER_KT;
+            // the K-tile's scale chunks: in the stage itself (tiled scales) or
+            // in the re-tiled slot of its group
+            const uint32_t tsrc = C::SF_TILED ? sb + C::OFF_SF
+                                              : t0 + g * C::T_SLOT_BYTES + (kt % C::SF_GROUP) * C::T_PER_KT;
             tmem_cp_32x128b_warpx4<CG>(sfa_t, smem_desc_rows16(tsrc));
 #pragma unroll
             for (uint32_t h = 0; h < C::SFB_CHUNKS; ++h)
-              tmem_cp_32x128b_warpx4<CG>(sfb_t + 4 * h, smem_desc_rows16(tsrc + C::SFA_T + 512 * h));
+              tmem_cp_32x128b_warpx4<CG>(sfb_t + 4 * h, smem_desc_rows16(tsrc + 512 * (1 + h)));
 #pragma unroll
             for (uint32_t k = 0; k < C::K_STEPS; ++k)
               mma_mxf8<CG>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc_mxf8(C::UMMA_M, C::UMMA_N, k, k),
@@ -752,7 +793,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
               mma_bf16<CG>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kt != w.k_begin || k != 0u));
           }
           commit_to<CG>(empty_bar(s));   // frees the stage once these MMAs finish
-          if (C::MX && (kt % C::SF_GROUP == C::SF_GROUP - 1 || kt + 1 == w.k_end)) {
+          if (C::SF_WARP && (kt % C::SF_GROUP == C::SF_GROUP - 1 || kt + 1 == w.k_end)) {
             commit_to<CG>(t_empty_bar(g));   // and the re-tiled scale slot
             ++gi;
           }
@@ -771,7 +812,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
         drain_wait(drain_bar, 0, wd, kSiteMmaDrain);
       }
     }
-  } else if (C::MX && warp == C::kSfWarp) {
+  } else if (C::SF_WARP && warp == C::kSfWarp) {
     // ==================== scale-factor warp (every CTA) ===========================
     // Load this CTA's scale bytes group by group (RAW_SLOTS groups ahead),
     // re-tile each landed group into the tcgen05.cp layout and report it to

@@ -40,4 +40,27 @@ bool plan_mxf8(int cg, bool tma_store, KernelPlan* out) {
   return false;
 }
 
+int launch_mxf8t_ws(int cg, bool tma_store, const Problem& p, const LaunchCtx& ctx,
+                    cudaStream_t stream) {
+  if (cg == 1)
+    return tma_store ? launch_ws_impl<1, Kind::MXF8T, true>(p, ctx, stream)
+                     : launch_ws_impl<1, Kind::MXF8T, false>(p, ctx, stream);
+  if (cg == 2)
+    return tma_store ? launch_ws_impl<2, Kind::MXF8T, true>(p, ctx, stream)
+                     : launch_ws_impl<2, Kind::MXF8T, false>(p, ctx, stream);
+  return GEMM_ERR_INVALID_ARG;
+}
+
+bool plan_mxf8t(int cg, bool tma_store, KernelPlan* out) {
+  if (cg == 1) {
+    tma_store ? fill_plan<1, Kind::MXF8T, true>(out) : fill_plan<1, Kind::MXF8T, false>(out);
+    return true;
+  }
+  if (cg == 2) {
+    tma_store ? fill_plan<2, Kind::MXF8T, true>(out) : fill_plan<2, Kind::MXF8T, false>(out);
+    return true;
+  }
+  return false;
+}
+
 }  // namespace gb300

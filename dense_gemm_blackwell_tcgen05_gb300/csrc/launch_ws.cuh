@@ -76,7 +76,7 @@ int ws_streamk_split_tiles(const Problem& p, const LaunchCtx& ctx, uint32_t* sk_
   const uint64_t tiles = static_cast<uint64_t>((p.M + C::UMMA_M - 1) / C::UMMA_M) *
                          ((p.N + C::UMMA_N - 1) / C::UMMA_N);
   const uint32_t kt = (p.K + C::BK - 1) / C::BK;
-  *sk_tiles = plan_streamk(tiles, resident, kt, C::MX ? C::SF_GROUP : 1u, streamk_mode()).sk_tiles;
+  *sk_tiles = plan_streamk(tiles, resident, kt, C::SF_WARP ? C::SF_GROUP : 1u, streamk_mode()).sk_tiles;
   return GEMM_OK;
 }
 
@@ -105,9 +105,18 @@ int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) 
   // pitches that are multiples of 16 bytes (TMA's rules); otherwise the
   // scale-factor warp gathers them with plain loads.
   const bool sf_gather =
-      C::MX && (((reinterpret_cast<uintptr_t>(p.SFA) | reinterpret_cast<uintptr_t>(p.SFB)) & 15u) != 0 ||
-                p.ldsfa % 16 != 0 || p.ldsfb % 16 != 0);
-  if (C::MX && !sf_gather) {
+      C::SF_WARP && (((reinterpret_cast<uintptr_t>(p.SFA) | reinterpret_cast<uintptr_t>(p.SFB)) & 15u) != 0 ||
+                     p.ldsfa % 16 != 0 || p.ldsfb % 16 != 0);
+  if constexpr (C::SF_TILED) {
+    // the tiled scale matrices as rows of 16 bytes: 32 rows per 512-byte
+    // chunk, chunks ordered (row block, K-tile); one 32-row box per chunk
+    const uint64_t kt = (p.K + C::BK - 1) / C::BK;
+    if (!encode_map_2d(&maps.SFA, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.SFA, 16,
+                       (p.M + 127) / 128 * kt * 32, 16, 16, 32, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_map_2d(&maps.SFB, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.SFB, 16,
+                       (p.N + 127) / 128 * kt * 32, 16, 16, 32, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return GEMM_ERR_LAUNCH;
+  } else if (C::MX && !sf_gather) {
     const uint64_t nblk = (p.K + 31) / 32;
     if (!encode_map_2d(&maps.SFA, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.SFA, nblk, p.M, p.ldsfa, 16,
                        C::BLOCK_M, CU_TENSOR_MAP_SWIZZLE_NONE) ||
@@ -153,7 +162,7 @@ int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) 
   // equal contiguous ranges.
   a.dp_tiles = static_cast<uint32_t>(tiles);
   a.sk_tiles = 0;
-  a.sk_unit = C::MX ? C::SF_GROUP : 1u;
+  a.sk_unit = C::SF_WARP ? C::SF_GROUP : 1u;
   uint64_t clusters = tiles < resident ? tiles : resident;
   if (p.workspace != nullptr) {
     const uint64_t need = resident * CG * streamk_bytes_per_cta(C::UMMA_N);

@@ -182,6 +182,21 @@ def mxfp8_operands(M: int, N: int, K: int, seed: int, dist: str = "normal",
     return qa, sfa, qb, sfb
 
 
+def tile_scales(sf: torch.Tensor, rows: int, K: int) -> torch.Tensor:
+    """Row-major UE8M0 scales [rows, >= ceil(K/32)] rearranged into the tiled
+    layout gemm_mxfp8_tiled takes (a pure permutation plus zero padding): 512-byte
+    chunks of 128 rows x 4 blocks, chunk (row block rb, block group g) at
+    512 * (rb * ceil(nblk/4) + g); inside it row 128 rb + 32 c + l, block
+    4 g + j at byte 16 l + 4 c + j.  Returns a flat uint8 tensor on sf's device."""
+    nb = (K + 31) // 32
+    R, C = (rows + 127) // 128 * 128, (nb + 3) // 4 * 4
+    p = torch.zeros(R, C, dtype=torch.uint8, device=sf.device)
+    p[:rows, :nb] = sf[:rows, :nb]
+    # [rb, c, l, g, j] -> [rb, g, l, c, j]
+    t = p.view(R // 128, 4, 32, C // 4, 4).permute(0, 3, 2, 1, 4)
+    return t.contiguous().view(-1)
+
+
 def workload_operands(name: str):
     """Operands of a named workload: (A, B) for bf16, (A, SFA, B, SFB) for MXFP8,
     (X,) float32 for the quantiser (the MXFP8 workload's A operand)."""

@@ -129,6 +129,31 @@ int gemm_mxfp8_variant(int variant, const void* A, const void* B, const void* SF
                        cudaStream_t stream);
 
 /*
+ * Block-scaled MXFP8 GEMM with the scale matrices already in the tensor
+ * core's chunk layout (b200-tmem-lifecycle-planner, "A1 -- Case 2": scale
+ * factors are staged SMEM -> TMEM by tcgen05.cp in their own layout; here
+ * they arrive in that layout, so TMA moves them into each pipeline stage
+ * with the operands and no thread touches them).  Same D and A/B operands,
+ * values and errors as gemm_mxfp8; the scales of an R-row operand
+ * (R = M for SFA, N for SFB) with nblk = ceil(K/32) blocks per row are
+ *     ceil(R/128) x ceil(nblk/4) chunks of 512 bytes, chunk (rb, g) at byte
+ *     512 * (rb * ceil(nblk/4) + g); inside it the scale byte of row
+ *     r = 128 rb + 32 c + l and block b = 4 g + j (0 <= l < 32, c, j < 4)
+ *     sits at byte 16 l + 4 c + j
+ * (the layout cuBLASLt's block-scaled GEMMs take).  SFA, SFB: 16-byte
+ * aligned device buffers of that size.  Bytes of rows >= R are never
+ * applied to D; bytes of blocks >= nblk multiply zero-filled operands and
+ * must not hold 255 (NaN): zero them.  Kernel: the CTA pair on 256x256 tiles
+ * (GEMM_VARIANT_AUTO / _2CTA) or one CTA on 128x256 tiles (_1CTA), one
+ * 256-column accumulator; optionally | GEMM_VARIANT_DIRECT_STORE.  Errors as
+ * gemm_mxfp8, plus GEMM_ERR_ALIGNMENT for SFA/SFB not 16-byte aligned and
+ * GEMM_ERR_INVALID_ARG when ceil(R/128) * ceil(K/128) * 32 exceeds 2^31 - 1.
+ */
+int gemm_mxfp8_tiled(int variant, const void* A, const void* B, const void* SFA, const void* SFB,
+                     void* D, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                     int64_t ldd, cudaStream_t stream);
+
+/*
  * Fused epilogue, applied to the fp32 accumulator on its way from TMEM to
  * memory (the readback step where "cast/epilogue/store" happen:
  * b200-tmem-lifecycle-planner, "A1 -- Case 1: dense MMA accumulator";
@@ -322,7 +347,9 @@ int64_t gemm_set_watchdog_ms(int64_t ms);
 
 /* Compile-time plan of a kernel variant, for reports: pipeline stages,
  * dynamic shared memory bytes, TMEM columns, threads per CTA, CTAs per
- * cluster, tile M and N.  Returns GEMM_OK or GEMM_ERR_INVALID_ARG. */
+ * cluster, tile M and N.  mxfp8: 0 = bf16, 1 = MXFP8 (row-major scales),
+ * 2 = MXFP8 with tiled scales (gemm_mxfp8_tiled).  Returns GEMM_OK or
+ * GEMM_ERR_INVALID_ARG. */
 int gemm_kernel_plan(int mxfp8, int variant, int32_t* stages, int32_t* smem_bytes,
                      int32_t* tmem_cols, int32_t* threads, int32_t* cluster, int32_t* tile_m,
                      int32_t* tile_n);

@@ -4,6 +4,23 @@ import torch
 import bench
 
 
+def test_tile_scales_layout():
+    # the tiled layout gemm_mxfp8_tiled takes, written out element by element
+    import gemm_inputs as gi
+    rows, K = 300, 32 * 9          # ragged rows and a partial block group
+    nb = (K + 31) // 32
+    g = torch.Generator().manual_seed(1)
+    sf = torch.randint(0, 255, (rows, 16), dtype=torch.uint8, generator=g)
+    out = gi.tile_scales(sf, rows, K)
+    G = (nb + 3) // 4
+    assert out.numel() == (rows + 127) // 128 * G * 512
+    for r in range(384):
+        for b in range(4 * G):
+            off = 512 * ((r // 128) * G + b // 4) + 16 * (r % 32) + 4 * ((r % 128) // 32) + b % 4
+            want = int(sf[r, b]) if r < rows and b < nb else 0
+            assert int(out[off]) == want, (r, b)
+
+
 def test_blocked_scales_layout():
     # cuBLASLt's block-scaled layout, written out element by element: a 128-row x
     # 4-block tile is 512 bytes, tiles ordered row-block major; inside a tile, row

@@ -323,3 +323,93 @@ def test_tma_store_epilogue_guard_band(v, M, N, ldd):
     assert torch.isnan(D[:, N:].float()).all(), "padding columns written"
     D_ref, _ = ref(A, SFA, B, SFB)
     assert np.array_equal(gi.bf16_codes(D[:, :N]), oracle.f64_to_bf16_rne(D_ref))
+
+
+# ------------------------------------ tiled scale layout (gemm_mxfp8_tiled)
+
+TILED_VARIANTS = {
+    "auto": g.VARIANT_AUTO,
+    "2cta": g.VARIANT_2CTA,
+    "2cta_direct": g.VARIANT_2CTA | g.VARIANT_DIRECT_STORE,
+    "1cta": g.VARIANT_1CTA,
+}
+
+
+def run_tiled(A, SFA, B, SFB, variant, K=None, ldd=None):
+    """The same operands as run(), the row-major scales rearranged into the
+    tiled layout on the host (a permutation with zero padding)."""
+    M, lda = A.shape
+    N, ldb = B.shape
+    K = lda if K is None else K
+    ldd = N if ldd is None else ldd
+    Ad, Bd = A.cuda(), B.cuda()
+    SAt, SBt = gi.tile_scales(SFA, M, K).cuda(), gi.tile_scales(SFB, N, K).cuda()
+    D = torch.full((M, ldd), float("nan"), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    rc = g.gemm_mxfp8_tiled(variant, Ad.data_ptr(), Bd.data_ptr(), SAt.data_ptr(), SBt.data_ptr(),
+                            D.data_ptr(), M, N, K, lda, ldb, ldd, s)
+    assert rc == g.GEMM_OK, g.gemm_status_string(rc)
+    st = g.gemm_last_status(s)
+    assert st == g.GEMM_OK, g.gemm_status_string(st)
+    D = D.cpu()
+    if ldd > N:
+        assert torch.isnan(D[:, N:].float()).all(), "padding columns written"
+    return D[:, :N]
+
+
+def test_tiled_plan():
+    for v, cg, tm in (("auto", 2, 256), ("2cta", 2, 256), ("1cta", 1, 128)):
+        p = g.gemm_kernel_plan(2, TILED_VARIANTS[v])
+        assert (p["cluster"], p["tile_m"], p["tile_n"], p["tmem_cols"]) == (cg, tm, 256, 512)
+
+
+@pytest.mark.parametrize("v", list(TILED_VARIANTS))
+@pytest.mark.parametrize("shape", [(128, 256, 128), (256, 256, 128), (300, 520, 256),
+                                   (129, 300, 160), (1000, 900, 1184), (513, 1031, 1056)])
+def test_tiled_exact_integers(v, shape):
+    """Bitwise against the oracle with scales varying per (row, 32-k block):
+    a scale chunk loaded for the wrong row block, K-tile or CTA shows up as a
+    wrong bit."""
+    M, N, K = shape
+    lda = (K + 15) // 16 * 16
+    A, SFA, B, SFB = int_operands(M, N, K, seed=M + 5 * N + K, lda=lda)
+    D = run_tiled(A, SFA, B, SFB, TILED_VARIANTS[v], K=K)
+    D_ref, _ = ref(A, SFA, B, SFB, K)
+    assert_matches_oracle(D, D_ref, f"tiled {shape}/{v}")
+
+
+@pytest.mark.parametrize("v", ["auto", "1cta"])
+@pytest.mark.parametrize("shape", [(300, 520, 384), (700, 1100, 2048)])
+def test_tiled_quantised_normal(v, shape):
+    M, N, K = shape
+    A, SFA, B, SFB = gi.mxfp8_operands(M, N, K, seed=M + N + 1)
+    D = run_tiled(A, SFA, B, SFB, TILED_VARIANTS[v], ldd=N + 8)
+    D_ref, S = ref(A, SFA, B, SFB)
+    P.check_within_bound(P.bf16_to_f64(D), D_ref, S, f"tiled mx {shape}/{v}")
+
+
+@pytest.mark.parametrize("v", ["auto", "1cta"])
+def test_tiled_nan_scale_and_code(v):
+    M, N, K = 300, 450, 192
+    A, SFA, B, SFB = int_operands(M, N, K, seed=41)
+    A[7, 64:96] = P.e4m3_from_ints(np.full(32, 3))
+    SFA[7, 2] = 0xFF
+    B[250, 100] = 0x7F
+    D = run_tiled(A, SFA, B, SFB, TILED_VARIANTS[v])
+    D_ref, _ = ref(A, SFA, B, SFB)
+    assert np.isnan(D_ref[7]).all() and np.isnan(D_ref[:, 250]).all()
+    assert_matches_oracle(D, D_ref, f"tiled nan/{v}")
+
+
+def test_tiled_validation():
+    A = torch.zeros(256, 256, dtype=torch.uint8, device="cuda")
+    D = torch.empty(256, 256, dtype=torch.bfloat16, device="cuda")
+    sf = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    f = lambda sfa, v=g.VARIANT_AUTO: g.gemm_mxfp8_tiled(v, A.data_ptr(), A.data_ptr(), sfa,
+                                                         sf.data_ptr(), D.data_ptr(), 256, 256,
+                                                         256, 256, 256, 256, 0)
+    assert f(sf.data_ptr() + 8) == g.GEMM_ERR_ALIGNMENT
+    assert f(0) == g.GEMM_ERR_INVALID_ARG
+    assert f(sf.data_ptr(), g.VARIANT_SYNC) == g.GEMM_ERR_INVALID_ARG
+    assert f(sf.data_ptr()) == g.GEMM_OK
+    assert g.gemm_last_status(0) == g.GEMM_OK
