@@ -228,7 +228,7 @@ struct GemmCfg {
   // core multiplies by all of them) and of its own 128 A rows.
   static constexpr uint32_t SF_GROUP = 4;
   static constexpr uint32_t RAW_SLOTS = 2;
-  static constexpr uint32_t T_SLOTS = CG == 2 ? 4 : 2;
+  static constexpr uint32_t T_SLOTS = CG == 2 || SF_TILED ? 4 : 2;
   static constexpr uint32_t SFB_ROWS = MX ? UMMA_N : 0;
   static constexpr uint32_t SFB_CHUNKS = (SFB_ROWS + 127) / 128;
   static constexpr uint32_t SFA_RAW = SF_WARP ? BLOCK_M * 16 : 0;
@@ -249,7 +249,8 @@ struct GemmCfg {
   // scale kernels (N = 256) keep one.
   static constexpr uint32_t ACC_STAGES = SF_TILED ? 1 : 2;
   // Unroll factor of the MMA issuer's K-tile loop.
-  static constexpr int MMA_UNROLL = CG == 2 ? (MX ? 2 : 4) : 1;
+  // (the tiled-scale pair: 4, measured +4% over 2 at 8192^3)
+  static constexpr int MMA_UNROLL = CG == 2 ? (SF_WARP ? 2 : 4) : 1;
   // Epilogue warpgroups (the ladder's multi-consumer level): with two, both
   // groups drain every tile, group g taking the 32-column chunks c with
   // c % 2 == g, so a tile's epilogue takes half as long.  Used where the
@@ -258,27 +259,39 @@ struct GemmCfg {
   // staging would cost a stage: 6 -> 5, measured 3% slower.)
   // EPI2 asks for the second group in an MXFP8 kernel as well (used for
   // launches that split tiles along K, whose epilogue also sums partial tiles).
-  static constexpr uint32_t EPI_WG = (!TMA_STORE && ACC_STAGES == 2 && (!MX || EPI2)) ? 2 : 1;
+  // The tiled-scale kernels (one accumulator) use two groups as well: their
+  // epilogue hands the accumulator back as soon as it sits in registers, so a
+  // faster drain shortens the MMA issuer's wait directly.
+  static constexpr uint32_t EPI_WG =
+      SF_TILED || (!TMA_STORE && ACC_STAGES == 2 && (!MX || EPI2)) ? 2 : 1;
   static constexpr uint32_t kEpiWg1Warp = SF_WARP ? 7 : 6;   // first warp of group 1
-  static constexpr uint32_t kThreads = 32 * (kEpiWg1Warp + 4 * (EPI_WG - 1));
+  // Tiled scales: one more warp after the epilogue groups issues the scale
+  // copies (tcgen05.cp) into two alternating TMEM scale sets, so the MMA
+  // thread issues only MMAs and commits.
+  static constexpr uint32_t kCpWarp = kEpiWg1Warp + 4 * (EPI_WG - 1);
+  static constexpr uint32_t kThreads = 32 * (kCpWarp + (SF_TILED ? 1 : 0));
   static constexpr uint32_t SF_TMEM_COL = ACC_STAGES * UMMA_N;
+  static constexpr uint32_t SF_SET_COLS = MX ? 4 + 4 * SFB_CHUNKS : 0;   // one K-tile's scales
   static constexpr uint32_t TMEM_COLS = 512;
-  static_assert(SF_TMEM_COL + (MX ? 4 + 4 * SFB_CHUNKS : 0) <= TMEM_COLS, "TMEM column budget");
 
   // Epilogue staging for TMA stores: per epilogue warp, two buffers of 32
   // rows x TS_COLS bf16 columns -- 64 columns (128-byte rows, 128-byte
   // swizzle) where the tile width allows, else 32 (64-byte rows, 64-byte
   // swizzle: the MXFP8 tiles are 224 = 7 x 32 columns wide).
-  static constexpr uint32_t TS_COLS = UMMA_N % 64 == 0 ? 64 : 32;
+  // (The tiled-scale kernels use 32-column boxes too: half the staging, so
+  // the pair keeps six operand stages with eight epilogue warps.)
+  static constexpr uint32_t TS_COLS = UMMA_N % 64 == 0 && !SF_TILED ? 64 : 32;
   static_assert(!TMA_STORE || UMMA_N % TS_COLS == 0, "TMA-store chunks tile the accumulator");
   // The masked-store epilogue instead stages one 32x32 chunk per warp (2 KB)
   // and writes it back row by row, lanes across columns, so its global stores
   // are coalesced whatever the pitch.
   static constexpr uint32_t EPI_BUF_BYTES = 32 * TS_COLS * 2;
-  static constexpr uint32_t EPI_BUFS = 2;
+  // Staging buffers per epilogue warp: two (the next chunk's conversion
+  // overlaps the previous chunk's store), one with two epilogue groups.
+  static constexpr uint32_t EPI_BUFS = EPI_WG == 2 ? 1 : 2;
   static constexpr uint32_t CHUNK_BYTES = 32 * 64;
   static constexpr uint32_t EPI_BYTES =
-      TMA_STORE ? 4 * EPI_BUFS * EPI_BUF_BYTES : 4 * EPI_WG * CHUNK_BYTES;
+      TMA_STORE ? 4 * EPI_WG * EPI_BUFS * EPI_BUF_BYTES : 4 * EPI_WG * CHUNK_BYTES;
 
   static constexpr uint32_t SMEM_LIMIT = 232448;  // 227 KB opt-in per CTA
   static constexpr uint32_t BAR_BYTES = 512;
@@ -290,6 +303,16 @@ struct GemmCfg {
   static constexpr uint32_t SMEM_BYTES =
       ALIGN_SLACK + STAGES * STAGE_BYTES + SF_BYTES + EPI_BYTES + BAR_BYTES;
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
+  // Tiled scales: TMEM scale sets the copy thread rotates through (4 measured
+  // 16% faster than 2: the copies of the next K-tiles no longer wait for the
+  // MMAs just issued).  At most STAGES: the copy thread finds a set free by
+  // waiting for the stage barrier phase of the K-tile SF_SETS back, and that
+  // barrier must not have moved on to its next phase (K-tile SF_SETS back +
+  // STAGES, whose copies this thread has not issued yet).
+  static constexpr uint32_t SF_SETS = SF_TILED ? (STAGES < 4 ? STAGES : 4) : 1;
+  static_assert(SF_SETS <= STAGES, "a scale set's free phase must be unambiguous");
+  static_assert(SF_TMEM_COL + SF_SETS * SF_SET_COLS <= TMEM_COLS, "TMEM column budget");
+  static_assert(!SF_TILED || T_SLOTS >= SF_SETS, "scale-set barriers");
   // Stream-K owner: each epilogue warp streams its contributors' partial
   // chunks (32 rows x 32 fp32 columns, 4 KB) through FIX_SLOTS slots of its
   // own, placed in the operand stages, which are idle once the CTA's last MMA
@@ -481,6 +504,41 @@ __device__ __forceinline__ void store_chunk32_staged(uint8_t* buf, uint16_t* D, 
   __syncwarp();
 }
 
+// store_chunk32_staged for a chunk already converted to 16 packed bf16 pairs.
+__device__ __forceinline__ void store_chunk32_packed(uint8_t* buf, uint16_t* D, uint64_t ldd,
+                                                     uint32_t M, uint32_t N, uint32_t row0,
+                                                     uint32_t col0, const uint32_t (&p)[16],
+                                                     uint32_t lane) {
+#pragma unroll
+  for (uint32_t j = 0; j < 4; ++j)
+    *reinterpret_cast<uint4*>(buf + lane * 64 + ((j ^ ((lane >> 1) & 3u)) << 4)) =
+        make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+  __syncwarp();
+  const uint32_t ncols = min(32u, N - col0);
+  const uint32_t nrows = row0 < M ? min(32u, M - row0) : 0u;
+  const bool vec = ncols == 32 && ((reinterpret_cast<uintptr_t>(D + col0) | (ldd * 2)) & 15) == 0;
+  if (vec) {
+#pragma unroll
+    for (uint32_t i = 0; i < 4; ++i) {
+      const uint32_t r = 8 * i + (lane >> 2), j = lane & 3u;
+      if (r < nrows) {
+        const uint4 piece = *reinterpret_cast<const uint4*>(buf + r * 64 + ((j ^ ((r >> 1) & 3u)) << 4));
+        *reinterpret_cast<uint4*>(D + static_cast<uint64_t>(row0 + r) * ldd + col0 + 8 * j) = piece;
+      }
+    }
+  } else {
+    const uint32_t j = lane >> 3, e = lane & 7u;
+#pragma unroll 4
+    for (uint32_t r = 0; r < nrows; ++r) {
+      if (lane < ncols) {
+        const uint16_t x = *reinterpret_cast<const uint16_t*>(buf + r * 64 + ((j ^ ((r >> 1) & 3u)) << 4) + 2 * e);
+        D[static_cast<uint64_t>(row0 + r) * ldd + col0 + lane] = x;
+      }
+    }
+  }
+  __syncwarp();
+}
+
 // ------------------------------------------------------------ fused epilogue
 
 __device__ __forceinline__ float epi_act(float x, uint32_t act) {
@@ -637,8 +695,12 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
       mbar_init(raw_full_bar(g), 1);   // this CTA's scale bytes landed (expect_tx)
     }
     for (uint32_t g = 0; g < C::T_SLOTS; ++g) {
-      mbar_init(t_ready_bar(g), CG);   // leader: every CTA's SF warp filled the slot
-      mbar_init(t_empty_bar(g), 1);    // MMA issuer's commit after the group's last K-tile
+      // leader: every CTA's SF warp filled the slot (tiled scales: scale set
+      // g of TMEM written, the copy thread's commit)
+      mbar_init(t_ready_bar(g), C::SF_TILED ? 1 : CG);
+      // MMA issuer's commit after the group's last K-tile (tiled scales: g = 0
+      // is the copy thread's exit drain)
+      mbar_init(t_empty_bar(g), 1);
     }
     for (uint32_t b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);        // MMA issuer's commit after the last K-tile
@@ -767,21 +829,27 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
             ok = false;
             break;
           }
+          // tiled scales: the copy thread has written this K-tile's scale set
+          if (C::SF_TILED &&
+              !wait_bounded(t_ready_bar(it % C::SF_SETS), (it / C::SF_SETS) & 1u, wd, kSiteMmaFull)) {
+            ok = false;
+            break;
+          }
           const uint32_t sb = stage0 + s * C::STAGE_BYTES;
           tc_fence_after_sync();
           const uint64_t adesc = smem_desc_sw128(sb);
           const uint64_t bdesc = smem_desc_sw128(sb + C::OFF_B);
           if constexpr (C::MX) {
-            const uint32_t sfa_t = tmem_base + C::SF_TMEM_COL;
+            const uint32_t sfa_t = tmem_base + C::SF_TMEM_COL + (it % C::SF_SETS) * C::SF_SET_COLS;
             const uint32_t sfb_t = sfa_t + 4;
-            // the K-tile's scale chunks: in the stage itself (tiled scales) or
-            // in the re-tiled slot of its group
-            const uint32_t tsrc = C::SF_TILED ? sb + C::OFF_SF
-                                              : t0 + g * C::T_SLOT_BYTES + (kt % C::SF_GROUP) * C::T_PER_KT;
-            tmem_cp_32x128b_warpx4<CG>(sfa_t, smem_desc_rows16(tsrc));
+            if constexpr (C::SF_WARP) {
+              // the K-tile's chunks in the re-tiled slot of its group
+              const uint32_t tsrc = t0 + g * C::T_SLOT_BYTES + (kt % C::SF_GROUP) * C::T_PER_KT;
+              tmem_cp_32x128b_warpx4<CG>(sfa_t, smem_desc_rows16(tsrc));
 #pragma unroll
-            for (uint32_t h = 0; h < C::SFB_CHUNKS; ++h)
-              tmem_cp_32x128b_warpx4<CG>(sfb_t + 4 * h, smem_desc_rows16(tsrc + 512 * (1 + h)));
+              for (uint32_t h = 0; h < C::SFB_CHUNKS; ++h)
+                tmem_cp_32x128b_warpx4<CG>(sfb_t + 4 * h, smem_desc_rows16(tsrc + 512 * (1 + h)));
+            }
 #pragma unroll
             for (uint32_t k = 0; k < C::K_STEPS; ++k)
               mma_mxf8<CG>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc_mxf8(C::UMMA_M, C::UMMA_N, k, k),
@@ -810,6 +878,51 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
         else
           tc_commit_pair_multicast(drain_bar, 0x1);
         drain_wait(drain_bar, 0, wd, kSiteMmaDrain);
+      }
+    }
+  } else if (C::SF_TILED && warp == C::kCpWarp) {
+    // ==================== scale copies: one thread of the leader CTA ==============
+    // For each K-tile, once its stage has landed and the MMAs of the K-tile
+    // two back (which read the same scale set) have completed, copy its scale
+    // chunks from the stage into scale set it % 2 and commit to that set's
+    // barrier.  tcgen05 operations of different threads are ordered only
+    // through these commits and barrier waits.
+    if (leader && lane == 0) {
+      uint32_t it = 0;
+      bool issued = false, ok = true;
+      WorkItem w;
+      for (uint32_t wi = 0; ok && work_item(args, cluster_id, num_clusters, KT, wi, w); ++wi) {
+        for (uint32_t kt = w.k_begin; kt < w.k_end; ++kt, ++it) {
+          const uint32_t s = it % C::STAGES;
+          if (!wait_bounded(full_bar(s), (it / C::STAGES) & 1u, wd, kSiteSfFull)) { ok = false; break; }
+          if (it >= C::SF_SETS) {
+            const uint32_t p = it - C::SF_SETS;   // the K-tile whose MMAs read this set last
+            if (!wait_bounded(empty_bar(p % C::STAGES), (p / C::STAGES) & 1u, wd, kSiteSfFull)) {
+              ok = false;
+              break;
+            }
+          }
+          tc_fence_after_sync();
+          const uint32_t sb = stage0 + s * C::STAGE_BYTES;
+          const uint32_t sfa_t = tmem_base + C::SF_TMEM_COL + (it % C::SF_SETS) * C::SF_SET_COLS;
+          tmem_cp_32x128b_warpx4<CG>(sfa_t, smem_desc_rows16(sb + C::OFF_SF));
+#pragma unroll
+          for (uint32_t h = 0; h < C::SFB_CHUNKS; ++h)
+            tmem_cp_32x128b_warpx4<CG>(sfa_t + 4 + 4 * h, smem_desc_rows16(sb + C::OFF_SF + 512 * (1 + h)));
+          if constexpr (CG == 1)
+            tc_commit(t_ready_bar(it % C::SF_SETS));
+          else
+            tc_commit_pair_multicast(t_ready_bar(it % C::SF_SETS), 0x1);
+          issued = true;
+        }
+      }
+      // Exit path: this thread's copies complete before TMEM is released.
+      if (issued) {
+        if constexpr (CG == 1)
+          tc_commit(t_empty_bar(0));
+        else
+          tc_commit_pair_multicast(t_empty_bar(0), 0x1);
+        drain_wait(t_empty_bar(0), 0, wd, kSiteMmaDrain);
       }
     }
   } else if (C::SF_WARP && warp == C::kSfWarp) {
@@ -979,6 +1092,72 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
       const uint32_t t_addr = tmem_base + ((q * 32u) << 16) + b * C::UMMA_N;
       // 32-column chunks of this tile inside N
       const uint32_t live = min(NCH, (args.N - col_base + 31u) / 32u);
+      if constexpr (C::SF_TILED) {
+        // One accumulator, handed back early: this group's 128 columns go to
+        // registers as packed bf16 (4 chunks of 32, 64 words), the issuer is
+        // told the accumulator is free, and only then are the values staged
+        // and stored -- under the next tile's MMAs.  (The tiled-scale entry
+        // point has no stream-K or fused epilogue: whole tiles, plain store.)
+        // Chunks of group eg: the 32-column chunks eg, eg + 2, eg + 4, eg + 6.
+        static_assert(C::UMMA_N == 256 && NG == 2 && C::TS_COLS == 32, "early release: 4 chunks of 32");
+        const auto chunk = [&](uint32_t i) -> uint32_t { return 2 * i + eg; };
+        uint32_t pk[4][16];
+        const bool rows_live = row0 < args.M;
+        if (rows_live) {
+#pragma unroll
+          for (uint32_t i = 0; i < 4; ++i) {
+            if (chunk(i) < live) {
+              uint32_t v[32];
+              tmem_ld_32x32b_x32(t_addr + chunk(i) * 32, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (uint32_t t = 0; t < 16; ++t)
+                pk[i][t] = pack_bf16x2(__uint_as_float(v[2 * t]), __uint_as_float(v[2 * t + 1]));
+            }
+          }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (CG == 1)
+            mbar_arrive(acce_bar(b));
+          else
+            mbar_arrive_cluster(mapa_shared(acce_bar(b), 0));
+        }
+        if (rows_live) {
+          if constexpr (TMA_STORE) {
+#pragma unroll
+            for (uint32_t i = 0; i < 4; ++i) {
+              if (chunk(i) < live) {
+                const uint32_t buf = epi0 + (ew * C::EPI_BUFS + (chunk_ctr % C::EPI_BUFS)) * C::EPI_BUF_BYTES;
+                if (lane == 0) bulk_wait_group_read<C::EPI_BUFS - 1>();   // the buffer's last store has read it
+                __syncwarp();
+                uint8_t* rowp = base_ptr + (buf - base) + lane * 64;
+#pragma unroll
+                for (uint32_t j = 0; j < 4; ++j)
+                  // 64-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ ((r / 2) % 4)
+                  *reinterpret_cast<uint4*>(rowp + ((j ^ ((lane >> 1) & 3u)) << 4)) =
+                      make_uint4(pk[i][4 * j], pk[i][4 * j + 1], pk[i][4 * j + 2], pk[i][4 * j + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                  tma_store_2d(&tmD, buf, static_cast<int32_t>(col_base + chunk(i) * 32), static_cast<int32_t>(row0));
+                  bulk_commit_group();
+                }
+                ++chunk_ctr;
+              }
+            }
+          } else {
+#pragma unroll
+            for (uint32_t i = 0; i < 4; ++i)
+              if (chunk(i) < live)
+                store_chunk32_packed(base_ptr + (epi0 - base) + ew * C::CHUNK_BYTES,
+                                     static_cast<uint16_t*>(args.D), args.ldd, args.M, args.N, row0,
+                                     col_base + chunk(i) * 32, pk[i], lane);
+          }
+        }
+        continue;
+      }
       if (w.kind == 2) {
         // a later K-range of a split tile: park the fp32 slice in this
         // cluster's slot (float4 index (chunk * 8 + i / 4) * 32 + lane, so each
