@@ -238,6 +238,17 @@ class Problem:
         import dense_gemm_blackwell_tcgen05_gb300 as g
         import gemm_inputs as gi
         self.w = w
+        self.tiled = w.kind == "mxfp8" and w.sf_layout == "tiled"
+        self.rows_dev = None
+        if self.tiled:
+            # the same scale bytes, rearranged on the host into the tiled layout
+            # the GEMM takes (what a caller keeps its scales in for this path)
+            A, SFA, B, SFB = host[:4]
+            self.rows_dev = (SFA.to(device), SFB.to(device))   # row-major twin (context only)
+            tiles = (gi.tile_scales(SFA, w.M, w.K), gi.tile_scales(SFB, w.N, w.K))
+            if SFA.is_pinned():
+                tiles = tuple(t.pin_memory() for t in tiles)
+            host = (A, tiles[0], B, tiles[1]) + tuple(host[4:])
         self.host = host
         self.dev = tuple(t.to(device, non_blocking=False) for t in host)
         self.spec = gi.epilogue_spec(w)
@@ -299,6 +310,10 @@ class Problem:
                                            stream_handle)
             return g.gemm_bf16_variant(v, *args, stream_handle)
         A, SFA, B, SFB = ops
+        if self.tiled:
+            return g.gemm_mxfp8_tiled(v, A.data_ptr(), B.data_ptr(), SFA.data_ptr(), SFB.data_ptr(),
+                                      D.data_ptr(), w.M, w.N, w.K, A.stride(0), B.stride(0),
+                                      D.stride(0), stream_handle)
         args = (A.data_ptr(), B.data_ptr(), SFA.data_ptr(), SFB.data_ptr(), D.data_ptr(), w.M,
                 w.N, w.K, A.stride(0), B.stride(0), SFA.stride(0), SFB.stride(0), D.stride(0))
         if self.spec:
@@ -427,16 +442,14 @@ def run_reference(args, rank, world):
 
 
 def blocked_scales(sf, rows: int, K: int):
-    """UE8M0 scales [rows, >= K/32] rearranged into cuBLASLt's block-scaled layout (128-row x
-    4-block tiles of 512 bytes; inside a tile, row r's byte for block c sits at
-    16*(r % 32) + 4*(r // 32) + c), as torch._scaled_mm takes them.  Context leg only."""
+    """UE8M0 scales [rows, >= K/32] in cuBLASLt's block-scaled layout (the tiled layout of
+    gemm_inputs.tile_scales: 128-row x 4-block tiles of 512 bytes), shaped [R, C] and typed
+    as torch._scaled_mm takes them.  Context leg only."""
     import torch
-    nb = (K + 31) // 32
-    R, C = (rows + 127) // 128 * 128, (nb + 3) // 4 * 4
-    p = torch.zeros(R, C, dtype=torch.uint8, device=sf.device)
-    p[:rows, :nb] = sf[:rows, :nb]
-    t = p.view(R // 128, 128, C // 4, 4).permute(0, 2, 1, 3).reshape(-1, 4, 32, 4).transpose(1, 2)
-    return t.reshape(R, C).contiguous().view(torch.float8_e8m0fnu)
+
+    import gemm_inputs as gi
+    R, C = (rows + 127) // 128 * 128, ((K + 31) // 32 + 3) // 4 * 4
+    return gi.tile_scales(sf, rows, K).view(R, C).view(torch.float8_e8m0fnu)
 
 
 def library_context(probs, stream, n: int, flush_buf, flush_each):
@@ -460,7 +473,13 @@ def library_context(probs, stream, n: int, flush_buf, flush_each):
                 lib = lambda A=A, B=B: torch.matmul(A, B.t())
             else:
                 A, SFA, B, SFB = p.dev[:4]
-                sa, sb = blocked_scales(SFA, w.M, w.K), blocked_scales(SFB, w.N, w.K)
+                if p.tiled:   # already the layout cuBLASLt takes
+                    R = lambda n: (n + 127) // 128 * 128
+                    C = ((w.K + 31) // 32 + 3) // 4 * 4
+                    sa = SFA.view(R(w.M), C).view(torch.float8_e8m0fnu)
+                    sb = SFB.view(R(w.N), C).view(torch.float8_e8m0fnu)
+                else:
+                    sa, sb = blocked_scales(SFA, w.M, w.K), blocked_scales(SFB, w.N, w.K)
                 a8, b8 = A.view(torch.float8_e4m3fn), B.view(torch.float8_e4m3fn)
                 lib_name = "torch._scaled_mm (cuBLASLt, block-scaled E4M3)"
                 lib = lambda a8=a8, b8=b8, sa=sa, sb=sb: torch._scaled_mm(
@@ -503,6 +522,15 @@ def library_context(probs, stream, n: int, flush_buf, flush_each):
                            "library_tflops": w.flops / (min(t_lib) / 1e3) / 1e12,
                            "ours_tflops": w.flops / (min(t_ours) / 1e3) / 1e12,
                            "launches": 2 * n, "bitwise_equal_to_ours": same}
+            if p.tiled:
+                # our row-major-scale entry point on the same operands
+                SAr, SBr = p.rows_dev
+                rows_f = lambda: g.gemm_mxfp8_variant(
+                    0, A.data_ptr(), B.data_ptr(), SAr.data_ptr(), SBr.data_ptr(), p.D.data_ptr(),
+                    w.M, w.N, w.K, A.stride(0), B.stride(0), SAr.stride(0), SBr.stride(0),
+                    p.D.stride(0), stream.cuda_stream)
+                t_rows = [timed(rows_f) for _ in range(2)]
+                out[w.name]["ours_row_major_scales_tflops"] = w.flops / (min(t_rows) / 1e3) / 1e12
         except Exception as exc:   # a torch without block-scaled _scaled_mm, for instance
             out[w.name] = {"unavailable": repr(exc)[:200]}
     return out
@@ -717,7 +745,9 @@ def run_ours(args, rank, world, local):
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "+".join(sorted({"bf16" if w.kind == "bf16" else "e4m3" for w in works})) + "->f32",
-            "data": "synthetic (seeded; bf16 N(0,1)*0.5, MXFP8 quantised from N(0,1))",
+            "data": "synthetic (seeded; bf16 N(0,1)*0.5, MXFP8 quantised from N(0,1)"
+                    + ("; MXFP8 scales passed in the tiled layout" if any(p.tiled for p in probs) else "")
+                    + ")",
             "config": {"workload": " + ".join(f"{w.name} {w.M}x{w.N}x{w.K} {w.kind}" for w in works),
                        "variant": args.variant,
                        "l2": ("512 MiB write before each launch of a workload whose inputs fit "

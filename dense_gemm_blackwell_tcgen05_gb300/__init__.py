@@ -22,7 +22,7 @@ __all__ = [
     "VARIANT_DIRECT_STORE",
     "GemmError", "load", "library_path", "EXPORTED_SYMBOLS",
     "gemm_bf16", "gemm_bf16_variant", "gemm_mxfp8", "gemm_mxfp8_variant", "gemm_mxfp8_tiled",
-    "matmul_mxfp8_tiled", "gemm_last_status", "gemm_last_status_word", "gemm_status_string", "gemm_set_watchdog_ms",
+    "matmul_mxfp8_tiled", "gemm_mxfp8_quantize_tiled", "quantize_mxfp8_tiled", "gemm_last_status", "gemm_last_status_word", "gemm_status_string", "gemm_set_watchdog_ms",
     "gemm_kernel_plan", "gemm_last_cuda_error", "gemm_debug_stall_next_launch",
     "gemm_mxfp8_quantize", "quantize_mxfp8", "gemm_bf16_streamk", "gemm_mxfp8_streamk",
     "gemm_streamk_workspace_bytes", "gemm_last_schedule", "streamk_workspace",
@@ -55,6 +55,7 @@ EXPORTED_SYMBOLS = (
     "gemm_bf16_streamk", "gemm_mxfp8_streamk", "gemm_streamk_workspace_bytes",
     "gemm_last_schedule", "gemm_bf16_streamk_noalloc", "gemm_set_streamk_mode",
     "gemm_streamk_plan", "gemm_bf16_fused", "gemm_mxfp8_fused", "gemm_mxfp8_tiled",
+    "gemm_mxfp8_quantize_tiled",
 )
 
 _lock = threading.Lock()
@@ -135,6 +136,8 @@ def load() -> ctypes.CDLL:
             L.gemm_last_schedule.restype = ctypes.c_int
             L.gemm_mxfp8_quantize.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp]
             L.gemm_mxfp8_quantize.restype = ctypes.c_int
+            L.gemm_mxfp8_quantize_tiled.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp]
+            L.gemm_mxfp8_quantize_tiled.restype = ctypes.c_int
             L.gemm_last_status.argtypes = [_vp]
             L.gemm_last_status.restype = ctypes.c_int
             L.gemm_last_status_word.argtypes = [_vp]
@@ -322,6 +325,11 @@ def gemm_mxfp8_quantize(X: int, rows: int, K: int, ldx: int, Q: int, ldq: int, S
     return load().gemm_mxfp8_quantize(X, rows, K, ldx, Q, ldq, SF, ldsf, stream)
 
 
+def gemm_mxfp8_quantize_tiled(X: int, rows: int, K: int, ldx: int, Q: int, ldq: int, SF: int,
+                              stream: int = 0) -> int:
+    return load().gemm_mxfp8_quantize_tiled(X, rows, K, ldx, Q, ldq, SF, stream)
+
+
 def gemm_last_status(stream: int = 0) -> int:
     return load().gemm_last_status(stream)
 
@@ -430,6 +438,24 @@ def matmul_mxfp8(A, SFA, B, SFB, out=None, variant: int = VARIANT_AUTO, stream=N
     if rc != GEMM_OK:
         raise GemmError(rc, "gemm_mxfp8")
     return out
+
+
+def quantize_mxfp8_tiled(X, stream=None):
+    """MXFP8-encode a float32 CUDA tensor X [rows, K]: returns (Q uint8 [rows, K],
+    SF uint8, flat, in the tiled layout of gemm_mxfp8_tiled)."""
+    import torch
+    _check_2d(X, "X")
+    if X.dtype != torch.float32:
+        raise TypeError("X must be float32")
+    rows, K = X.shape
+    n = (rows + 127) // 128 * (((K + 31) // 32 + 3) // 4) * 512
+    Q = torch.empty(rows, K, dtype=torch.uint8, device=X.device)
+    SF = torch.empty(n, dtype=torch.uint8, device=X.device)
+    rc = gemm_mxfp8_quantize_tiled(X.data_ptr(), rows, K, X.stride(0), Q.data_ptr(), Q.stride(0),
+                                   SF.data_ptr(), _stream_handle(stream))
+    if rc != GEMM_OK:
+        raise GemmError(rc, "gemm_mxfp8_quantize_tiled")
+    return Q, SF
 
 
 def matmul_mxfp8_tiled(A, SFA, B, SFB, out=None, variant: int = VARIANT_AUTO, stream=None):

@@ -520,7 +520,26 @@ int gemm_mxfp8_quantize(const float* X, int64_t rows, int64_t K, int64_t ldx, vo
   return launch_mxfp8_quantize(X, static_cast<uint32_t>(rows), static_cast<uint32_t>(K),
                                static_cast<uint64_t>(ldx), static_cast<uint8_t*>(Q),
                                static_cast<uint64_t>(ldq), static_cast<uint8_t*>(SF),
-                               static_cast<uint64_t>(ldsf), ctx.num_sms, stream);
+                               static_cast<uint64_t>(ldsf), false, ctx.num_sms, stream);
+}
+
+int gemm_mxfp8_quantize_tiled(const float* X, int64_t rows, int64_t K, int64_t ldx, void* Q,
+                              int64_t ldq, void* SF, cudaStream_t stream) {
+  if (rows < 0 || K < 0 || rows > kMaxDim || K > kMaxDim) return GEMM_ERR_INVALID_ARG;
+  if (rows == 0 || K == 0) return GEMM_OK;
+  if (X == nullptr || Q == nullptr || SF == nullptr || ldx < K || ldq < K ||
+      ldx > (int64_t(1) << 36) || ldq > (int64_t(1) << 36))
+    return GEMM_ERR_INVALID_ARG;
+  LaunchCtx ctx;
+  int rc = current_device(&ctx);
+  if (rc != GEMM_OK) return rc;
+  if (!is_device_pointer(X, ctx.device) || !is_device_pointer(Q, ctx.device) ||
+      !is_device_pointer(SF, ctx.device))
+    return GEMM_ERR_INVALID_ARG;
+  return launch_mxfp8_quantize(X, static_cast<uint32_t>(rows), static_cast<uint32_t>(K),
+                               static_cast<uint64_t>(ldx), static_cast<uint8_t*>(Q),
+                               static_cast<uint64_t>(ldq), static_cast<uint8_t*>(SF), 0, true,
+                               ctx.num_sms, stream);
 }
 
 uint64_t gemm_last_status_word(cudaStream_t stream) {

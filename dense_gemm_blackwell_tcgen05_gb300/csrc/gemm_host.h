@@ -144,7 +144,7 @@ uint32_t smallk_max_k();
 // K == 0 with a fused epilogue: D = act(alpha * 0 + beta * C + bias).
 int launch_epilogue_only(const Problem& p, int num_sms, cudaStream_t stream);
 int launch_mxfp8_quantize(const float* X, uint32_t rows, uint32_t K, uint64_t ldx, uint8_t* Q,
-                          uint64_t ldq, uint8_t* SF, uint64_t ldsf, int num_sms,
+                          uint64_t ldq, uint8_t* SF, uint64_t ldsf, bool tiled, int num_sms,
                           cudaStream_t stream);
 
 // Compile-time plans for gemm_kernel_plan().

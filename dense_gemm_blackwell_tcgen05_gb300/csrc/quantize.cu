@@ -7,7 +7,9 @@
 //          (amax = 0 gives e = -127); scale byte = e + 127
 //   q    = round-to-nearest-even E4M3 of x * 2^-e (exact power-of-two scaling;
 //          |x * 2^-e| <= 448 by construction); NaN / +-Inf -> E4M3 NaN.
-// HBM-bound: 4 bytes read and ~1.03 bytes written per element.
+// HBM-bound: 4 bytes read and ~1.03 bytes written per element.  The scale
+// bytes go to a row-major matrix, or to the tiled layout of gemm_mxfp8_tiled
+// (512-byte chunks of 128 rows x 4 blocks), whose padding is written as zero.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -26,7 +28,16 @@ struct QuantArgs {
   uint64_t ldx, ldq, ldsf;
   uint32_t units_per_row;   // ceil(K / kUnit)
   bool vec_in, vec_out;     // 16-byte loads / 4-byte stores are aligned everywhere
+  bool tiled;               // SF in the tiled layout (ldsf unused)
+  uint32_t groups;          // tiled: ceil(nblk / 4) block groups per row block
 };
+
+// Byte offset of the scale of (row, block b) in the SF buffer.
+__device__ __forceinline__ uint64_t sf_offset(const QuantArgs& a, uint32_t row, uint32_t b) {
+  if (!a.tiled) return static_cast<uint64_t>(row) * a.ldsf + b;
+  return 512ull * (static_cast<uint64_t>(row / 128) * a.groups + b / 4) + 16 * (row % 32) +
+         4 * ((row % 128) / 32) + b % 4;
+}
 
 // Elements per warp iteration (32 blocks of 32): eight 16-byte loads in flight
 // per lane; 512 measured 5% slower, 2048 slower still.
@@ -88,7 +99,11 @@ __global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const QuantArgs a) 
       m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
       m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
       m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-      if (kb >= a.K) continue;   // whole block past K (all lanes took part in the shuffles)
+      if (kb >= a.K) {   // whole block past K (all lanes took part in the shuffles)
+        // tiled layout: the last group's blocks past K hold zero
+        if (a.tiled && (lane & 7u) == 0 && kb / 32 < 4 * a.groups) a.SF[sf_offset(a, row, kb / 32)] = 0;
+        continue;
+      }
       const int e = scale_exponent(m);
       const float scale = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);   // 2^-e, e <= 126
       const uint32_t k = k0 + 128 * j + 4 * lane;
@@ -103,15 +118,23 @@ __global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const QuantArgs a) 
         for (uint32_t t = 0; t < 4; ++t)
           if (k + t < a.K) qr[k + t] = static_cast<uint8_t>(q >> (8 * t));
       }
-      if ((lane & 7u) == 0) a.SF[row * a.ldsf + kb / 32] = static_cast<uint8_t>(e + 127);
+      if ((lane & 7u) == 0) a.SF[sf_offset(a, row, kb / 32)] = static_cast<uint8_t>(e + 127);
     }
+  }
+  if (a.tiled) {
+    // rows past the last real row of the last row block: zero scales
+    const uint32_t pad_rows = (a.rows + 127) / 128 * 128 - a.rows;
+    const uint64_t pad = static_cast<uint64_t>(pad_rows) * 4 * a.groups;
+    for (uint64_t i = blockIdx.x * blockDim.x + threadIdx.x; i < pad; i += gridDim.x * blockDim.x)
+      a.SF[sf_offset(a, a.rows + static_cast<uint32_t>(i / (4 * a.groups)),
+                     static_cast<uint32_t>(i % (4 * a.groups)))] = 0;
   }
 }
 
 }  // namespace
 
 int launch_mxfp8_quantize(const float* X, uint32_t rows, uint32_t K, uint64_t ldx, uint8_t* Q,
-                          uint64_t ldq, uint8_t* SF, uint64_t ldsf, int num_sms,
+                          uint64_t ldq, uint8_t* SF, uint64_t ldsf, bool tiled, int num_sms,
                           cudaStream_t stream) {
   QuantArgs a;
   a.X = X;
@@ -123,6 +146,8 @@ int launch_mxfp8_quantize(const float* X, uint32_t rows, uint32_t K, uint64_t ld
   a.ldq = ldq;
   a.ldsf = ldsf;
   a.units_per_row = (K + kUnit - 1) / kUnit;
+  a.tiled = tiled;
+  a.groups = ((K + 31) / 32 + 3) / 4;
   a.vec_in = (reinterpret_cast<uintptr_t>(X) & 15u) == 0 && (ldx % 4) == 0;
   a.vec_out = (reinterpret_cast<uintptr_t>(Q) & 3u) == 0 && (ldq % 4) == 0;
   const uint64_t units = static_cast<uint64_t>(rows) * a.units_per_row;

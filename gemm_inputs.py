@@ -17,6 +17,8 @@ ragged_k1040           M=4099, N=2053, K=1040, N(0,1) -> bf16  2
 ragged_k8              M=4099, N=2053, K=8,    N(0,1) -> bf16  2
 square_8192            M=N=K=8192, 0.5*N(0,1) -> bf16          3
 mxfp8_8192             M=N=K=8192, N(0,1) -> MXFP8             4
+                       (scales passed to the GEMM in the tiled layout)
+mxfp8_8192_rows        the same operands, scales passed row-major  4
 quantize_8192          [8192, 8192] float32 N(0,1) (the A       4
                        operand above, before encoding)
 fused_gelu_8192        square_8192's A, B; C [M,N] N(0,1) ->   3 (+100 for C,
@@ -62,6 +64,10 @@ class Workload:
     epilogue: str = ""
     schedule: str = "dp"  # "dp" | "streamk" (caller workspace, automatic split)
     variant: int = 0      # kernel variant the bench runs it with (0 = automatic)
+    # MXFP8: the layout the scale matrices are handed to the GEMM in -- "rows"
+    # (row-major, gemm_mxfp8) or "tiled" (tile_scales of the same bytes,
+    # gemm_mxfp8_tiled).  The operands and their values are the same.
+    sf_layout: str = "rows"
 
     @property
     def flops(self) -> int:
@@ -75,7 +81,8 @@ WORKLOADS = {
         Workload("ragged_k1040", 4099, 2053, 1040, 2, "normal"),
         Workload("ragged_k8", 4099, 2053, 8, 2, "normal"),
         Workload("square_8192", 8192, 8192, 8192, 3, "normal", 0.5),
-        Workload("mxfp8_8192", 8192, 8192, 8192, 4, "normal", 1.0, "mxfp8"),
+        Workload("mxfp8_8192", 8192, 8192, 8192, 4, "normal", 1.0, "mxfp8", sf_layout="tiled"),
+        Workload("mxfp8_8192_rows", 8192, 8192, 8192, 4, "normal", 1.0, "mxfp8"),
         Workload("quantize_8192", 8192, 0, 8192, 4, "normal", 1.0, "quant"),
         Workload("fused_gelu_8192", 8192, 8192, 8192, 3, "normal", 0.5, "bf16",
                  epilogue="1.0,1.0,gelu,bf16,bf16"),

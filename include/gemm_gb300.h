@@ -304,6 +304,15 @@ int64_t gemm_streamk_workspace_bytes(int mxfp8, int variant);
 int gemm_mxfp8_quantize(const float* X, int64_t rows, int64_t K, int64_t ldx, void* Q,
                         int64_t ldq, void* SF, int64_t ldsf, cudaStream_t stream);
 
+/* gemm_mxfp8_quantize writing the scale bytes in the tiled layout that
+ * gemm_mxfp8_tiled takes (no counterpart on the pages beyond the scale
+ * layout itself): SF receives ceil(rows/128) * ceil(ceil(K/32)/4) * 512
+ * bytes, every one written -- the scales, and zero in the padding (rows past
+ * `rows` in the last row block, blocks past ceil(K/32) in the last group).
+ * Q as for gemm_mxfp8_quantize.  Same errors, minus the scale pitch. */
+int gemm_mxfp8_quantize_tiled(const float* X, int64_t rows, int64_t K, int64_t ldx, void* Q,
+                              int64_t ldq, void* SF, cudaStream_t stream);
+
 /*
  * Synchronises `stream`, then returns and clears the current device's status
  * word: GEMM_OK, GEMM_ERR_TIMEOUT when a kernel's bounded barrier wait gave up

@@ -118,8 +118,23 @@ def test_wide_scale_pitch():
 
 
 @pytest.mark.slow
-def test_workload_mxfp8_8192():
+def test_workload_mxfp8_8192_tiled():
+    """The bench's MXFP8 headline configuration: gemm_mxfp8_tiled, automatic
+    kernel (the CTA pair, 256x256 tiles), every tile edge sampled."""
     w = gi.WORKLOADS["mxfp8_8192"]
+    assert w.sf_layout == "tiled"
+    A, SFA, B, SFB = gi.workload_operands("mxfp8_8192")
+    D = g.matmul_mxfp8_tiled(A.cuda(), gi.tile_scales(SFA, w.M, w.K).cuda(), B.cuda(),
+                             gi.tile_scales(SFB, w.N, w.K).cuda())
+    assert g.gemm_last_status(0) == g.GEMM_OK
+    rows, cols = P.sample_positions(w.M, w.N, 3000, seed=w.seed, tile_m=128, tile_n=256)
+    D_ref, S = oracle.gemm_mxfp8_entries(A.numpy(), B.numpy(), SFA.numpy(), SFB.numpy(), rows, cols)
+    P.check_within_bound(P.bf16_to_f64(D.cpu())[rows, cols], D_ref, S, "mxfp8_8192 tiled")
+
+
+@pytest.mark.slow
+def test_workload_mxfp8_8192():
+    w = gi.WORKLOADS["mxfp8_8192_rows"]
     A, SFA, B, SFB = gi.workload_operands("mxfp8_8192")
     D = run(A, SFA, B, SFB, g.VARIANT_AUTO)
     # every 224-column tile edge of the MXFP8 kernels and every 128-row edge

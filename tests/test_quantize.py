@@ -111,3 +111,44 @@ def test_quantise_then_gemm():
     assert np.array_equal(qa.cpu().numpy(), Qa) and np.array_equal(qb.cpu().numpy(), Qb)
     D_ref, S = oracle.gemm_mxfp8(Qa, Qb, SFa, SFb)
     P.check_within_bound(P.bf16_to_f64(D), D_ref, S, "quantise->gemm")
+
+
+@pytest.mark.parametrize("rows, K", [(1, 1), (127, 31), (128, 32), (129, 33), (300, 100),
+                                     (257, 1040), (64, 4096)])
+def test_quantize_tiled_layout(rows, K):
+    """The tiled scale output: every byte of the buffer written -- the oracle's
+    scales at their tiled positions, zero in the padding -- and the codes as
+    in the row-major form."""
+    rng = np.random.default_rng(rows + K)
+    X_cpu = (rng.standard_normal((rows, K)) * rng.uniform(1e-3, 1e3, (rows, 1))).astype(np.float32)
+    X = torch.from_numpy(X_cpu).cuda()
+    n = (rows + 127) // 128 * (((K + 31) // 32 + 3) // 4) * 512
+    Q = torch.full((rows, K), 0xAB, dtype=torch.uint8, device="cuda")
+    SF = torch.full((n,), 0xCD, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    rc = g.gemm_mxfp8_quantize_tiled(X.data_ptr(), rows, K, K, Q.data_ptr(), K, SF.data_ptr(), s)
+    assert rc == g.GEMM_OK, g.gemm_status_string(rc)
+    torch.cuda.synchronize()
+    Qr, SFr = oracle.mxfp8_quantize(X_cpu)
+    assert np.array_equal(Q.cpu().numpy(), Qr)
+    want = gi.tile_scales(torch.from_numpy(np.ascontiguousarray(SFr)), rows, K).numpy()
+    got = SF.cpu().numpy()
+    assert got.shape == want.shape
+    if not np.array_equal(got, want):
+        i = int(np.flatnonzero(got != want)[0])
+        raise AssertionError(f"tiled scale byte {i}: gpu {got[i]} want {want[i]}")
+
+
+def test_quantize_tiled_feeds_the_tiled_gemm():
+    """GPU-quantised operands with tiled scales into gemm_mxfp8_tiled, against
+    the oracle on the oracle's own quantisation of the same floats."""
+    M, N, K = 300, 520, 384
+    XA, XB = gi.float_operands(M, N, K, seed=12)
+    A, SFA = g.quantize_mxfp8_tiled(XA.cuda())
+    B, SFB = g.quantize_mxfp8_tiled(XB.cuda())
+    D = g.matmul_mxfp8_tiled(A, SFA, B, SFB)
+    assert g.gemm_last_status(0) == g.GEMM_OK
+    QA, SA = oracle.mxfp8_quantize(XA.numpy())
+    QB, SB = oracle.mxfp8_quantize(XB.numpy())
+    D_ref, S = oracle.gemm_mxfp8(QA, QB, SA, SB)
+    P.check_within_bound(P.bf16_to_f64(D), D_ref, S, "quantised tiled gemm")
