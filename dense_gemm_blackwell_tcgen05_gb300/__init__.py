@@ -19,6 +19,7 @@ __all__ = [
     "GEMM_OK", "GEMM_ERR_INVALID_ARG", "GEMM_ERR_ALIGNMENT", "GEMM_ERR_UNSUPPORTED_DEVICE",
     "GEMM_ERR_LAUNCH", "GEMM_ERR_TIMEOUT", "GEMM_ERR_DEVICE_FAULT",
     "VARIANT_AUTO", "VARIANT_1CTA", "VARIANT_2CTA", "VARIANT_SYNC", "VARIANT_SMALLK",
+    "VARIANT_SMALLK_TC",
     "VARIANT_DIRECT_STORE",
     "GemmError", "load", "library_path", "EXPORTED_SYMBOLS",
     "gemm_bf16", "gemm_bf16_variant", "gemm_mxfp8", "gemm_mxfp8_variant", "gemm_mxfp8_tiled",
@@ -45,6 +46,7 @@ VARIANT_1CTA = 1
 VARIANT_2CTA = 2
 VARIANT_SYNC = 3
 VARIANT_SMALLK = 4
+VARIANT_SMALLK_TC = 5
 VARIANT_DIRECT_STORE = 0x100
 
 # Every function include/gemm_gb300.h declares.

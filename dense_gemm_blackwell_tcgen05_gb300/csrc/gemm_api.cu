@@ -294,10 +294,10 @@ static int bf16_impl(int variant, const void* A, const void* B, void* D, int64_t
                      const gemm_epilogue_t* epi, cudaStream_t stream) {
   const int base = variant & 0xFF;
   const bool direct = (variant & GEMM_VARIANT_DIRECT_STORE) != 0;
-  if ((variant & ~(0xFF | GEMM_VARIANT_DIRECT_STORE)) != 0 || base > GEMM_VARIANT_SMALLK)
+  if ((variant & ~(0xFF | GEMM_VARIANT_DIRECT_STORE)) != 0 || base > GEMM_VARIANT_SMALLK_TC)
     return GEMM_ERR_INVALID_ARG;
-  if (base == GEMM_VARIANT_SMALLK && (ws != nullptr || epi != nullptr || K > smallk_max_k()))
-    return GEMM_ERR_INVALID_ARG;
+  const bool smallk = base == GEMM_VARIANT_SMALLK || base == GEMM_VARIANT_SMALLK_TC;
+  if (smallk && (ws != nullptr || epi != nullptr || K > smallk_max_k())) return GEMM_ERR_INVALID_ARG;
   int rc = check_shape(A, B, D, M, N, K, lda, ldb, ldd, 2);
   if (rc == GEMM_OK && M != 0 && N != 0) rc = check_epilogue_alignment(epi, D);
   if (rc != GEMM_OK || M == 0 || N == 0) return rc;
@@ -344,6 +344,8 @@ static int bf16_impl(int variant, const void* A, const void* B, void* D, int64_t
   switch (base) {
     case GEMM_VARIANT_SMALLK:
       return launch_bf16_smallk(p, ctx.num_sms, stream);
+    case GEMM_VARIANT_SMALLK_TC:
+      return launch_bf16_smallk_tc(p, ctx, stream);
     case GEMM_VARIANT_SYNC:
       return launch_bf16_sync(p, ctx, stream);
     case GEMM_VARIANT_1CTA:

@@ -141,6 +141,8 @@ int launch_zero_fill(const Problem& p, cudaStream_t stream);
 // CUDA-core kernel for 1 <= K <= smallk_max_k() (plain bf16 store only).
 int launch_bf16_smallk(const Problem& p, int num_sms, cudaStream_t stream);
 uint32_t smallk_max_k();
+// Tensor-core kernel for 1 <= K <= 16 (plain bf16 store only).
+int launch_bf16_smallk_tc(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream);
 // K == 0 with a fused epilogue: D = act(alpha * 0 + beta * C + bias).
 int launch_epilogue_only(const Problem& p, int num_sms, cudaStream_t stream);
 int launch_mxfp8_quantize(const float* X, uint32_t rows, uint32_t K, uint64_t ldx, uint8_t* Q,

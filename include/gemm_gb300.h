@@ -78,8 +78,13 @@ typedef enum {
                                    (ladder levels 1-3; bf16 only, reference rung)  */
   GEMM_VARIANT_SMALLK = 4,      /* bf16 only, 1 <= K <= 16: CUDA-core kernel for
                                    the HBM-bound case (a write of D at about 8
-                                   flops per byte), coalesced row stores; AUTO
-                                   picks it for plain calls with K <= 16           */
+                                   flops per byte), aligned 16-byte row stores     */
+  GEMM_VARIANT_SMALLK_TC = 5,   /* bf16 only, 1 <= K <= 16: one tcgen05.mma per
+                                   128x256 tile (operands loaded at their real K,
+                                   rows grouped by residue mod 8 so that every
+                                   store is an aligned 16-byte one); AUTO picks
+                                   one of the two small-K kernels for plain
+                                   calls with K <= 16                              */
   GEMM_VARIANT_DIRECT_STORE = 0x100  /* flag: masked st.global epilogue instead of
                                         TMA stores, even when D is aligned.  Without
                                         it the library picks: TMA stores where D is

@@ -118,7 +118,12 @@ def test_smallk_plan_and_validation():
         g.GEMM_ERR_INVALID_ARG
     assert g.gemm_bf16_fused(4, FAKE, FAKE, FAKE, 4, 4, 8, 8, 8, 4, g.GemmEpilogue(), 0) == \
         g.GEMM_ERR_INVALID_ARG
-    assert g.gemm_bf16_variant(5, FAKE, FAKE, FAKE, 4, 4, 8, 8, 8, 4, 0) == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_bf16_variant(6, FAKE, FAKE, FAKE, 4, 4, 8, 8, 8, 4, 0) == g.GEMM_ERR_INVALID_ARG
+    # the tensor-core small-K kernel takes the same limits
+    assert g.gemm_bf16_variant(g.VARIANT_SMALLK_TC, FAKE, FAKE, FAKE, 4, 4, 17, 24, 24, 4, 0) == \
+        g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_bf16_fused(g.VARIANT_SMALLK_TC, FAKE, FAKE, FAKE, 4, 4, 8, 8, 8, 4,
+                             g.GemmEpilogue(), 0) == g.GEMM_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("mx, variant", [(0, 1), (0, 2), (0, 3), (0, 0x101), (0, 0x102), (1, 1), (1, 0x101),

@@ -23,6 +23,7 @@ BF16_VARIANTS = {
     "1cta_direct": g.VARIANT_1CTA | g.VARIANT_DIRECT_STORE,
     "2cta_direct": g.VARIANT_2CTA | g.VARIANT_DIRECT_STORE,
     "smallk": g.VARIANT_SMALLK,
+    "smallk_tc": g.VARIANT_SMALLK_TC,
     "auto": g.VARIANT_AUTO,
 }
 MX_VARIANTS = {
@@ -57,7 +58,7 @@ def _check(Dbuf, M, N, D_ref):
 @pytest.mark.parametrize("shape", BF16_SHAPES)
 def test_bf16_degenerate(v, shape):
     M, N, K = shape
-    if v == "smallk" and K > 16:
+    if v in ("smallk", "smallk_tc") and K > 16:
         pytest.skip("the small-K kernel takes K <= 16")
     lda = (K + 7) // 8 * 8          # a 16-byte row pitch
     rng = np.random.default_rng(M * 7 + N * 3 + K)

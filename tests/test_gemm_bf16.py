@@ -278,7 +278,10 @@ def test_ragged_n_never_writes_padding(v, N, ldd):
 
 # --------------------------------------------- small-K CUDA-core kernel (K <= 16)
 
-@pytest.mark.parametrize("v", ["smallk", "auto"])
+SMALLK_VARIANTS = {"smallk": g.VARIANT_SMALLK, "smallk_tc": g.VARIANT_SMALLK_TC, "auto": g.VARIANT_AUTO}
+
+
+@pytest.mark.parametrize("v", list(SMALLK_VARIANTS))
 @pytest.mark.parametrize("M, N, K, lda, ldd", [(300, 520, 8, 8, 520), (4099, 2053, 8, 8, 2053),
                                                (129, 257, 1, 8, 264), (257, 300, 16, 16, 301),
                                                (33, 1031, 3, 8, 1031), (1, 1, 5, 8, 1)])
@@ -286,7 +289,7 @@ def test_smallk_small_integers_bitwise(v, M, N, K, lda, ldd):
     """Bitwise for both row-store forms: bf16 pairs (4-byte aligned rows) and
     single values (odd pitch: every other row), ragged M and N, padding left
     untouched."""
-    variant = g.VARIANT_SMALLK if v == "smallk" else g.VARIANT_AUTO
+    variant = SMALLK_VARIANTS[v]
     gen = torch.Generator().manual_seed(M + N + K)
     A = torch.zeros(M, lda, dtype=torch.bfloat16)
     B = torch.zeros(N, lda, dtype=torch.bfloat16)
@@ -307,10 +310,11 @@ def test_smallk_small_integers_bitwise(v, M, N, K, lda, ldd):
     assert_bitwise(D[:, :N], D_ref)
 
 
+@pytest.mark.parametrize("v", ["smallk", "smallk_tc"])
 @pytest.mark.parametrize("M, N, K, ldd, offset", [
     (64, 2053, 8, 2053, 0), (64, 2053, 8, 2053, 3), (40, 257, 5, 261, 1), (40, 255, 8, 255, 7),
     (48, 513, 12, 515, 2), (48, 127, 16, 133, 5), (70000, 40, 4, 41, 1), (300, 1, 8, 1, 1)])
-def test_smallk_any_row_alignment(M, N, K, ldd, offset):
+def test_smallk_any_row_alignment(v, M, N, K, ldd, offset):
     """Rows that start at every element offset within a 16-byte line (odd
     pitches, D placed `offset` elements into its buffer), ragged column strips
     and a grid that walks several row tiles per block: bitwise, and nothing
@@ -324,7 +328,7 @@ def test_smallk_any_row_alignment(M, N, K, ldd, offset):
     Ad, Bd = A.cuda(), B.cuda()
     buf = torch.full((offset + M * ldd + 64,), -1234.0, dtype=torch.bfloat16, device="cuda")
     dptr = buf.data_ptr() + 2 * offset
-    rc = g.gemm_bf16_variant(g.VARIANT_SMALLK, Ad.data_ptr(), Bd.data_ptr(), dptr, M, N, K, lda,
+    rc = g.gemm_bf16_variant(SMALLK_VARIANTS[v], Ad.data_ptr(), Bd.data_ptr(), dptr, M, N, K, lda,
                              lda, ldd, 0)
     assert rc == g.GEMM_OK, g.gemm_status_string(rc)
     assert g.gemm_last_status(0) == g.GEMM_OK
@@ -345,21 +349,28 @@ def test_smallk_rejects_an_odd_byte_address():
     assert rc == g.GEMM_ERR_ALIGNMENT
 
 
-def test_smallk_random_within_bound():
-    A, B = gi.bf16_operands(1000, 777, 16, seed=41)
-    D = run(A, B, g.VARIANT_SMALLK)
-    D_ref, S = ref(A, B)
+@pytest.mark.parametrize("v", ["smallk", "smallk_tc"])
+@pytest.mark.parametrize("K", [3, 8, 13, 16])
+def test_smallk_random_within_bound(v, K):
+    A0, B0 = gi.bf16_operands(1000, 777, K, seed=41 + K)
+    lda = (K + 7) // 8 * 8   # a pitch of whole 16-byte lines, NaN past K
+    A = torch.full((1000, lda), float("nan"), dtype=torch.bfloat16)
+    B = torch.full((777, lda), float("nan"), dtype=torch.bfloat16)
+    A[:, :K], B[:, :K] = A0, B0
+    D = run(A, B, SMALLK_VARIANTS[v], K=K)
+    D_ref, S = ref(A, B, K)
     P.check_within_bound(P.bf16_to_f64(D), D_ref, S, "smallk random")
 
 
-def test_smallk_nonfinite():
+@pytest.mark.parametrize("v", ["smallk", "smallk_tc"])
+def test_smallk_nonfinite(v):
     M, N, K = 64, 300, 8
     A = torch.ones(M, K, dtype=torch.bfloat16)
     B = torch.ones(N, K, dtype=torch.bfloat16)
     A[3, 2] = float("nan")
     A[7, 0] = float("inf")
     B[11, 0] = 0.0                          # inf * 0 = NaN at (7, 11)
-    D = run(A, B, g.VARIANT_SMALLK).float()
+    D = run(A, B, SMALLK_VARIANTS[v]).float()
     assert torch.isnan(D[3]).all()
     assert torch.isnan(D[7, 11]) and torch.isinf(D[7, 12]) and D[7, 12] > 0
     others = torch.ones(M, dtype=torch.bool)
