@@ -615,6 +615,21 @@ def run_ours(args, rank, world, local):
     if per_launch:
         kern_ms = [statistics.fmean(s.elapsed_time(e) for s, e in zip(starts[j], ends[j]))
                    for j in range(len(probs))]
+    # The same events around a one-element fill after the same flush: the floor
+    # this protocol puts under any launch (context for the small workloads).
+    event_floor_us = None
+    if any(flush_each):
+        tiny = torch.zeros(1, device=device)
+        floor = []
+        for _ in range(20):
+            flush_buf.zero_()
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            tiny.zero_()
+            a1.record(stream)
+            a1.synchronize()
+            floor.append(a0.elapsed_time(a1))
+        event_floor_us = 1e3 * statistics.median(floor)
     if any(flush_each):
         elapsed_ms = max_over_ranks(args.steps * sum(kern_ms), world)
     else:
@@ -753,6 +768,7 @@ def run_ours(args, rank, world, local):
                        "l2": ("512 MiB write before each launch of a workload whose inputs fit "
                               "in L2; its kernels' event time only" if any(flush_each)
                               else "operands larger than L2, no flush"),
+                       "event_floor_us": event_floor_us,
                        "parallelism": f"replicas x{world} (no data-path collective)"},
             "roofline": roof,
             "kernels": kernels,

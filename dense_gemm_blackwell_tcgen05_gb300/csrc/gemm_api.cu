@@ -337,10 +337,16 @@ static int bf16_impl(int variant, const void* A, const void* B, void* D, int64_t
     if ((rc = bf16_streamk_split_tiles(cg, p, ctx, &sk_tiles)) != GEMM_OK) return rc;
     if (sk_tiles != 0) tma_store = false;
   }
-  // Small K is a write of D: the CUDA-core kernel unless the call needs the
-  // persistent kernel's extras (an epilogue, a stream-K workspace).
-  if (base == GEMM_VARIANT_AUTO && K <= smallk_max_k() && p.epi_mode == 0 && ws == nullptr)
+  // Small K is a write of D: a small-K kernel unless the call needs the
+  // persistent kernel's extras (an epilogue, a stream-K workspace).  The
+  // tensor-core one writes D faster (3.2-3.6 TB/s against 2.5-2.7 at K = 8)
+  // but costs about 6 us more to get going, so it takes outputs of 48 MB and
+  // more (measured crossover about 46 MB).
+  if (base == GEMM_VARIANT_AUTO && K <= smallk_max_k() && p.epi_mode == 0 && ws == nullptr) {
+    if (static_cast<uint64_t>(M) * static_cast<uint64_t>(N) * 2 >= (48ull << 20))
+      return launch_bf16_smallk_tc(p, ctx, stream);
     return launch_bf16_smallk(p, ctx.num_sms, stream);
+  }
   switch (base) {
     case GEMM_VARIANT_SMALLK:
       return launch_bf16_smallk(p, ctx.num_sms, stream);

@@ -83,8 +83,8 @@ typedef enum {
                                    128x256 tile (operands loaded at their real K,
                                    rows grouped by residue mod 8 so that every
                                    store is an aligned 16-byte one); AUTO picks
-                                   one of the two small-K kernels for plain
-                                   calls with K <= 16                              */
+                                   for plain calls with K <= 16 the CUDA-core
+                                   kernel below 48 MB of output, this one above  */
   GEMM_VARIANT_DIRECT_STORE = 0x100  /* flag: masked st.global epilogue instead of
                                         TMA stores, even when D is aligned.  Without
                                         it the library picks: TMA stores where D is

@@ -341,6 +341,24 @@ def test_smallk_any_row_alignment(v, M, N, K, ldd, offset):
     assert_bitwise(D[:, :N], D_ref)
 
 
+@pytest.mark.slow
+def test_smallk_auto_large_output():
+    """K = 8 with a 52 MB output: the automatic choice takes the tensor-core
+    small-K kernel; bitwise on small integers, odd pitch, padding untouched."""
+    M, N, K, ldd = 8192, 3199, 8, 3201
+    gen = torch.Generator().manual_seed(5)
+    A = torch.randint(-4, 5, (M, K), generator=gen).to(torch.bfloat16)
+    B = torch.randint(-4, 5, (N, K), generator=gen).to(torch.bfloat16)
+    Ad, Bd = A.cuda(), B.cuda()
+    D = torch.full((M, ldd), float("nan"), dtype=torch.bfloat16, device="cuda")
+    rc = g.gemm_bf16(Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), M, N, K, K, K, ldd, 0)
+    assert rc == g.GEMM_OK and g.gemm_last_status(0) == g.GEMM_OK
+    D = D.cpu()
+    assert torch.isnan(D[:, N:].float()).all()
+    D_ref, _ = ref(A, B, K)
+    assert_bitwise(D[:, :N], D_ref)
+
+
 def test_smallk_rejects_an_odd_byte_address():
     A = torch.zeros(8, 8, dtype=torch.bfloat16, device="cuda")
     buf = torch.zeros(100, dtype=torch.uint8, device="cuda")
