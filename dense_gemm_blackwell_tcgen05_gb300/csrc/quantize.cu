@@ -28,13 +28,14 @@ struct QuantArgs {
   uint64_t ldx, ldq, ldsf;
   uint32_t units_per_row;   // ceil(K / kUnit)
   bool vec_in, vec_out;     // 16-byte loads / 4-byte stores are aligned everywhere
-  bool tiled;               // SF in the tiled layout (ldsf unused)
-  uint32_t groups;          // tiled: ceil(nblk / 4) block groups per row block
+  uint32_t groups;          // tiled layout: ceil(nblk / 4) block groups per row block
 };
 
-// Byte offset of the scale of (row, block b) in the SF buffer.
+// Byte offset of the scale of (row, block b) in the SF buffer: row-major
+// with pitch ldsf, or the tiled layout (ldsf unused).
+template <bool TILED>
 __device__ __forceinline__ uint64_t sf_offset(const QuantArgs& a, uint32_t row, uint32_t b) {
-  if (!a.tiled) return static_cast<uint64_t>(row) * a.ldsf + b;
+  if constexpr (!TILED) return static_cast<uint64_t>(row) * a.ldsf + b;
   return 512ull * (static_cast<uint64_t>(row / 128) * a.groups + b / 4) + 16 * (row % 32) +
          4 * ((row % 128) / 32) + b % 4;
 }
@@ -65,6 +66,7 @@ __device__ __forceinline__ uint32_t encode_one(float x, float scale) {
   return e4m3x2(x * scale, 0.0f) & 0xFFu;
 }
 
+template <bool TILED>
 __global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const QuantArgs a) {
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -101,7 +103,7 @@ __global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const QuantArgs a) 
       m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
       if (kb >= a.K) {   // whole block past K (all lanes took part in the shuffles)
         // tiled layout: the last group's blocks past K hold zero
-        if (a.tiled && (lane & 7u) == 0 && kb / 32 < 4 * a.groups) a.SF[sf_offset(a, row, kb / 32)] = 0;
+        if (TILED && (lane & 7u) == 0 && kb / 32 < 4 * a.groups) a.SF[sf_offset<TILED>(a, row, kb / 32)] = 0;
         continue;
       }
       const int e = scale_exponent(m);
@@ -118,16 +120,16 @@ __global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const QuantArgs a) 
         for (uint32_t t = 0; t < 4; ++t)
           if (k + t < a.K) qr[k + t] = static_cast<uint8_t>(q >> (8 * t));
       }
-      if ((lane & 7u) == 0) a.SF[sf_offset(a, row, kb / 32)] = static_cast<uint8_t>(e + 127);
+      if ((lane & 7u) == 0) a.SF[sf_offset<TILED>(a, row, kb / 32)] = static_cast<uint8_t>(e + 127);
     }
   }
-  if (a.tiled) {
+  if constexpr (TILED) {
     // rows past the last real row of the last row block: zero scales
     const uint32_t pad_rows = (a.rows + 127) / 128 * 128 - a.rows;
     const uint64_t pad = static_cast<uint64_t>(pad_rows) * 4 * a.groups;
     for (uint64_t i = blockIdx.x * blockDim.x + threadIdx.x; i < pad; i += gridDim.x * blockDim.x)
-      a.SF[sf_offset(a, a.rows + static_cast<uint32_t>(i / (4 * a.groups)),
-                     static_cast<uint32_t>(i % (4 * a.groups)))] = 0;
+      a.SF[sf_offset<TILED>(a, a.rows + static_cast<uint32_t>(i / (4 * a.groups)),
+                            static_cast<uint32_t>(i % (4 * a.groups)))] = 0;
   }
 }
 
@@ -146,7 +148,6 @@ int launch_mxfp8_quantize(const float* X, uint32_t rows, uint32_t K, uint64_t ld
   a.ldq = ldq;
   a.ldsf = ldsf;
   a.units_per_row = (K + kUnit - 1) / kUnit;
-  a.tiled = tiled;
   a.groups = ((K + 31) / 32 + 3) / 4;
   a.vec_in = (reinterpret_cast<uintptr_t>(X) & 15u) == 0 && (ldx % 4) == 0;
   a.vec_out = (reinterpret_cast<uintptr_t>(Q) & 3u) == 0 && (ldq % 4) == 0;
@@ -154,7 +155,10 @@ int launch_mxfp8_quantize(const float* X, uint32_t rows, uint32_t K, uint64_t ld
   const uint64_t want = (units + 7) / 8;                      // 8 warps per block
   const uint64_t cap = static_cast<uint64_t>(num_sms) * 8;    // 8 blocks (64 warps) per SM
   const unsigned blocks = static_cast<unsigned>(want < cap ? want : cap);
-  mxfp8_quantize_kernel<<<blocks, 256, 0, stream>>>(a);
+  if (tiled)
+    mxfp8_quantize_kernel<true><<<blocks, 256, 0, stream>>>(a);
+  else
+    mxfp8_quantize_kernel<false><<<blocks, 256, 0, stream>>>(a);
   if (const cudaError_t e = cudaGetLastError(); e != cudaSuccess) {
     note_cuda_error(e);
     return GEMM_ERR_LAUNCH;
