@@ -883,9 +883,9 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
   } else if (C::SF_TILED && warp == C::kCpWarp) {
     // ==================== scale copies: one thread of the leader CTA ==============
     // For each K-tile, once its stage has landed and the MMAs of the K-tile
-    // two back (which read the same scale set) have completed, copy its scale
-    // chunks from the stage into scale set it % 2 and commit to that set's
-    // barrier.  tcgen05 operations of different threads are ordered only
+    // SF_SETS back (which read the same scale set) have completed, copy its
+    // scale chunks from the stage into scale set it % SF_SETS and commit to
+    // that set's barrier.  tcgen05 operations of different threads are ordered only
     // through these commits and barrier waits.
     if (leader && lane == 0) {
       uint32_t it = 0;
