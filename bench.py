@@ -630,6 +630,29 @@ def run_ours(args, rank, world, local):
             a1.synchronize()
             floor.append(a0.elapsed_time(a1))
         event_floor_us = 1e3 * statistics.median(floor)
+    # Context for the same workloads, outside the timed region: the mean time
+    # per launch of 1000 back-to-back launches with no flush between them (the
+    # operands stay in L2), the figure a caller sees in a loop of small GEMMs.
+    back_to_back_us = None
+    if any(flush_each):
+        back_to_back_us = {}
+        for j, p in enumerate(probs):
+            if not flush_each[j]:
+                continue
+            for _ in range(3):
+                p.launch(sh)
+            b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            b0.record(stream)
+            for _ in range(1000):
+                rc = p.launch(sh)
+                if rc != g.GEMM_OK:
+                    raise g.GemmError(rc, p.w.name)
+            b1.record(stream)
+            b1.synchronize()
+            back_to_back_us[p.w.name] = 1e3 * b0.elapsed_time(b1) / 1000
+        st = g.gemm_last_status(sh)
+        if st != g.GEMM_OK:
+            raise g.GemmError(st, "back-to-back launches")
     if any(flush_each):
         elapsed_ms = max_over_ranks(args.steps * sum(kern_ms), world)
     else:
@@ -769,6 +792,7 @@ def run_ours(args, rank, world, local):
                               "in L2; its kernels' event time only" if any(flush_each)
                               else "operands larger than L2, no flush"),
                        "event_floor_us": event_floor_us,
+                       "back_to_back_us": back_to_back_us,
                        "parallelism": f"replicas x{world} (no data-path collective)"},
             "roofline": roof,
             "kernels": kernels,

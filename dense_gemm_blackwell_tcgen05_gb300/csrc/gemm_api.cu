@@ -34,10 +34,11 @@ DeviceState g_devices[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::atomic<int64_t> g_watchdog_ms{-1};
 std::atomic<int> g_streamk_mode{kStreamKAuto};
+std::atomic<int> g_tail_split{1};
 std::atomic<uint32_t> g_streamk_epoch{0};
 thread_local int t_last_cuda_error = 0;
 thread_local int64_t t_stall_next = -1;   // one-shot watchdog test hook
-thread_local int64_t t_schedule[5] = {0, 0, 0, 0, 0};
+thread_local int64_t t_schedule[6] = {0, 0, 0, 0, 0, 0};
 
 // Consumes the calling thread's pending stall request, if any.
 uint32_t take_stall() {
@@ -209,6 +210,14 @@ void note_cuda_error(cudaError_t e) { t_last_cuda_error = static_cast<int>(e); }
 
 int streamk_mode() { return g_streamk_mode.load(); }
 
+uint32_t plan_tail_split(uint64_t tiles, uint64_t resident) {
+  if (g_tail_split.load() == 0 || tiles == 0 || resident == 0) return 0;
+  // the tiles of the last round (all of them when there are fewer tiles than
+  // clusters): cut in halves when the halves still fit in one round
+  const uint64_t r = tiles % resident;
+  return r != 0 && 2 * r <= resident ? static_cast<uint32_t>(r) : 0u;
+}
+
 uint32_t next_streamk_epoch() {
   uint32_t e = g_streamk_epoch.fetch_add(1) + 1;
   if (e == 0) e = g_streamk_epoch.fetch_add(1) + 1;   // 0 means "no partial yet"
@@ -216,12 +225,13 @@ uint32_t next_streamk_epoch() {
 }
 
 void note_schedule(uint32_t clusters, uint32_t cg, uint32_t dp_tiles, uint32_t sk_tiles,
-                   uint32_t sk_unit) {
+                   uint32_t sk_unit, uint32_t half_tiles) {
   t_schedule[0] = clusters;
   t_schedule[1] = cg;
   t_schedule[2] = dp_tiles;
   t_schedule[3] = sk_tiles;
   t_schedule[4] = sk_unit;
+  t_schedule[5] = half_tiles;
 }
 
 namespace {
@@ -608,6 +618,17 @@ int gemm_set_streamk_mode(int mode) {
   return g_streamk_mode.exchange(mode);
 }
 
+int gemm_set_tail_split(int enable) {
+  if (enable != 0 && enable != 1) return GEMM_ERR_INVALID_ARG;
+  return g_tail_split.exchange(enable);
+}
+
+int64_t gemm_tail_split_plan(int64_t tiles, int64_t resident) {
+  if (tiles < 0 || resident < 0 || tiles > 0xFFFFFFFFll || resident > 0xFFFFFFFFll)
+    return GEMM_ERR_INVALID_ARG;
+  return plan_tail_split(static_cast<uint64_t>(tiles), static_cast<uint64_t>(resident));
+}
+
 int gemm_streamk_plan(int64_t tiles, int64_t resident, int64_t k_tiles, int64_t unit, int mode,
                       int64_t* out) {
   if (out == nullptr || tiles < 0 || resident < 1 || k_tiles < 0 || unit < 1 ||
@@ -630,7 +651,7 @@ int gemm_streamk_plan(int64_t tiles, int64_t resident, int64_t k_tiles, int64_t 
 
 int gemm_last_schedule(int64_t* out) {
   if (out == nullptr) return GEMM_ERR_INVALID_ARG;
-  for (int i = 0; i < 5; ++i) out[i] = t_schedule[i];
+  for (int i = 0; i < 6; ++i) out[i] = t_schedule[i];
   return GEMM_OK;
 }
 

@@ -51,6 +51,12 @@ struct StreamKPlan {
 enum StreamKMode { kStreamKAuto = 0, kStreamKAlways = 1, kStreamKNever = 2 };
 int streamk_mode();
 
+// Tail split of the data-parallel schedule: how many of `tiles` whole tiles
+// (the last ones) to cut into two column halves over `resident` clusters --
+// the tiles of the last, partial round, when their halves fit in one round
+// (0 when switched off with gemm_set_tail_split).
+uint32_t plan_tail_split(uint64_t tiles, uint64_t resident);
+
 // The flag value of the next split launch: one process-wide sequence shared by
 // every kernel configuration, never 0.  A flag word left behind by a launch
 // that gave up (watchdog timeout) holds an earlier launch's value, which no
@@ -111,13 +117,14 @@ struct Maps {
   CUtensorMap D;
   CUtensorMap SFA;
   CUtensorMap SFB;
+  CUtensorMap Bh;   // B with a half-height box, for column-half work items
 };
 
 // Records the CUDA error behind a GEMM_ERR_LAUNCH for gemm_last_cuda_error().
 void note_cuda_error(cudaError_t e);
 // Records the calling thread's last persistent-kernel schedule (gemm_last_schedule).
 void note_schedule(uint32_t clusters, uint32_t cg, uint32_t dp_tiles, uint32_t sk_tiles,
-                   uint32_t sk_unit);
+                   uint32_t sk_unit, uint32_t half_tiles);
 
 // Encodes a 2-D tiled tensor map (rows of `inner` elements, pitch in bytes).
 // Returns false when the driver rejects it.

@@ -51,6 +51,11 @@ struct GemmArgs {
   uint32_t dp_tiles;
   uint32_t sk_tiles;
   uint32_t sk_unit;
+  // Tail split (data-parallel schedule only): the last half_tiles of the
+  // dp_tiles whole tiles are cut into two column halves of UMMA_N / 2, each
+  // a work item of its own, so a last round that would leave most clusters
+  // idle takes about half a tile's time.
+  uint32_t half_tiles;
   float* ws_part;             // stream-K partial accumulators, one slot per cluster
   uint32_t* ws_flag;          // per (slot, CTA, epilogue warp) ready flags
   uint32_t epoch;             // this launch's flag value (never 0)
@@ -72,9 +77,20 @@ struct GemmArgs {
 //   kind 0: the whole tile;  1: the first K-range of a split tile (this
 //   cluster owns it: adds the later ranges' partials and stores D);
 //   2: a later K-range (partial accumulator goes to this cluster's slot).
+//   half 0: all UMMA_N columns of the tile; 1 / 2: its first / second
+//   column half (tail split, kind 0 only).
 struct WorkItem {
-  uint32_t tile, k_begin, k_end, kind;
+  uint32_t tile, k_begin, k_end, kind, half;
 };
+
+// First column of D and number of columns that work item w covers in its
+// tile's column block nb.
+__device__ __forceinline__ uint32_t item_n0(const WorkItem& w, uint32_t nb, uint32_t umma_n) {
+  return nb * umma_n + (w.half == 2u ? umma_n / 2 : 0u);
+}
+__device__ __forceinline__ uint32_t item_cols(const WorkItem& w, uint32_t umma_n) {
+  return w.half != 0u ? umma_n / 2 : umma_n;
+}
 
 __device__ __forceinline__ uint64_t sk_bound(uint64_t units, uint32_t c, uint32_t G) {
   return units * c / G;
@@ -85,9 +101,20 @@ __device__ __forceinline__ uint64_t sk_bound(uint64_t units, uint32_t c, uint32_
 // walk the same sequence.
 __device__ __forceinline__ bool work_item(const GemmArgs& a, uint32_t c, uint32_t G, uint32_t KT,
                                           uint32_t wi, WorkItem& w) {
-  const uint32_t n_dp = a.dp_tiles > c ? (a.dp_tiles - c + G - 1) / G : 0u;
+  // data-parallel items: the whole tiles, then two halves of each of the
+  // last half_tiles tiles
+  const uint32_t n_items = a.dp_tiles + a.half_tiles;
+  const uint32_t n_dp = n_items > c ? (n_items - c + G - 1) / G : 0u;
   if (wi < n_dp) {
-    w.tile = c + wi * G;
+    const uint32_t x = c + wi * G;
+    const uint32_t whole = a.dp_tiles - a.half_tiles;
+    if (x < whole) {
+      w.tile = x;
+      w.half = 0;
+    } else {
+      w.tile = whole + (x - whole) / 2u;
+      w.half = 1u + ((x - whole) & 1u);
+    }
     w.k_begin = 0;
     w.k_end = KT;
     w.kind = 0;
@@ -105,6 +132,7 @@ __device__ __forceinline__ bool work_item(const GemmArgs& a, uint32_t c, uint32_
   const uint32_t ub = static_cast<uint32_t>(start - ts * KU);
   const uint32_t ue = static_cast<uint32_t>(end - ts * KU);
   w.tile = a.dp_tiles + static_cast<uint32_t>(ts);
+  w.half = 0;
   w.k_begin = ub * a.sk_unit;
   w.k_end = min(KT, ue * a.sk_unit);
   w.kind = (ub == 0 && ue == KU) ? 0u : (ub == 0 ? 1u : 2u);
@@ -650,7 +678,8 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
     gemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD,
                    const __grid_constant__ CUtensorMap tmSFA,
-                   const __grid_constant__ CUtensorMap tmSFB, const GemmArgs args) {
+                   const __grid_constant__ CUtensorMap tmSFB,
+                   const __grid_constant__ CUtensorMap tmBh, const GemmArgs args) {
   using C = GemmCfg<CG, KIND, TMA_STORE, EPI2>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -712,6 +741,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (args.half_tiles != 0) tma_prefetch_desc(&tmBh);
     if constexpr (TMA_STORE) tma_prefetch_desc(&tmD);
     if (C::MX && !args.sf_gather) {
       tma_prefetch_desc(&tmSFA);
@@ -741,7 +771,12 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
         uint32_t mb, nb;
         tile_coords(w.tile, args.num_m_blocks, args.num_n_blocks, args.group_m, mb, nb);
         const int32_t a_row = static_cast<int32_t>(mb * C::UMMA_M + rank * C::BLOCK_M);
-        const int32_t b_row = static_cast<int32_t>(nb * C::UMMA_N + rank * C::B_ROWS);
+        // this CTA's share of the item's B rows: B_ROWS, or half of them
+        // for a column half (through the half-height box of tmBh)
+        const uint32_t n0 = item_n0(w, nb, C::UMMA_N);
+        const int32_t b_row = static_cast<int32_t>(n0 + rank * (item_cols(w, C::UMMA_N) / CG));
+        const CUtensorMap* const mapB = w.half != 0 ? &tmBh : &tmB;
+        const uint32_t tx = w.half != 0 ? C::AB_TX - C::B_BYTES / 2 : C::AB_TX;
         for (uint32_t kt = w.k_begin; kt < w.k_end; ++kt, ++it) {
           const uint32_t s = it % C::STAGES;
           const uint32_t round = it / C::STAGES;
@@ -757,11 +792,11 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
           // (row block * KT + kt) * 32 of the 16-byte-row view; this CTA's A
           // row block, then the tile's B row blocks.
           const int32_t sfa_y = static_cast<int32_t>(((static_cast<uint32_t>(a_row) / 128u) * KT + kt) * 32u);
-          const uint32_t sfb_blk = (nb * C::UMMA_N) / 128u;
+          const uint32_t sfb_blk = n0 / 128u;
           if constexpr (CG == 1) {
-            mbar_arrive_expect_tx(full_bar(s), C::AB_TX);
+            mbar_arrive_expect_tx(full_bar(s), tx);
             tma_load_2d(sb, &tmA, full_bar(s), kx, a_row, pol);
-            tma_load_2d(sb + C::OFF_B, &tmB, full_bar(s), kx, b_row, pol);
+            tma_load_2d(sb + C::OFF_B, mapB, full_bar(s), kx, b_row, pol);
             if constexpr (C::SF_TILED) {
               tma_load_2d(sb + C::OFF_SF, &tmSFA, full_bar(s), 0, sfa_y, pol);
 #pragma unroll
@@ -772,9 +807,9 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
           } else {
             // both CTAs' operand bytes land on the leader's ready barrier
             const uint32_t leader_full = mapa_shared(full_bar(s), 0);
-            if (leader) mbar_arrive_expect_tx(full_bar(s), CG * C::AB_TX);
+            if (leader) mbar_arrive_expect_tx(full_bar(s), CG * tx);
             tma_load_2d_pair(sb, &tmA, leader_full, kx, a_row, pol);
-            tma_load_2d_pair(sb + C::OFF_B, &tmB, leader_full, kx, b_row, pol);
+            tma_load_2d_pair(sb + C::OFF_B, mapB, leader_full, kx, b_row, pol);
             if constexpr (C::SF_TILED) {
               tma_load_2d_pair(sb + C::OFF_SF, &tmSFA, leader_full, 0, sfa_y, pol);
 #pragma unroll
@@ -809,6 +844,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
         if (!wait_bounded(acce_bar(b), (around & 1u) ^ 1u, wd, kSiteMmaAccEmpty)) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + b * C::UMMA_N;
+        const uint32_t n_mma = item_cols(w, C::UMMA_N);   // N of this item's MMAs
         bool ok = true;
         // Unrolled in the pair kernels (measured: +1-3% bf16 with 4, +2.4% MXFP8 with 2;
         // the one-CTA MXFP8 kernel measured slightly slower unrolled).
@@ -852,10 +888,10 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
             }
 #pragma unroll
             for (uint32_t k = 0; k < C::K_STEPS; ++k)
-              mma_mxf8<CG>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc_mxf8(C::UMMA_M, C::UMMA_N, k, k),
+              mma_mxf8<CG>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc_mxf8(C::UMMA_M, n_mma, k, k),
                            sfa_t, sfb_t, (kt != w.k_begin || k != 0u));
           } else {
-            constexpr uint32_t idesc = idesc_bf16(C::UMMA_M, C::UMMA_N);
+            const uint32_t idesc = idesc_bf16(C::UMMA_M, n_mma);
 #pragma unroll
             for (uint32_t k = 0; k < C::K_STEPS; ++k)
               mma_bf16<CG>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kt != w.k_begin || k != 0u));
@@ -1030,7 +1066,6 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
     const uint32_t eg = warp < 6 ? 0u : 1u;  // epilogue group: the chunks c with c % NG == eg
     const uint32_t q = warp & 3u;            // TMEM lanes 32q .. 32q+31
     const uint32_t ew = eg == 0 ? warp - 2u : 4u + warp - C::kEpiWg1Warp;   // staging slot owner
-    constexpr uint32_t NCH = C::UMMA_N / 32;
     uint32_t j = 0, chunk_ctr = 0;
     bool ok = true;
     // the 32 x UMMA_N fp32 slice of a stream-K partial slot for this lane
@@ -1088,10 +1123,11 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
       uint32_t mb, nb;
       tile_coords(w.tile, args.num_m_blocks, args.num_n_blocks, args.group_m, mb, nb);
       const uint32_t row0 = mb * C::UMMA_M + rank * C::BLOCK_M + q * 32;
-      const uint32_t col_base = nb * C::UMMA_N;
+      const uint32_t col_base = item_n0(w, nb, C::UMMA_N);
       const uint32_t t_addr = tmem_base + ((q * 32u) << 16) + b * C::UMMA_N;
-      // 32-column chunks of this tile inside N
-      const uint32_t live = min(NCH, (args.N - col_base + 31u) / 32u);
+      // 32-column chunks of this item inside N (none for a column half past N)
+      const uint32_t item_nch = item_cols(w, C::UMMA_N) / 32u;
+      const uint32_t live = col_base < args.N ? min(item_nch, (args.N - col_base + 31u) / 32u) : 0u;
       if constexpr (C::SF_TILED) {
         // One accumulator, handed back early: this group's 128 columns go to
         // registers as packed bf16 (4 chunks of 32, 64 words), the issuer is
@@ -1196,7 +1232,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
         if constexpr (TMA_STORE && C::TS_COLS == 32) {
           // 32-column chunks: one tcgen05.ld, one 32x32 box per chunk
 #pragma unroll 1
-          for (uint32_t c = 0; c < C::UMMA_N / 32; ++c) {
+          for (uint32_t c = 0; c < item_nch; ++c) {
             if (col_base + c * 32 >= args.N) break;
             uint32_t v[32];
             tmem_ld_32x32b_x32(t_addr + c * 32, v);
@@ -1226,7 +1262,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
           }
         } else if constexpr (TMA_STORE) {
 #pragma unroll 1
-          for (uint32_t c = 0; c < C::UMMA_N / 64; ++c) {
+          for (uint32_t c = 0; c < item_nch / 2; ++c) {
             if (col_base + c * 64 >= args.N) break;
             uint32_t v0[32], v1[32];
             tmem_ld_32x32b_x32(t_addr + c * 64, v0);

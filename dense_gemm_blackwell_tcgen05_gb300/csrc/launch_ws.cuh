@@ -180,6 +180,21 @@ int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) 
       a.epoch = next_streamk_epoch();
     }
   }
+  // Tail split: a data-parallel launch cuts the tiles of a last, partial round
+  // into column halves when those fit in one round (not in the kernels whose
+  // scale-factor warp loads B scales by whole tiles).
+  a.half_tiles = 0;
+  if constexpr (!C::SF_WARP) {
+    if (a.sk_tiles == 0) {
+      a.half_tiles = plan_tail_split(tiles, resident);
+      const uint64_t items = tiles + a.half_tiles;
+      clusters = items < resident ? items : resident;
+    }
+  }
+  if (a.half_tiles != 0 &&
+      !encode_map_2d(&maps.Bh, dt, p.B, p.K, p.N, p.ldb * C::ELEM, C::BK, C::B_ROWS / 2,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+    return GEMM_ERR_LAUNCH;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
@@ -196,8 +211,9 @@ int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) 
   } else {
     cfg.gridDim = dim3(static_cast<unsigned>(clusters));
   }
-  note_schedule(static_cast<uint32_t>(clusters), CG, a.dp_tiles, a.sk_tiles, a.sk_unit);
-  const cudaError_t err = cudaLaunchKernelEx(&cfg, kern, maps.A, maps.B, maps.D, maps.SFA, maps.SFB, a);
+  note_schedule(static_cast<uint32_t>(clusters), CG, a.dp_tiles, a.sk_tiles, a.sk_unit, a.half_tiles);
+  const cudaError_t err =
+      cudaLaunchKernelEx(&cfg, kern, maps.A, maps.B, maps.D, maps.SFA, maps.SFB, maps.Bh, a);
   if (err != cudaSuccess) {
     note_cuda_error(err);
     cudaGetLastError();

@@ -337,10 +337,31 @@ int gemm_last_cuda_error(void);
 
 /* Schedule of the calling thread's most recent persistent-kernel launch
  * (diagnostic, no counterpart on the pages): out[0] clusters launched,
- * out[1] CTAs per cluster, out[2] tiles computed whole, out[3] tiles split
- * along K by the stream-K schedule, out[4] K-tiles per stream-K unit.  `out`
- * holds 5 values.  Returns GEMM_OK, or GEMM_ERR_INVALID_ARG for NULL. */
+ * out[1] CTAs per cluster, out[2] tiles computed whole (column halves
+ * included), out[3] tiles split along K by the stream-K schedule, out[4]
+ * K-tiles per stream-K unit, out[5] tiles of the last round cut into two
+ * column halves (the tail split below).  `out` holds 6 values.  Returns
+ * GEMM_OK, or GEMM_ERR_INVALID_ARG for NULL. */
 int gemm_last_schedule(int64_t* out);
+
+/* Tail split of the data-parallel schedule (b200-gemm-optimization-ladder,
+ * level 6, "check the tail and tile order").  With T output tiles over G
+ * co-resident clusters, the last round holds r = T mod G tiles (all T when
+ * T < G) and would leave G - r clusters idle for a whole tile's time.  When
+ * 2r <= G, the persistent kernels (bf16, and MXFP8 with tiled scales) cut
+ * those r tiles into two halves of UMMA_N / 2 columns each, which run as
+ * separate work items with N = UMMA_N / 2 MMAs: the round then takes about
+ * half a tile's time.  The halves cover disjoint columns of D, so nothing is
+ * summed across them and each element is computed exactly as in the whole
+ * tile.  Not applied to stream-K launches that split tiles along K, nor to
+ * the MXFP8 kernels with row-major scales.
+ * gemm_set_tail_split(1) (the default) enables it process-wide, 0 disables
+ * it; returns the previous setting, or GEMM_ERR_INVALID_ARG for another
+ * value.  gemm_tail_split_plan returns the number of tiles the launchers cut
+ * for `tiles` tiles over `resident` clusters under the current setting
+ * (host only), or GEMM_ERR_INVALID_ARG for negative or > 2^32 - 1 inputs. */
+int gemm_set_tail_split(int enable);
+int64_t gemm_tail_split_plan(int64_t tiles, int64_t resident);
 
 /* Test hook for the device watchdog (no counterpart on the pages: it exists to
  * exercise the failure path without faulting a GPU).  The calling thread's NEXT

@@ -164,7 +164,8 @@ def test_streamk_validation_without_device():
     assert g.gemm_bf16_streamk(0x40, FAKE, FAKE, FAKE, 4, 4, 16, 16, 16, 4, FAKE, 1 << 20, 0) == \
         g.GEMM_ERR_INVALID_ARG
     sched = g.gemm_last_schedule()
-    assert set(sched) == {"clusters", "ctas_per_cluster", "dp_tiles", "sk_tiles", "sk_unit"}
+    assert set(sched) == {"clusters", "ctas_per_cluster", "dp_tiles", "sk_tiles", "sk_unit",
+                          "half_tiles"}
 
 
 def test_streamk_workspace_query_without_device():

@@ -302,7 +302,11 @@ def test_never_mode_is_data_parallel():
     g.gemm_set_streamk_mode(g.STREAMK_NEVER)
     A, B = int_bf16(1024, 1024, 4096, seed=4, lo=-1, hi=2)
     (_,), sched = run_bf16(A, B, g.VARIANT_1CTA)
-    assert sched["sk_tiles"] == 0 and sched["clusters"] == 32
+    # 32 tiles: one partial round, cut into 64 column halves by the tail split
+    assert sched["sk_tiles"] == 0 and sched["dp_tiles"] == 32
+    assert sched["clusters"] == 32 + sched["half_tiles"]
+    assert sched["half_tiles"] == g.gemm_tail_split_plan(
+        32, torch.cuda.get_device_properties(0).multi_processor_count)
 
 
 # ------------------------------------------------------------ argument errors
