@@ -105,10 +105,16 @@ def stored_traffic(kernel_key: str):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    """nvidia-smi clock / throttle-reason samples while the timed region runs,
+    every 20 ms.  A sample counts as under load when the board draws at least
+    30% of its power limit; sm_mhz is the median over those (over all samples
+    when there are none).  A timed region of a few
+    tens of milliseconds holds few samples, and samples between kernels show
+    the idle boost clock, so the count is reported too."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+             "power.limit")
 
     def __init__(self, index: int):
         self.index = index
@@ -119,7 +125,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (FileNotFoundError, OSError):
             self.proc = None
@@ -133,18 +139,29 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        rows = [r for r in csv.reader(io.StringIO(out)) if len(r) >= 9]
+        rows = [r for r in csv.reader(io.StringIO(out)) if len(r) >= 10]
         if not rows:
             return None
-        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        pairs = [(num(r[1]), num(r[3]), num(r[9])) for r in rows]
+        sm = [c for c, _, _ in pairs if c is not None]
+        mx = [v for v in (num(r[2]) for r in rows) if v is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
-        power = [float(r[3]) for r in rows if r[3].strip().replace(".", "").isdigit()]
-        return {"sm_mhz": statistics.median(sm) if sm else None,
+        power = [w for _, w, _ in pairs if w is not None]
+        pmax = max(power) if power else None
+        loaded = [c for c, w, lim in pairs
+                  if c is not None and w is not None and lim is not None and w >= 0.3 * lim]
+        return {"sm_mhz": statistics.median(loaded or sm) if sm else None,
+                "sm_mhz_all_samples": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows),
-                "power_w_max": max(power) if power else None}
+                "reasons": reasons, "active_masks": sorted({r[4].strip() for r in rows}),
+                "samples": len(rows), "samples_under_load": len(loaded),
+                "power_w_max": pmax}
 
 
 def tensor_peak_choice(region_s: float, clk) -> tuple[str, str]:

@@ -50,3 +50,40 @@ def test_tensor_peak_choice():
     assert bench.tensor_peak_choice(5.0, {"reasons": []})[0] == "burst"
     assert bench.tensor_peak_choice(5.0, None)[0] == "burst"
     assert bench.tensor_peak_choice(1.2, capped)[0] == "sustained"
+
+
+def test_clock_sampler_takes_the_median_under_load():
+    # nvidia-smi rows as the sampler queries them: index, clocks.sm, clocks.max.sm,
+    # power.draw, reasons.active, hw_slowdown, hw_thermal, sw_thermal, sw_power_cap,
+    # power.limit.  Idle samples (boost clock, low power) sit around the loaded ones.
+    rows = [
+        "0, 2070, 2070, 180.5, 0x0, Not Active, Not Active, Not Active, Not Active, 1400.00",
+        "0, 1665, 2070, 1210.0, 0x0, Not Active, Not Active, Not Active, Not Active, 1400.00",
+        "0, 1650, 2070, 1302.4, 0x4, Not Active, Not Active, Not Active, Active, 1400.00",
+        "0, 1680, 2070, 1190.2, 0x0, Not Active, Not Active, Not Active, Not Active, 1400.00",
+        "0, 2070, 2070, 175.0, 0x0, Not Active, Not Active, Not Active, Not Active, 1400.00",
+        "garbage line",
+    ]
+
+    class FakeProc:
+        def terminate(self):
+            pass
+
+        def communicate(self, timeout=None):
+            return "\n".join(rows) + "\n", ""
+
+    s = bench.ClockSampler(0)
+    s.proc = FakeProc()
+    clk = s.stop()
+    assert clk["samples"] == 5 and clk["samples_under_load"] == 3
+    assert clk["sm_mhz"] == 1665.0
+    assert clk["sm_mhz_all_samples"] == 1680.0
+    assert clk["sm_max_mhz"] == 2070.0
+    assert clk["reasons"] == ["sw_power_cap"]
+    assert clk["active_masks"] == ["0x0", "0x4"]
+    assert clk["power_w_max"] == 1302.4
+    # no sample under load: the median over all of them
+    rows[1:4] = []
+    s.proc = FakeProc()
+    clk = s.stop()
+    assert clk["samples_under_load"] == 0 and clk["sm_mhz"] == 2070.0
