@@ -118,6 +118,7 @@ struct Maps {
   CUtensorMap SFA;
   CUtensorMap SFB;
   CUtensorMap Bh;   // B with a half-height box, for column-half work items
+  CUtensorMap C;    // the fused epilogue's C in D's staging boxes (when loaded by TMA)
 };
 
 // Records the CUDA error behind a GEMM_ERR_LAUNCH for gemm_last_cuda_error().

@@ -65,6 +65,10 @@ struct GemmArgs {
   const void* C;
   uint64_t ldc;
   const void* bias;
+  // C of the fused epilogue arrives by TMA (tmC) into the epilogue warp's
+  // second staging buffer, one chunk ahead, instead of by per-thread loads
+  // (bf16 C in the TMA-store kernels with 64-column chunks)
+  uint32_t c_tma;
   // MXFP8 scale bytes read with plain loads (sf_gather != 0: a pitch or base
   // that TMA cannot take) instead of through the tmSFA / tmSFB tensor maps
   uint32_t sf_gather;
@@ -350,7 +354,7 @@ struct GemmCfg {
   static constexpr uint32_t FIX_SLOT_BYTES = 32 * 32 * 4;
   static constexpr uint32_t FIX_TOTAL = 4 * EPI_WG * FIX_SLOTS;
   static_assert(FIX_TOTAL * FIX_SLOT_BYTES <= STAGES * STAGE_BYTES, "partial ring fits the stages");
-  static_assert((2 * STAGES + RAW_SLOTS + 2 * T_SLOTS + 5) * 8 + 8 + FIX_TOTAL * 8 <= BAR_BYTES,
+  static_assert((2 * STAGES + RAW_SLOTS + 2 * T_SLOTS + 5) * 8 + 8 + FIX_TOTAL * 8 + 4 * 8 <= BAR_BYTES,
                 "barrier area");
 };
 
@@ -616,8 +620,10 @@ __device__ __forceinline__ void load_row32(const void* p, uint32_t n, float (&x)
 // The fused epilogue on one thread's 32 accumulators: row `row`, columns
 // col0 .. col0 + 31 (columns >= N and rows >= M read nothing):
 // v = alpha * acc + beta * C[row, col] + bias[col], then the activation, in fp32.
+// cpk: this row's 32 bf16 values of C already in registers (packed pairs,
+// element 2t in the low half of word t), or nullptr to load them here.
 __device__ __forceinline__ void epi_apply(uint32_t (&v)[32], const GemmArgs& a, uint32_t row,
-                                          uint32_t col0) {
+                                          uint32_t col0, const uint32_t* cpk = nullptr) {
   const uint32_t mode = a.epi_mode;
   const uint32_t n = col0 < a.N ? min(32u, a.N - col0) : 0u;
   float x[32];
@@ -629,7 +635,13 @@ __device__ __forceinline__ void epi_apply(uint32_t (&v)[32], const GemmArgs& a, 
   }
   if ((mode & kEpiC) && row < a.M && n > 0) {
     float c[32];
-    if (mode & kEpiOutF32)
+    if (cpk != nullptr) {
+#pragma unroll
+      for (uint32_t t = 0; t < 16; ++t) {
+        c[2 * t] = bf16_bits_to_f32(cpk[t] & 0xFFFFu);
+        c[2 * t + 1] = bf16_bits_to_f32(cpk[t] >> 16);
+      }
+    } else if (mode & kEpiOutF32)
       load_row32<true>(static_cast<const float*>(a.C) + static_cast<uint64_t>(row) * a.ldc + col0, n, c);
     else
       load_row32<false>(static_cast<const uint16_t*>(a.C) + static_cast<uint64_t>(row) * a.ldc + col0, n, c);
@@ -679,7 +691,8 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
                    const __grid_constant__ CUtensorMap tmD,
                    const __grid_constant__ CUtensorMap tmSFA,
                    const __grid_constant__ CUtensorMap tmSFB,
-                   const __grid_constant__ CUtensorMap tmBh, const GemmArgs args) {
+                   const __grid_constant__ CUtensorMap tmBh,
+                   const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
   using C = GemmCfg<CG, KIND, TMA_STORE, EPI2>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -704,6 +717,8 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
   const uint32_t drain_bar = bar0 + 8 * (kAccBar0 + 4);
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + (bar0 - base) + 8 * (kAccBar0 + 5));
   constexpr uint32_t kFixBar0 = kAccBar0 + 6;
+  // one barrier per epilogue warp of group 0: its TMA-loaded C chunk landed
+  constexpr uint32_t kCBar0 = kFixBar0 + C::FIX_TOTAL;
   volatile uint32_t* const abort_flag = tmem_slot + 1;
 
   const uint32_t warp = warp_idx_sync();
@@ -737,11 +752,13 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
     }
     mbar_init(drain_bar, 1);
     for (uint32_t i = 0; i < C::FIX_TOTAL; ++i) mbar_init(bar0 + 8 * (kFixBar0 + i), 1);
+    for (uint32_t i = 0; i < 4; ++i) mbar_init(bar0 + 8 * (kCBar0 + i), 1);
     *abort_flag = 0u;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     if (args.half_tiles != 0) tma_prefetch_desc(&tmBh);
+    if (args.c_tma != 0) tma_prefetch_desc(&tmC);
     if constexpr (TMA_STORE) tma_prefetch_desc(&tmD);
     if (C::MX && !args.sf_gather) {
       tma_prefetch_desc(&tmSFA);
@@ -1078,6 +1095,20 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
       return args.ws_flag + ((slot * CG + rank) * 4 + q) * 2 + eg;
     };
     const uint32_t ring = (q * NG + eg) * C::FIX_SLOTS;   // this warp's fix-up slots
+    // C by TMA (args.c_tma; kernels with one epilogue group and two 64-column
+    // staging buffers per warp): chunk c of an item's C lands in the second
+    // buffer; the first chunk is requested before the accumulator wait, each
+    // next one as soon as the current one has been read into registers.
+    constexpr bool kCTma = TMA_STORE && C::TS_COLS == 64 && C::EPI_BUFS == 2;
+    const uint32_t cbuf = epi0 + (ew * C::EPI_BUFS + 1) * C::EPI_BUF_BYTES;
+    const uint32_t c_bar = bar0 + 8 * (kCBar0 + (ew & 3u));
+    const uint64_t pol_c = l2_policy_evict_first();
+    uint32_t c_issued = 0, c_done = 0;
+    const auto issue_c = [&](uint32_t r0, uint32_t col) {
+      fence_proxy_async_smem();   // the lanes' reads of the buffer come first
+      mbar_arrive_expect_tx(c_bar, C::EPI_BUF_BYTES);
+      tma_load_2d(cbuf, &tmC, c_bar, static_cast<int32_t>(col), static_cast<int32_t>(r0), pol_c);
+    };
     const auto fix_slot = [&](uint32_t r) { return stage0 + (ring + r) * C::FIX_SLOT_BYTES; };
     const auto fix_bar = [&](uint32_t r) { return bar0 + 8 * (kFixBar0 + ring + r); };
     // owner-side transfer stream: transfer n = this warp's (n / nc)-th chunk
@@ -1118,6 +1149,18 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
     for (uint32_t wi = 0; ok && work_item(args, cluster_id, num_clusters, KT, wi, w); ++wi, ++j) {
       const uint32_t b = j % C::ACC_STAGES;
       const uint32_t around = j / C::ACC_STAGES;
+      if constexpr (kCTma) {
+        if (args.c_tma != 0 && w.kind != 2) {
+          uint32_t mb0, nb0;
+          tile_coords(w.tile, args.num_m_blocks, args.num_n_blocks, args.group_m, mb0, nb0);
+          const uint32_t r0 = mb0 * C::UMMA_M + rank * C::BLOCK_M + q * 32;
+          const uint32_t c0 = item_n0(w, nb0, C::UMMA_N);
+          if (r0 < args.M && c0 < args.N) {
+            if (lane == 0) issue_c(r0, c0);
+            ++c_issued;
+          }
+        }
+      }
       if (!warp_wait(accf_bar(b), around & 1u, wd, kSiteEpiAccFull, lane)) break;
       tc_fence_after_sync();
       uint32_t mb, nb;
@@ -1272,12 +1315,42 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
               if (!add_partials(v0, 2 * c)) { ok = false; break; }
               if (2 * c + 1 < live && !add_partials(v1, 2 * c + 1)) { ok = false; break; }
             }
-            if (args.epi_mode != 0) {
-              epi_apply(v0, args, row0 + lane, col_base + c * 64);
-              epi_apply(v1, args, row0 + lane, col_base + c * 64 + 32);
+            const bool ctma = kCTma && args.c_tma != 0;
+            uint32_t cw[32];   // this lane's row of the C chunk: bf16 pairs
+            if (ctma) {
+              if (!warp_wait(c_bar, c_done & 1u, wd, kSiteEpiC, lane)) { ok = false; break; }
+              ++c_done;
+              const uint8_t* crow = base_ptr + (cbuf - base) + lane * 128;
+#pragma unroll
+              for (uint32_t i = 0; i < 8; ++i) {
+                // 128-byte swizzle, as for D: 16-byte chunk i of row r at chunk i ^ (r % 8)
+                const uint4 t = *reinterpret_cast<const uint4*>(crow + ((i ^ (lane & 7u)) << 4));
+                cw[4 * i] = t.x;
+                cw[4 * i + 1] = t.y;
+                cw[4 * i + 2] = t.z;
+                cw[4 * i + 3] = t.w;
+              }
+              __syncwarp();   // every lane has read the buffer
+              const uint32_t cn = col_base + (c + 1) * 64;
+              if (c + 1 < item_nch / 2 && cn < args.N) {
+                if (lane == 0) issue_c(row0, cn);
+                ++c_issued;
+              }
             }
-            const uint32_t buf = epi0 + (ew * C::EPI_BUFS + (chunk_ctr % C::EPI_BUFS)) * C::EPI_BUF_BYTES;
-            if (lane == 0) bulk_wait_group_read<C::EPI_BUFS - 1>();   // this buffer's last store has read it
+            if (args.epi_mode != 0) {
+              epi_apply(v0, args, row0 + lane, col_base + c * 64, ctma ? cw : nullptr);
+              epi_apply(v1, args, row0 + lane, col_base + c * 64 + 32, ctma ? cw + 16 : nullptr);
+            }
+            // D staging: the rotating buffers, or the first one alone when
+            // the second receives C
+            const uint32_t buf = ctma ? epi0 + ew * C::EPI_BUFS * C::EPI_BUF_BYTES
+                                      : epi0 + (ew * C::EPI_BUFS + (chunk_ctr % C::EPI_BUFS)) * C::EPI_BUF_BYTES;
+            if (lane == 0) {   // the buffer's last store has read it
+              if (ctma)
+                bulk_wait_group_read<0>();
+              else
+                bulk_wait_group_read<C::EPI_BUFS - 1>();
+            }
             __syncwarp();
             uint8_t* rowp = base_ptr + (buf - base) + lane * 128;
 #pragma unroll
@@ -1349,10 +1422,13 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
           mbar_arrive_cluster(mapa_shared(acce_bar(b), 0));
       }
     }
-    // Exit path after a give-up: let the partial transfers still in flight land.
-    if (lane == 0)
+    // Exit path after a give-up: let the partial transfers and a C chunk
+    // still in flight land.
+    if (lane == 0) {
       for (uint32_t n = fix_done; n < fix_issued; ++n)
         drain_wait(fix_bar(n % C::FIX_SLOTS), (n / C::FIX_SLOTS) & 1u, wd, kSiteStreamKFlag);
+      if (c_issued > c_done) drain_wait(c_bar, c_done & 1u, wd, kSiteEpiC);
+    }
     if constexpr (TMA_STORE) {
       if (lane == 0) bulk_wait_group<0>();
       __syncwarp();

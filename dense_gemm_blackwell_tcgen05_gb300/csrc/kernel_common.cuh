@@ -22,6 +22,7 @@ enum WaitSite : uint32_t {
   kSiteSyncMma = 7,         // single-tile kernel waiting for its MMA
   kSiteSfFull = 8,          // scale-factor warp waiting for its scale bytes
   kSiteStreamKFlag = 9,     // stream-K owner waiting for a partial accumulator
+  kSiteEpiC = 10,           // epilogue waiting for a TMA-loaded tile of C
 };
 
 // Fused-epilogue mode word (0: the plain bf16 store of the accumulator).

@@ -147,6 +147,18 @@ int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) 
   a.C = p.C;
   a.ldc = p.ldc;
   a.bias = p.bias;
+  // C by TMA: bf16 C (bf16 output) in the TMA-store kernels with 64-column
+  // staging chunks, when TMA can address it (16-byte base and pitch)
+  a.c_tma = 0;
+  if constexpr (TMA_STORE && C::TS_COLS == 64 && C::EPI_BUFS == 2) {
+    if ((p.epi_mode & kEpiC) && !(p.epi_mode & kEpiOutF32) && p.C != nullptr &&
+        (reinterpret_cast<uintptr_t>(p.C) & 15u) == 0 && (p.ldc * 2) % 16 == 0) {
+      if (!encode_map_2d(&maps.C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.C, p.N, p.M, p.ldc * 2,
+                         C::TS_COLS, 32, CU_TENSOR_MAP_SWIZZLE_128B))
+        return GEMM_ERR_LAUNCH;
+      a.c_tma = 1;
+    }
+  }
   a.sf_gather = sf_gather ? 1u : 0u;
   a.sfa = static_cast<const uint8_t*>(p.SFA);
   a.sfb = static_cast<const uint8_t*>(p.SFB);
@@ -213,7 +225,7 @@ int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) 
   }
   note_schedule(static_cast<uint32_t>(clusters), CG, a.dp_tiles, a.sk_tiles, a.sk_unit, a.half_tiles);
   const cudaError_t err =
-      cudaLaunchKernelEx(&cfg, kern, maps.A, maps.B, maps.D, maps.SFA, maps.SFB, maps.Bh, a);
+      cudaLaunchKernelEx(&cfg, kern, maps.A, maps.B, maps.D, maps.SFA, maps.SFB, maps.Bh, maps.C, a);
   if (err != cudaSuccess) {
     note_cuda_error(err);
     cudaGetLastError();

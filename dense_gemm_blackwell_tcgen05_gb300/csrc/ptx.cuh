@@ -107,6 +107,12 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   return p;
 }
 
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 // 2-D tiled load into this CTA's shared memory; completion is signalled as
 // transaction bytes on `bar` (this CTA).
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
