@@ -93,3 +93,31 @@ def test_mxfp8_degenerate(v, shape):
     assert g.gemm_last_status(s) == g.GEMM_OK
     D_ref, _ = oracle.gemm_mxfp8(A.numpy(), B.numpy(), SFA.numpy(), SFB.numpy(), K)
     _check(Dbuf, M, N, D_ref)
+
+
+TILED_VARIANTS = {
+    "auto": g.VARIANT_AUTO,
+    "1cta": g.VARIANT_1CTA,
+    "2cta": g.VARIANT_2CTA,
+    "2cta_direct": g.VARIANT_2CTA | g.VARIANT_DIRECT_STORE,
+}
+
+
+@pytest.mark.parametrize("v", list(TILED_VARIANTS))
+@pytest.mark.parametrize("shape", MX_SHAPES)
+def test_mxfp8_tiled_degenerate(v, shape):
+    """The same shapes through gemm_mxfp8_tiled: scales rearranged into the
+    tiled layout (zero-padded to whole 128-row blocks and 4-block groups)."""
+    M, N, K = shape
+    lda = (K + 15) // 16 * 16
+    A, SFA, B, SFB = int_operands(M, N, K, seed=M * 5 + N + K, lda=lda)
+    Dbuf, ldd = _guarded_output(M, N)
+    Ad, Bd = A.cuda(), B.cuda()
+    SAt, SBt = gi.tile_scales(SFA, M, K).cuda(), gi.tile_scales(SFB, N, K).cuda()
+    s = torch.cuda.current_stream().cuda_stream
+    rc = g.gemm_mxfp8_tiled(TILED_VARIANTS[v], Ad.data_ptr(), Bd.data_ptr(), SAt.data_ptr(),
+                            SBt.data_ptr(), Dbuf.data_ptr(), M, N, K, lda, lda, ldd, s)
+    assert rc == g.GEMM_OK, g.gemm_status_string(rc)
+    assert g.gemm_last_status(s) == g.GEMM_OK
+    D_ref, _ = oracle.gemm_mxfp8(A.numpy(), B.numpy(), SFA.numpy(), SFB.numpy(), K)
+    _check(Dbuf, M, N, D_ref)
