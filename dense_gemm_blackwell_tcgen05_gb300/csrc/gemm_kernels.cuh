@@ -1187,8 +1187,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
           for (uint32_t i = 0; i < 4; ++i) {
             if (chunk(i) < live) {
               uint32_t v[32];
-              tmem_ld_32x32b_x32(t_addr + chunk(i) * 32, v);
-              tmem_wait_ld();
+              tmem_ld_32x32b_x32_sync(t_addr + chunk(i) * 32, v);
 #pragma unroll
               for (uint32_t t = 0; t < 16; ++t)
                 pk[i][t] = pack_bf16x2(__uint_as_float(v[2 * t]), __uint_as_float(v[2 * t + 1]));
@@ -1245,8 +1244,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
 #pragma unroll 1
         for (uint32_t c = eg; c < live; c += NG) {
           uint32_t v[32];
-          tmem_ld_32x32b_x32(t_addr + c * 32, v);
-          tmem_wait_ld();
+          tmem_ld_32x32b_x32_sync(t_addr + c * 32, v);
           float4* dst = reinterpret_cast<float4*>(part + c * 1024);
 #pragma unroll
           for (uint32_t i4 = 0; i4 < 8; ++i4)
@@ -1278,8 +1276,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
           for (uint32_t c = 0; c < item_nch; ++c) {
             if (col_base + c * 32 >= args.N) break;
             uint32_t v[32];
-            tmem_ld_32x32b_x32(t_addr + c * 32, v);
-            tmem_wait_ld();
+            tmem_ld_32x32b_x32_sync(t_addr + c * 32, v);
             if (w.kind == 1 && !add_partials(v, c)) { ok = false; break; }
             if (args.epi_mode != 0) epi_apply(v, args, row0 + lane, col_base + c * 32);
             const uint32_t buf = epi0 + (ew * C::EPI_BUFS + (chunk_ctr % C::EPI_BUFS)) * C::EPI_BUF_BYTES;
@@ -1308,9 +1305,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
           for (uint32_t c = 0; c < item_nch / 2; ++c) {
             if (col_base + c * 64 >= args.N) break;
             uint32_t v0[32], v1[32];
-            tmem_ld_32x32b_x32(t_addr + c * 64, v0);
-            tmem_ld_32x32b_x32(t_addr + c * 64 + 32, v1);
-            tmem_wait_ld();
+            tmem_ld2_32x32b_x32_sync(t_addr + c * 64, t_addr + c * 64 + 32, v0, v1);
             if (w.kind == 1) {
               if (!add_partials(v0, 2 * c)) { ok = false; break; }
               if (2 * c + 1 < live && !add_partials(v1, 2 * c + 1)) { ok = false; break; }
@@ -1381,10 +1376,9 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
           }
         } else {
           // One 32-column chunk at a time (this group's chunks eg, eg + NG, ...).
-          // Each tcgen05.ld is followed at once by its tcgen05.wait::ld: the
-          // load writes its destination registers asynchronously while the
-          // compiler takes them as written by the asm statement, so no other
-          // code may sit between the two.
+          // Each tcgen05.ld and its tcgen05.wait::ld form one asm statement:
+          // the load writes its destination registers asynchronously, so no
+          // other code may sit between the two.
           const auto finish_chunk = [&](uint32_t (&v)[32], uint32_t c) -> bool {
             if (w.kind == 1 && !add_partials(v, c)) return false;
             if (args.epi_mode != 0) epi_apply(v, args, row0 + lane, col_base + c * 32);
@@ -1400,8 +1394,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
 #pragma unroll 1
           for (uint32_t c = eg; c < live; c += NG) {
             uint32_t v[32];
-            tmem_ld_32x32b_x32(t_addr + c * 32, v);
-            tmem_wait_ld();
+            tmem_ld_32x32b_x32_sync(t_addr + c * 32, v);
             if (!finish_chunk(v, c)) { ok = false; break; }
           }
         }

@@ -218,8 +218,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_smallk_tc_kernel(const __g
 #pragma unroll 1
       for (uint32_t c = eg; c < kTcCols / 32; c += 2) {
         uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem + b * kTcCols + ((q * 32u) << 16) + c * 32, v);
-        tmem_wait_ld();
+        tmem_ld_32x32b_x32_sync(tmem + b * kTcCols + ((q * 32u) << 16) + c * 32, v);
         const int64_t cc = col0 + 32 * c;   // first column of this run (warp-uniform)
         if (cc >= static_cast<int64_t>(a.N) || cc + 32 <= 0 || jr0 >= rows) continue;
         uint32_t p[16];

@@ -99,8 +99,7 @@ __global__ void __launch_bounds__(128, 1) gemm_sync_kernel(const SyncArgs args) 
 #pragma unroll 1
     for (uint32_t c = 0; c < 4; ++c) {
       uint32_t v[32];
-      tmem_ld_32x32b_x32(tmem + ((warp * 32u) << 16) + c * 32, v);
-      tmem_wait_ld();
+      tmem_ld_32x32b_x32_sync(tmem + ((warp * 32u) << 16) + c * 32, v);
       if (num_kt == 0) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = 0u;
