@@ -93,10 +93,15 @@ __global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const QuantArgs a) 
     for (uint32_t j = 0; j < 8; ++j) {
       const uint32_t kb = k0 + 128 * j + 32 * (lane >> 3);   // first k of this lane's block
       float m = 0.0f;
+      bool fin = true;   // this lane's four values are all finite
 #pragma unroll
       for (uint32_t t = 0; t < 4; ++t) {
         const float ax = fabsf(x[j][t]);
-        if (ax <= 3.402823466e38f && ax > m) m = ax;        // finite values only
+        if (ax <= 3.402823466e38f) {   // finite values only
+          if (ax > m) m = ax;
+        } else {
+          fin = false;
+        }
       }
       m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
       m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
@@ -109,9 +114,15 @@ __global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const QuantArgs a) 
       const int e = scale_exponent(m);
       const float scale = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);   // 2^-e, e <= 126
       const uint32_t k = k0 + 128 * j + 4 * lane;
+      // two values per conversion; a NaN or an infinity (E4M3 NaN, sign kept,
+      // where the saturating conversion would give 448) one at a time
       uint32_t q = 0;
+      if (fin) {
+        q = e4m3x2(x[j][0] * scale, x[j][1] * scale) | (e4m3x2(x[j][2] * scale, x[j][3] * scale) << 16);
+      } else {
 #pragma unroll
-      for (uint32_t t = 0; t < 4; ++t) q |= encode_one(x[j][t], scale) << (8 * t);
+        for (uint32_t t = 0; t < 4; ++t) q |= encode_one(x[j][t], scale) << (8 * t);
+      }
       uint8_t* qr = a.Q + row * a.ldq;
       if (a.vec_out && k + 4 <= a.K) {
         __stcs(reinterpret_cast<unsigned int*>(qr + k), q);   // written once
