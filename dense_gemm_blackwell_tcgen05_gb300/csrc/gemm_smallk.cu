@@ -90,27 +90,61 @@ __global__ void __launch_bounds__(kThreadsSmallK, 2) gemm_smallk_kernel(const Sm
   const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kStrip - e + CPL * lane;   // first column
   const bool lane_full = c0 >= 0 && c0 + CPL <= a.N;
   const bool lane_any = c0 + CPL > 0 && c0 < static_cast<int64_t>(a.N);
+  // The block's B strip -- the kStrip + CPL - 1 columns its warps' shifted
+  // strips cover -- staged once in shared memory as raw bf16 rows of KK
+  // values (16-byte chunks; one padding slot per 8 columns, so that lanes
+  // reading columns 8 apart hit different banks).  Every warp reads its
+  // columns from here: the block loads each B row from L2 once instead of
+  // once per warp.  Values at k >= K and columns outside [0, N) are zero,
+  // and nothing at k >= K is read.
+  constexpr uint32_t kBCols = kStrip + CPL - 1;
+  constexpr uint32_t kChunks = (KK + 7) / 8;
+  __shared__ __align__(16) uint4 sB[kBCols + kBCols / 8 + 1][kChunks];
+  const int64_t bbase = static_cast<int64_t>(blockIdx.x) * kStrip - (CPL - 1);
+  for (uint32_t i = threadIdx.x; i < kBCols; i += kThreadsSmallK) {
+    const int64_t c = bbase + i;
+    const bool in = c >= 0 && c < static_cast<int64_t>(a.N);
+#pragma unroll
+    for (uint32_t h = 0; h < kChunks; ++h) {
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      const uint16_t* src = a.B + static_cast<uint64_t>(in ? c : 0) * a.ldb + 8 * h;
+      if (in && a.K >= 8 * (h + 1)) {
+        // a whole chunk inside K: one 16-byte load (rows start 16-byte aligned)
+        v = __ldg(reinterpret_cast<const uint4*>(src));
+      } else if (in && 8 * h < a.K) {
+        // the chunk K ends in: only its values below K are read
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (uint32_t q = 0; q < 8; ++q)
+          if (8 * h + q < a.K) w[q / 2] |= static_cast<uint32_t>(__ldg(src + q)) << (16 * (q % 2));
+        v = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      sB[i + i / 8][h] = v;
+    }
+  }
+  __syncthreads();
   // B values of columns c0 .. c0 + CPL - 1 in registers as column pairs
-  // (zero outside [0, N))
   float2 b[W][KK];
+  {
+    float x[CPL][KK];
 #pragma unroll
-  for (uint32_t p = 0; p < W; ++p) {
-    float lo[KK], hi[KK];
-    const int64_t cl = c0 + 2 * p, ch = cl + 1;
-    if (cl >= 0 && cl < a.N) {
-      load_row<KK>(a.B + static_cast<uint64_t>(cl) * a.ldb, a.K, lo);
-    } else {
+    for (uint32_t t = 0; t < CPL; ++t) {
+      const uint32_t i = static_cast<uint32_t>(c0 + t - bbase);
 #pragma unroll
-      for (uint32_t k = 0; k < KK; ++k) lo[k] = 0.0f;
+      for (uint32_t h = 0; h < kChunks; ++h) {
+        const uint4 v = sB[i + i / 8][h];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (uint32_t q = 0; q < 4; ++q) {
+          if (8 * h + 2 * q < KK) x[t][8 * h + 2 * q] = bf16f(w[q] & 0xFFFFu);
+          if (8 * h + 2 * q + 1 < KK) x[t][8 * h + 2 * q + 1] = bf16f(w[q] >> 16);
+        }
+      }
     }
-    if (ch >= 0 && ch < a.N) {
-      load_row<KK>(a.B + static_cast<uint64_t>(ch) * a.ldb, a.K, hi);
-    } else {
 #pragma unroll
-      for (uint32_t k = 0; k < KK; ++k) hi[k] = 0.0f;
-    }
+    for (uint32_t p = 0; p < W; ++p)
 #pragma unroll
-    for (uint32_t k = 0; k < KK; ++k) b[p][k] = make_float2(lo[k], hi[k]);
+      for (uint32_t k = 0; k < KK; ++k) b[p][k] = make_float2(x[2 * p][k], x[2 * p + 1][k]);
   }
   for (uint32_t rt = blockIdx.y; rt * kTileRows < a.M; rt += gridDim.y) {
     const uint32_t row0 = rt * kTileRows;
