@@ -3,10 +3,15 @@
 //
 //  * gemm_ws_kernel   -- persistent, warp-specialised kernel (TMA producer
 //                        warp, single-thread MMA issuer, one or two groups of
-//                        four epilogue warps, a scale-factor warp for MXFP8),
-//                        one CTA (cta_group::1) or a CTA pair (cta_group::2);
-//                        bf16 operands (128x256 / 256x256 tiles) or
-//                        block-scaled MXFP8 operands (128x224 / 256x224).
+//                        four epilogue warps, a scale-factor warp for MXFP8
+//                        with row-major scales or a scale-copy thread for
+//                        tiled ones), one CTA (cta_group::1) or a CTA pair
+//                        (cta_group::2); bf16 operands (128x256 / 256x256
+//                        tiles), block-scaled MXFP8 operands with row-major
+//                        scales (128x224 / 256x224) or tiled scales
+//                        (128x256 / 256x256).  A short last round of tiles
+//                        may run as column halves; the fused epilogue can
+//                        bring C in by TMA.
 //  * gemm_sync_kernel -- (gemm_sync.cuh) one 128x128 tile per CTA with synchronous thread
 //                        copies into shared memory and one MMA batch per
 //                        K-tile: the first rungs of the optimisation ladder,
