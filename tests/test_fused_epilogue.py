@@ -246,6 +246,25 @@ def test_c_by_tma_matches_loaded_c(v):
     assert_bound(D_tma, D_ref, S, scale, 0.5, "gelu", f"C by TMA {v}")
 
 
+def test_c_by_tma_at_an_offset_base():
+    """C starting 16 bytes past an allocation's start (still TMA-aligned) with
+    a pitch other than D's: the TMA path reads the right rows and columns."""
+    M, N, K = 700, 1032, 128
+    A, B = ints((M, K), 51), ints((N, K), 52)
+    gen = torch.Generator().manual_seed(53)
+    Cbig = torch.randint(-8, 9, (M * (N + 40) + 8,), generator=gen).to(torch.bfloat16).cuda()
+    Cview = Cbig[8:8 + M * (N + 40)].view(M, N + 40)[:, :N]          # base + 16 bytes, pitch N + 40
+    e = g.make_epilogue(1.0, -1.0, Cview, None, "none", torch.bfloat16)
+    Ad, Bd = A.cuda(), B.cuda()
+    D = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    rc = g.gemm_bf16_fused(g.VARIANT_2CTA, Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), M, N, K,
+                           K, K, N, e, 0)
+    assert rc == g.GEMM_OK and g.gemm_last_status(0) == g.GEMM_OK
+    P_, S = oracle.gemm_bf16(gi.bf16_codes(A), gi.bf16_codes(B))
+    D_ref, _, _ = reference(P_, S, 1.0, -1.0, Cview.cpu(), None, "none")
+    assert_bitwise(D.cpu(), D_ref, "C at an offset base")
+
+
 def test_c_by_tma_in_place_over_several_waves():
     """C == D through the TMA path on a shape with more tiles than clusters:
     each chunk of C is read before the same chunk of D is stored."""

@@ -202,6 +202,36 @@ def test_fused_epilogue_columns_follow_the_halves():
     _assert_oracle_bitwise(D1, want, "fused split")
 
 
+@pytest.mark.gpu
+def test_fused_fp32_output_over_the_halves():
+    """fp32 output (the masked-store kernel, per-thread C loads) with column
+    halves: C, bias and the store all follow the half's column offset."""
+    M, N, K = 2600, 2000, 72
+    A, B = _ints(M, N, K, seed=15)
+    gen = torch.Generator().manual_seed(16)
+    bias = torch.randint(-8, 9, (N,), generator=gen).to(torch.float32)
+    C = torch.randint(-8, 9, (M, N), generator=gen).to(torch.float32)
+    bd, Cd = bias.cuda(), C.cuda()
+    epi = g.make_epilogue(0.5, 2.0, Cd, bd, "relu", torch.float32)
+
+    def fn():
+        Ad, Bd = A.cuda(), B.cuda()
+        D = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        s = torch.cuda.current_stream().cuda_stream
+        rc = g.gemm_bf16_fused(g.VARIANT_2CTA, Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), M, N, K,
+                               K, K, N, epi, s)
+        assert rc == g.GEMM_OK, g.gemm_status_string(rc)
+        assert g.gemm_last_status(s) == g.GEMM_OK
+        return D.cpu()
+    D1, s1 = _launch(fn, split=True)
+    assert s1["half_tiles"] > 0
+    P_ref, _ = oracle.gemm_bf16(gi.bf16_codes(A), gi.bf16_codes(B))
+    want = np.maximum(0.5 * P_ref + 2.0 * C.double().numpy() + bias.double().numpy()[None, :], 0.0)
+    got = D1.double().numpy()
+    bad = np.argwhere(got != want)
+    assert len(bad) == 0, f"{len(bad)} mismatches, first at {tuple(bad[0])}"
+
+
 MX_CASES = [("auto", 2600, 2000, 256), ("auto", 700, 1100, 384), ("1cta", 2560, 2048, 128)]
 MX_VARIANT = {"auto": g.VARIANT_AUTO, "1cta": g.VARIANT_1CTA}
 
