@@ -247,7 +247,11 @@ struct GemmCfg {
   static constexpr uint32_t OFF_B = A_BYTES;
   static constexpr uint32_t OFF_SF = A_BYTES + B_BYTES;
   static constexpr uint32_t STAGE_BYTES = align_up_u32(A_BYTES + B_BYTES + SF_STAGE_BYTES, 1024);
-  static constexpr uint32_t AB_TX = A_BYTES + B_BYTES + SF_STAGE_BYTES;   // per CTA
+  // Bytes that land on a stage's ready barrier, per CTA: the A and B tiles.
+  // Tiled scales have a ready barrier of their own per stage, and the
+  // producer issues their loads first: the scale copies into TMEM then start
+  // while the operand tiles are still arriving.
+  static constexpr uint32_t AB_TX = A_BYTES + B_BYTES;
   static constexpr uint32_t FULL_ARRIVALS = 1;                    // the producer's expect_tx
 
   // MXFP8 scale factors travel in two rings of their own, one slot per group
@@ -331,7 +335,7 @@ struct GemmCfg {
       TMA_STORE ? 4 * EPI_WG * EPI_BUFS * EPI_BUF_BYTES : 4 * EPI_WG * CHUNK_BYTES;
 
   static constexpr uint32_t SMEM_LIMIT = 232448;  // 227 KB opt-in per CTA
-  static constexpr uint32_t BAR_BYTES = 512;
+  static constexpr uint32_t BAR_BYTES = SF_TILED ? 1024 : 512;
   static constexpr uint32_t ALIGN_SLACK = 1024;
   static constexpr uint32_t STAGES_FIT =
       (SMEM_LIMIT - ALIGN_SLACK - BAR_BYTES - EPI_BYTES - SF_BYTES) / STAGE_BYTES;
@@ -359,7 +363,8 @@ struct GemmCfg {
   static constexpr uint32_t FIX_SLOT_BYTES = 32 * 32 * 4;
   static constexpr uint32_t FIX_TOTAL = 4 * EPI_WG * FIX_SLOTS;
   static_assert(FIX_TOTAL * FIX_SLOT_BYTES <= STAGES * STAGE_BYTES, "partial ring fits the stages");
-  static_assert((2 * STAGES + RAW_SLOTS + 2 * T_SLOTS + 5) * 8 + 8 + FIX_TOTAL * 8 + 4 * 8 <= BAR_BYTES,
+  static_assert((2 * STAGES + RAW_SLOTS + 2 * T_SLOTS + 5) * 8 + 8 + FIX_TOTAL * 8 + 4 * 8 +
+                        (SF_TILED ? STAGES * 8 : 0) <= BAR_BYTES,
                 "barrier area");
 };
 
@@ -724,6 +729,9 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
   constexpr uint32_t kFixBar0 = kAccBar0 + 6;
   // one barrier per epilogue warp of group 0: its TMA-loaded C chunk landed
   constexpr uint32_t kCBar0 = kFixBar0 + C::FIX_TOTAL;
+  // tiled scales: one per stage, the stage's scale chunks landed
+  constexpr uint32_t kSfStageBar0 = kCBar0 + 4;
+  const auto sf_full_bar = [&](uint32_t s) { return bar0 + 8 * (kSfStageBar0 + s); };
   volatile uint32_t* const abort_flag = tmem_slot + 1;
 
   const uint32_t warp = warp_idx_sync();
@@ -739,6 +747,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
     for (uint32_t s = 0; s < C::STAGES; ++s) {
       mbar_init(full_bar(s), C::FULL_ARRIVALS);  // producer's expect_tx (+ TMA bytes)
       mbar_init(empty_bar(s), 1);                // MMA issuer's commit
+      if constexpr (C::SF_TILED) mbar_init(sf_full_bar(s), 1);   // producer's expect_tx (+ scale bytes)
     }
     for (uint32_t g = 0; g < C::RAW_SLOTS; ++g) {
       mbar_init(raw_full_bar(g), 1);   // this CTA's scale bytes landed (expect_tx)
@@ -816,29 +825,32 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
           const int32_t sfa_y = static_cast<int32_t>(((static_cast<uint32_t>(a_row) / 128u) * KT + kt) * 32u);
           const uint32_t sfb_blk = n0 / 128u;
           if constexpr (CG == 1) {
+            if constexpr (C::SF_TILED) {
+              mbar_arrive_expect_tx(sf_full_bar(s), C::SF_STAGE_BYTES);
+              tma_load_2d(sb + C::OFF_SF, &tmSFA, sf_full_bar(s), 0, sfa_y, pol);
+#pragma unroll
+              for (uint32_t h = 0; h < C::SFB_TILE_CHUNKS; ++h)
+                tma_load_2d(sb + C::OFF_SF + 512 * (1 + h), &tmSFB, sf_full_bar(s), 0,
+                            static_cast<int32_t>(((sfb_blk + h) * KT + kt) * 32u), pol);
+            }
             mbar_arrive_expect_tx(full_bar(s), tx);
             tma_load_2d(sb, &tmA, full_bar(s), kx, a_row, pol);
             tma_load_2d(sb + C::OFF_B, mapB, full_bar(s), kx, b_row, pol);
+          } else {
+            // both CTAs' bytes land on the leader's barriers
             if constexpr (C::SF_TILED) {
-              tma_load_2d(sb + C::OFF_SF, &tmSFA, full_bar(s), 0, sfa_y, pol);
+              const uint32_t leader_sf = mapa_shared(sf_full_bar(s), 0);
+              if (leader) mbar_arrive_expect_tx(sf_full_bar(s), CG * C::SF_STAGE_BYTES);
+              tma_load_2d_pair(sb + C::OFF_SF, &tmSFA, leader_sf, 0, sfa_y, pol);
 #pragma unroll
               for (uint32_t h = 0; h < C::SFB_TILE_CHUNKS; ++h)
-                tma_load_2d(sb + C::OFF_SF + 512 * (1 + h), &tmSFB, full_bar(s), 0,
-                            static_cast<int32_t>(((sfb_blk + h) * KT + kt) * 32u), pol);
+                tma_load_2d_pair(sb + C::OFF_SF + 512 * (1 + h), &tmSFB, leader_sf, 0,
+                                 static_cast<int32_t>(((sfb_blk + h) * KT + kt) * 32u), pol);
             }
-          } else {
-            // both CTAs' operand bytes land on the leader's ready barrier
             const uint32_t leader_full = mapa_shared(full_bar(s), 0);
             if (leader) mbar_arrive_expect_tx(full_bar(s), CG * tx);
             tma_load_2d_pair(sb, &tmA, leader_full, kx, a_row, pol);
             tma_load_2d_pair(sb + C::OFF_B, mapB, leader_full, kx, b_row, pol);
-            if constexpr (C::SF_TILED) {
-              tma_load_2d_pair(sb + C::OFF_SF, &tmSFA, leader_full, 0, sfa_y, pol);
-#pragma unroll
-              for (uint32_t h = 0; h < C::SFB_TILE_CHUNKS; ++h)
-                tma_load_2d_pair(sb + C::OFF_SF + 512 * (1 + h), &tmSFB, leader_full, 0,
-                                 static_cast<int32_t>(((sfb_blk + h) * KT + kt) * 32u), pol);
-            }
           }
         }
       }
@@ -847,8 +859,11 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
         const uint32_t first = it > C::STAGES ? it - C::STAGES : 0u;
         if (leader)
           for (uint32_t i = first; i < it; ++i)
-            if (i != args.stall_iter)
+            if (i != args.stall_iter) {
               drain_wait(full_bar(i % C::STAGES), (i / C::STAGES) & 1u, wd, kSiteProducerDrain);
+              if constexpr (C::SF_TILED)
+                drain_wait(sf_full_bar(i % C::STAGES), (i / C::STAGES) & 1u, wd, kSiteProducerDrain);
+            }
       }
     }
   } else if (warp == 1) {
@@ -940,8 +955,8 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
     }
   } else if (C::SF_TILED && warp == C::kCpWarp) {
     // ==================== scale copies: one thread of the leader CTA ==============
-    // For each K-tile, once its stage has landed and the MMAs of the K-tile
-    // SF_SETS back (which read the same scale set) have completed, copy its
+    // For each K-tile, once its stage's scale chunks have landed and the MMAs
+    // of the K-tile SF_SETS back (which read the same scale set) have completed, copy its
     // scale chunks from the stage into scale set it % SF_SETS and commit to
     // that set's barrier.  tcgen05 operations of different threads are ordered only
     // through these commits and barrier waits.
@@ -952,7 +967,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
       for (uint32_t wi = 0; ok && work_item(args, cluster_id, num_clusters, KT, wi, w); ++wi) {
         for (uint32_t kt = w.k_begin; kt < w.k_end; ++kt, ++it) {
           const uint32_t s = it % C::STAGES;
-          if (!wait_bounded(full_bar(s), (it / C::STAGES) & 1u, wd, kSiteSfFull)) { ok = false; break; }
+          if (!wait_bounded(sf_full_bar(s), (it / C::STAGES) & 1u, wd, kSiteSfFull)) { ok = false; break; }
           if (it >= C::SF_SETS) {
             const uint32_t p = it - C::SF_SETS;   // the K-tile whose MMAs read this set last
             if (!wait_bounded(empty_bar(p % C::STAGES), (p / C::STAGES) & 1u, wd, kSiteSfFull)) {
