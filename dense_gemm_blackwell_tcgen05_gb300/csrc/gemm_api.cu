@@ -242,10 +242,12 @@ struct MapKey {
   uint64_t inner, rows, pitch;
   uint32_t box_inner, box_rows;
   int dtype, swizzle;
+  uint64_t dim2 = 0, pitch2 = 0;   // third dimension (0: a 2-D map)
+  uint32_t box2 = 0;
   bool operator==(const MapKey& o) const {
     return base == o.base && inner == o.inner && rows == o.rows && pitch == o.pitch &&
            box_inner == o.box_inner && box_rows == o.box_rows && dtype == o.dtype &&
-           swizzle == o.swizzle;
+           swizzle == o.swizzle && dim2 == o.dim2 && pitch2 == o.pitch2 && box2 == o.box2;
   }
 };
 struct MapEntry {
@@ -259,7 +261,8 @@ thread_local MapEntry t_map_cache[kMapCacheSize];
 uint32_t map_slot(const MapKey& k) {
   uint64_t h = reinterpret_cast<uintptr_t>(k.base) * 0x9E3779B97F4A7C15ull;
   h ^= (k.inner + 31 * k.rows + 131 * k.pitch + 1009ull * k.box_inner + 9176ull * k.box_rows +
-        7ull * static_cast<uint64_t>(k.dtype) + 3ull * static_cast<uint64_t>(k.swizzle)) *
+        7ull * static_cast<uint64_t>(k.dtype) + 3ull * static_cast<uint64_t>(k.swizzle) +
+        10007ull * k.dim2 + 37ull * k.pitch2 + 101ull * k.box2) *
        0xC2B2AE3D27D4EB4Full;
   return static_cast<uint32_t>(h >> 58) % kMapCacheSize;
 }
@@ -282,6 +285,36 @@ bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
                               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    t_last_cuda_error = 100000 + static_cast<int>(r);
+    return false;
+  }
+  slot.valid = true;
+  slot.key = key;
+  slot.map = *map;
+  return true;
+}
+
+bool encode_map_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                   const uint64_t (&dims)[3], const uint64_t (&strides)[2], const uint32_t (&box)[3]) {
+  if (g_encode == nullptr) return false;
+  MapKey key{base, dims[0], dims[1], strides[0], box[0], box[1], static_cast<int>(dtype),
+             static_cast<int>(CU_TENSOR_MAP_SWIZZLE_NONE)};
+  key.dim2 = dims[2];
+  key.pitch2 = strides[1];
+  key.box2 = box[2];
+  MapEntry& slot = t_map_cache[map_slot(key)];
+  if (slot.valid && slot.key == key) {
+    *map = slot.map;
+    return true;
+  }
+  const cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+  const cuuint64_t st[2] = {strides[0], strides[1]};
+  const cuuint32_t bx[3] = {box[0], box[1], box[2]};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(map, dtype, 3, const_cast<void*>(base), d, st, bx, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     t_last_cuda_error = 100000 + static_cast<int>(r);
@@ -416,8 +449,8 @@ static int mxfp8_impl(int variant, const void* A, const void* B, const void* SFA
   if (rc == GEMM_OK && M != 0 && N != 0) rc = check_epilogue_alignment(epi, D);
   if (rc != GEMM_OK || M == 0 || N == 0) return rc;
   if (K > 0 && sf_tiled) {
-    // 512-byte chunks read by TMA: 16-byte aligned bases, and the 16-byte-row
-    // view (32 rows per chunk) addressable with 32-bit coordinates
+    // 512-byte chunks read by TMA: 16-byte aligned bases; each buffer's size
+    // in 16-byte rows (32 per chunk) stays within a signed 32-bit count
     const int64_t kt = (K + 127) / 128;
     if (SFA == nullptr || SFB == nullptr || (M + 127) / 128 * kt * 32 > INT32_MAX ||
         (N + 127) / 128 * kt * 32 > INT32_MAX)

@@ -132,6 +132,10 @@ void note_schedule(uint32_t clusters, uint32_t cg, uint32_t dp_tiles, uint32_t s
 bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
                    uint64_t rows, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_rows,
                    CUtensorMapSwizzle swizzle);
+// Encodes a 3-D tiled tensor map without swizzle: extents dims[0..2]
+// (elements), strides of dimensions 1 and 2 in bytes, box extents box[0..2].
+bool encode_map_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                   const uint64_t (&dims)[3], const uint64_t (&strides)[2], const uint32_t (&box)[3]);
 
 // Kernel launchers; each returns a gemm_status_t value.
 int launch_bf16_ws(int cg, bool tma_store, const Problem& p, const LaunchCtx& ctx,

@@ -819,19 +819,16 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
           }
           const uint32_t sb = stage0 + s * C::STAGE_BYTES;
           const int32_t kx = static_cast<int32_t>(kt * C::BK);
-          // Tiled scales: chunk (row block, K-tile) sits at chunk row
-          // (row block * KT + kt) * 32 of the 16-byte-row view; this CTA's A
-          // row block, then the tile's B row blocks.
-          const int32_t sfa_y = static_cast<int32_t>(((static_cast<uint32_t>(a_row) / 128u) * KT + kt) * 32u);
-          const uint32_t sfb_blk = n0 / 128u;
+          // Tiled scales: the K-tile's chunk of this CTA's A row block, then
+          // those of the tile's B row blocks (one box each).
+          const int32_t sfa_blk = static_cast<int32_t>(static_cast<uint32_t>(a_row) / 128u);
+          const int32_t sfb_blk = static_cast<int32_t>(n0 / 128u);
           if constexpr (CG == 1) {
             if constexpr (C::SF_TILED) {
               mbar_arrive_expect_tx(sf_full_bar(s), C::SF_STAGE_BYTES);
-              tma_load_2d(sb + C::OFF_SF, &tmSFA, sf_full_bar(s), 0, sfa_y, pol);
-#pragma unroll
-              for (uint32_t h = 0; h < C::SFB_TILE_CHUNKS; ++h)
-                tma_load_2d(sb + C::OFF_SF + 512 * (1 + h), &tmSFB, sf_full_bar(s), 0,
-                            static_cast<int32_t>(((sfb_blk + h) * KT + kt) * 32u), pol);
+              tma_load_3d(sb + C::OFF_SF, &tmSFA, sf_full_bar(s), 0, static_cast<int32_t>(kt), sfa_blk, pol);
+              tma_load_3d(sb + C::OFF_SF + 512, &tmSFB, sf_full_bar(s), 0, static_cast<int32_t>(kt), sfb_blk,
+                          pol);
             }
             mbar_arrive_expect_tx(full_bar(s), tx);
             tma_load_2d(sb, &tmA, full_bar(s), kx, a_row, pol);
@@ -841,11 +838,9 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
             if constexpr (C::SF_TILED) {
               const uint32_t leader_sf = mapa_shared(sf_full_bar(s), 0);
               if (leader) mbar_arrive_expect_tx(sf_full_bar(s), CG * C::SF_STAGE_BYTES);
-              tma_load_2d_pair(sb + C::OFF_SF, &tmSFA, leader_sf, 0, sfa_y, pol);
-#pragma unroll
-              for (uint32_t h = 0; h < C::SFB_TILE_CHUNKS; ++h)
-                tma_load_2d_pair(sb + C::OFF_SF + 512 * (1 + h), &tmSFB, leader_sf, 0,
-                                 static_cast<int32_t>(((sfb_blk + h) * KT + kt) * 32u), pol);
+              tma_load_3d_pair(sb + C::OFF_SF, &tmSFA, leader_sf, 0, static_cast<int32_t>(kt), sfa_blk, pol);
+              tma_load_3d_pair(sb + C::OFF_SF + 512, &tmSFB, leader_sf, 0, static_cast<int32_t>(kt), sfb_blk,
+                               pol);
             }
             const uint32_t leader_full = mapa_shared(full_bar(s), 0);
             if (leader) mbar_arrive_expect_tx(full_bar(s), CG * tx);

@@ -108,13 +108,18 @@ int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) 
       C::SF_WARP && (((reinterpret_cast<uintptr_t>(p.SFA) | reinterpret_cast<uintptr_t>(p.SFB)) & 15u) != 0 ||
                      p.ldsfa % 16 != 0 || p.ldsfb % 16 != 0);
   if constexpr (C::SF_TILED) {
-    // the tiled scale matrices as rows of 16 bytes: 32 rows per 512-byte
-    // chunk, chunks ordered (row block, K-tile); one 32-row box per chunk
+    // the tiled scale matrices as 512-byte chunks (128 words of 32 bits),
+    // indexed (K-tile, row block): one box is a K-tile's chunk of one row
+    // block for A, of the tile's SFB_TILE_CHUNKS row blocks for B (chunks of
+    // consecutive row blocks lie KT chunks apart)
     const uint64_t kt = (p.K + C::BK - 1) / C::BK;
-    if (!encode_map_2d(&maps.SFA, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.SFA, 16,
-                       (p.M + 127) / 128 * kt * 32, 16, 16, 32, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_map_2d(&maps.SFB, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.SFB, 16,
-                       (p.N + 127) / 128 * kt * 32, 16, 16, 32, CU_TENSOR_MAP_SWIZZLE_NONE))
+    const uint64_t sa_dims[3] = {128, kt, (p.M + 127) / 128};
+    const uint64_t sb_dims[3] = {128, kt, (p.N + 127) / 128};
+    const uint64_t strides[2] = {512, kt * 512};
+    const uint32_t sa_box[3] = {128, 1, 1};
+    const uint32_t sb_box[3] = {128, 1, C::SFB_TILE_CHUNKS};
+    if (!encode_map_3d(&maps.SFA, CU_TENSOR_MAP_DATA_TYPE_UINT32, p.SFA, sa_dims, strides, sa_box) ||
+        !encode_map_3d(&maps.SFB, CU_TENSOR_MAP_DATA_TYPE_UINT32, p.SFB, sb_dims, strides, sb_box))
       return GEMM_ERR_LAUNCH;
   } else if (C::MX && !sf_gather) {
     const uint64_t nblk = (p.K + 31) / 32;
