@@ -13,13 +13,41 @@
 
 namespace gb300 {
 
-// One-time, per device: opt gemm_ws_kernel<CG, KIND, TMA_STORE> into the large
-// shared-memory carve-out and (pairs) find how many clusters can be resident at
-// once.  *resident: the clusters a launch may use.
+// The builds of gemm_ws_kernel<CG, KIND, TMA_STORE, EPI2> the library keeps:
+// the plain one (PLAIN = true) for bf16 and the tiled-scale MXFP8 kernels,
+// the general one for bf16 and the row-major-scale MXFP8 kernels (the
+// tiled-scale entry point never splits tiles along K or fuses an epilogue).
+template <int CG, Kind KIND, bool TMA_STORE, bool EPI2>
+struct WsBuilds {
+  static constexpr bool kPlain = KIND != Kind::MXF8 && !EPI2;
+  static constexpr bool kGeneral = KIND != Kind::MXF8T;
+  static_assert(kPlain || kGeneral, "at least one build");
+};
+
+// The kernel a launch runs: the plain build when the launch needs nothing it
+// leaves out, else the general one; nullptr when this configuration keeps no
+// build that fits (not reachable from the API).  Only the kept builds are
+// named, so only they are instantiated.
+template <int CG, Kind KIND, bool TMA_STORE, bool EPI2>
+auto ws_kernel_for(bool plain) {
+  using Bld = WsBuilds<CG, KIND, TMA_STORE, EPI2>;
+  decltype(&gemm_ws_kernel<CG, KIND, TMA_STORE, EPI2, false>) k = nullptr;
+  if constexpr (Bld::kPlain) {
+    if (plain) k = gemm_ws_kernel<CG, KIND, TMA_STORE, EPI2, true>;
+  }
+  if constexpr (Bld::kGeneral) {
+    if (k == nullptr) k = gemm_ws_kernel<CG, KIND, TMA_STORE, EPI2, false>;
+  }
+  return k;
+}
+
+// One-time, per device: opt the builds of gemm_ws_kernel<CG, KIND, TMA_STORE>
+// into the large shared-memory carve-out and (pairs) find how many clusters
+// can be resident at once.  *resident: the clusters a launch may use.
 template <int CG, Kind KIND, bool TMA_STORE, bool EPI2 = false>
 int ws_resident(const LaunchCtx& ctx, uint64_t* resident) {
   using C = GemmCfg<CG, KIND, TMA_STORE, EPI2>;
-  auto kern = gemm_ws_kernel<CG, KIND, TMA_STORE, EPI2>;
+  using Bld = WsBuilds<CG, KIND, TMA_STORE, EPI2>;
   static std::mutex mu;
   static int prepared[128] = {0};
   static int max_clusters[128] = {0};
@@ -27,17 +55,23 @@ int ws_resident(const LaunchCtx& ctx, uint64_t* resident) {
   {
     std::lock_guard<std::mutex> lk(mu);
     if (!prepared[ctx.device]) {
-      if (const cudaError_t e = cudaFuncSetAttribute(
-              kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM_BYTES));
-          e != cudaSuccess) {
-        note_cuda_error(e);
-        cudaGetLastError();
-        return GEMM_ERR_LAUNCH;
+      for (int build = 0; build < 2; ++build) {
+        if (build == 0 ? !Bld::kPlain : !Bld::kGeneral) continue;
+        auto k = ws_kernel_for<CG, KIND, TMA_STORE, EPI2>(build == 0);
+        if (const cudaError_t e = cudaFuncSetAttribute(
+                k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM_BYTES));
+            e != cudaSuccess) {
+          note_cuda_error(e);
+          cudaGetLastError();
+          return GEMM_ERR_LAUNCH;
+        }
+        if constexpr (CG == 2) {
+          if (cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) !=
+              cudaSuccess)
+            cudaGetLastError();
+        }
       }
       if constexpr (CG == 2) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) !=
-            cudaSuccess)
-          cudaGetLastError();
         cudaLaunchConfig_t q = {};
         q.gridDim = dim3(2 * ctx.num_sms);
         q.blockDim = dim3(C::kThreads);
@@ -50,7 +84,9 @@ int ws_resident(const LaunchCtx& ctx, uint64_t* resident) {
         q.attrs = qa;
         q.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess || n <= 0) {
+        if (cudaOccupancyMaxActiveClusters(&n, ws_kernel_for<CG, KIND, TMA_STORE, EPI2>(Bld::kPlain), &q) !=
+                cudaSuccess ||
+            n <= 0) {
           cudaGetLastError();
           n = ctx.num_sms / 2;
         }
@@ -83,7 +119,6 @@ int ws_streamk_split_tiles(const Problem& p, const LaunchCtx& ctx, uint32_t* sk_
 template <int CG, Kind KIND, bool TMA_STORE, bool EPI2 = false>
 int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) {
   using C = GemmCfg<CG, KIND, TMA_STORE, EPI2>;
-  auto kern = gemm_ws_kernel<CG, KIND, TMA_STORE, EPI2>;
   uint64_t resident = 0;
   if (const int rc = ws_resident<CG, KIND, TMA_STORE, EPI2>(ctx, &resident); rc != GEMM_OK) return rc;
 
@@ -229,6 +264,9 @@ int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) 
     cfg.gridDim = dim3(static_cast<unsigned>(clusters));
   }
   note_schedule(static_cast<uint32_t>(clusters), CG, a.dp_tiles, a.sk_tiles, a.sk_unit, a.half_tiles);
+  const auto kern =
+      ws_kernel_for<CG, KIND, TMA_STORE, EPI2>(a.sk_tiles == 0 && a.epi_mode == 0 && a.c_tma == 0);
+  if (kern == nullptr) return GEMM_ERR_INVALID_ARG;
   const cudaError_t err =
       cudaLaunchKernelEx(&cfg, kern, maps.A, maps.B, maps.D, maps.SFA, maps.SFB, maps.Bh, maps.C, a);
   if (err != cudaSuccess) {
