@@ -886,7 +886,22 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
         if (!wait_bounded(acce_bar(b), (around & 1u) ^ 1u, wd, kSiteMmaAccEmpty)) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + b * C::UMMA_N;
-        const uint32_t n_mma = item_cols(w, C::UMMA_N);   // N of this item's MMAs
+        // N of this item's MMAs: the item's columns; in the one-CTA bf16
+        // kernels only those inside N, rounded up to the epilogue's chunk (a
+        // tile at the right edge of D with 5 live columns multiplies 64, not
+        // 256).  Not in the pair: there the MMA takes N / 2 B rows from each
+        // CTA's stage, so its N is tied to the height of the B box the
+        // producer loaded (UMMA_N / 2 rows, or a quarter for a column half).
+        uint32_t n_mma = item_cols(w, C::UMMA_N);
+        if constexpr (KIND == Kind::BF16 && CG == 1) {
+          uint32_t mb, nb;
+          tile_coords(w.tile, args.num_m_blocks, args.num_n_blocks, args.group_m, mb, nb);
+          const uint32_t n0 = item_n0(w, nb, C::UMMA_N);
+          constexpr uint32_t kChunk = TMA_STORE ? C::TS_COLS : 32u;
+          const uint32_t live_cols = args.N > n0 ? args.N - n0 : 0u;
+          const uint32_t need = live_cols == 0 ? kChunk : (live_cols + kChunk - 1) / kChunk * kChunk;
+          if (need < n_mma) n_mma = need;
+        }
         bool ok = true;
         // Unrolled in the pair kernels (measured: +1-3% bf16 with 4, +2.4% MXFP8 with 2;
         // the one-CTA MXFP8 kernel measured slightly slower unrolled).
