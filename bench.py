@@ -22,6 +22,7 @@ from __future__ import annotations
 
 import argparse
 import csv
+import datetime
 import hashlib
 import io
 import json
@@ -105,16 +106,17 @@ def stored_traffic(kernel_key: str):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples while the timed region runs,
-    every 20 ms.  A sample counts as under load when the board draws at least
-    30% of its power limit; sm_mhz is the median over those (over all samples
-    when there are none).  A timed region of a few
-    tens of milliseconds holds few samples, and samples between kernels show
-    the idle boost clock, so the count is reported too."""
+    """nvidia-smi clock / throttle-reason samples around the timed region,
+    every 10 ms, each with its host timestamp.  sm_mhz is the median over the
+    samples taken inside the timed region's wall-clock window; with none
+    there, over the samples under load (the board drawing at least 30% of its
+    power limit -- nvidia-smi averages power.draw over a window longer than a
+    short region, so short regions rarely show it), else over all samples.
+    The counts are reported too."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
-             "power.limit")
+             "power.limit,timestamp")
 
     def __init__(self, index: int):
         self.index = index
@@ -125,12 +127,21 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "20"],
+                 "--format=csv,noheader,nounits", "-lms", "10"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (FileNotFoundError, OSError):
             self.proc = None
 
-    def stop(self):
+    @staticmethod
+    def _stamp(x):
+        try:
+            return datetime.datetime.strptime(x.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
+    def stop(self, window=None):
+        """Stop sampling and summarise; window = (start, end) of the timed
+        region in host seconds since the epoch (time.time())."""
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -156,7 +167,14 @@ class ClockSampler:
         pmax = max(power) if power else None
         loaded = [c for c, w, lim in pairs
                   if c is not None and w is not None and lim is not None and w >= 0.3 * lim]
-        return {"sm_mhz": statistics.median(loaded or sm) if sm else None,
+        inside = []
+        if window is not None:
+            for r, (c, _, _) in zip(rows, pairs):
+                ts = self._stamp(r[10]) if len(r) > 10 else None
+                if c is not None and ts is not None and window[0] <= ts <= window[1]:
+                    inside.append(c)
+        return {"sm_mhz": statistics.median(inside or loaded or sm) if sm else None,
+                "samples_in_region": len(inside),
                 "sm_mhz_all_samples": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None,
                 "reasons": reasons, "active_masks": sorted({r[4].strip() for r in rows}),
@@ -620,12 +638,14 @@ def run_ours(args, rank, world, local):
     starts = ends = None
     if per_launch:
         starts, ends = event_grid(args.steps), event_grid(args.steps)
+    wall0 = time.time()
     t0.record(stream)
     launches(args.steps, starts, ends)
     t1.record(stream)
     torch.cuda.synchronize(device)
+    wall1 = time.time()
     barrier(world)
-    clk = clocks.stop()
+    clk = clocks.stop((wall0, wall1))
     st = g.gemm_last_status(sh)
     if st != g.GEMM_OK:
         raise g.GemmError(st, "timed region")

@@ -87,3 +87,35 @@ def test_clock_sampler_takes_the_median_under_load():
     s.proc = FakeProc()
     clk = s.stop()
     assert clk["samples_under_load"] == 0 and clk["sm_mhz"] == 2070.0
+
+
+def test_clock_sampler_prefers_samples_inside_the_timed_region():
+    # the same fields plus the host timestamp; power.draw is an average that
+    # a short region never lifts, so only the timestamps tell which samples
+    # fall inside it
+    import datetime
+    t = [datetime.datetime(2026, 1, 2, 3, 4, 5, 100000 * i) for i in range(6)]
+    f = [x.strftime("%Y/%m/%d %H:%M:%S.%f")[:-3] for x in t]
+    rows = [
+        f"0, 2070, 2070, 150.0, 0x0, Not Active, Not Active, Not Active, Not Active, 1400.00, {f[0]}",
+        f"0, 1710, 2070, 160.0, 0x0, Not Active, Not Active, Not Active, Not Active, 1400.00, {f[2]}",
+        f"0, 1690, 2070, 170.0, 0x0, Not Active, Not Active, Not Active, Not Active, 1400.00, {f[3]}",
+        f"0, 1700, 2070, 170.0, 0x0, Not Active, Not Active, Not Active, Not Active, 1400.00, {f[4]}",
+        f"0, 2070, 2070, 175.0, 0x0, Not Active, Not Active, Not Active, Not Active, 1400.00, {f[5]}",
+    ]
+
+    class FakeProc:
+        def terminate(self):
+            pass
+
+        def communicate(self, timeout=None):
+            return "\n".join(rows) + "\n", ""
+
+    s = bench.ClockSampler(0)
+    s.proc = FakeProc()
+    clk = s.stop((t[1].timestamp(), t[4].timestamp() + 0.01))
+    assert clk["samples"] == 5 and clk["samples_under_load"] == 0
+    assert clk["samples_in_region"] == 3 and clk["sm_mhz"] == 1700.0
+    s.proc = FakeProc()
+    clk = s.stop()   # no window: nothing inside, the median over all samples
+    assert clk["samples_in_region"] == 0 and clk["sm_mhz"] == 1710.0
