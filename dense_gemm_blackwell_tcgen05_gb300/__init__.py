@@ -29,7 +29,7 @@ __all__ = [
     "gemm_streamk_workspace_bytes", "gemm_last_schedule", "streamk_workspace",
     "gemm_bf16_streamk_noalloc", "gemm_set_streamk_mode", "STREAMK_AUTO", "STREAMK_ALWAYS",
     "STREAMK_NEVER", "gemm_streamk_plan", "gemm_set_tail_split", "gemm_tail_split_plan",
-    "gemm_bf16_fused", "gemm_mxfp8_fused", "GemmEpilogue",
+    "gemm_set_edge_last", "gemm_bf16_fused", "gemm_mxfp8_fused", "GemmEpilogue",
     "make_epilogue", "matmul_fused", "DTYPE_BF16", "DTYPE_F32", "ACT_NONE", "ACT_RELU", "ACT_GELU", "matmul_bf16",
     "matmul_mxfp8",
 ]
@@ -59,6 +59,7 @@ EXPORTED_SYMBOLS = (
     "gemm_last_schedule", "gemm_bf16_streamk_noalloc", "gemm_set_streamk_mode",
     "gemm_streamk_plan", "gemm_bf16_fused", "gemm_mxfp8_fused", "gemm_mxfp8_tiled",
     "gemm_mxfp8_quantize_tiled", "gemm_set_tail_split", "gemm_tail_split_plan",
+    "gemm_set_edge_last",
 )
 
 _lock = threading.Lock()
@@ -139,6 +140,8 @@ def load() -> ctypes.CDLL:
             L.gemm_last_schedule.restype = ctypes.c_int
             L.gemm_set_tail_split.argtypes = [ctypes.c_int]
             L.gemm_set_tail_split.restype = ctypes.c_int
+            L.gemm_set_edge_last.argtypes = [ctypes.c_int]
+            L.gemm_set_edge_last.restype = ctypes.c_int
             L.gemm_tail_split_plan.argtypes = [_i64, _i64]
             L.gemm_tail_split_plan.restype = _i64
             L.gemm_mxfp8_quantize.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp]
@@ -225,6 +228,10 @@ def gemm_set_streamk_mode(mode: int) -> int:
 
 def gemm_set_tail_split(enable: int) -> int:
     return load().gemm_set_tail_split(enable)
+
+
+def gemm_set_edge_last(enable: int) -> int:
+    return load().gemm_set_edge_last(enable)
 
 
 def gemm_tail_split_plan(tiles: int, resident: int) -> int:
@@ -317,12 +324,12 @@ def gemm_streamk_plan(tiles: int, resident: int, k_tiles: int, unit: int,
 
 def gemm_last_schedule() -> dict:
     """Schedule of this thread's last persistent-kernel launch."""
-    out = (ctypes.c_int64 * 6)()
+    out = (ctypes.c_int64 * 7)()
     rc = load().gemm_last_schedule(out)
     if rc != GEMM_OK:
         raise GemmError(rc, "gemm_last_schedule")
     return {"clusters": out[0], "ctas_per_cluster": out[1], "dp_tiles": out[2],
-            "sk_tiles": out[3], "sk_unit": out[4], "half_tiles": out[5]}
+            "sk_tiles": out[3], "sk_unit": out[4], "half_tiles": out[5], "edge_last": out[6]}
 
 
 def streamk_workspace(mxfp8: bool = False, variant: int = VARIANT_AUTO, device=None):

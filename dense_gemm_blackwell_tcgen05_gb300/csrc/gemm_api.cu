@@ -35,10 +35,11 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::atomic<int64_t> g_watchdog_ms{-1};
 std::atomic<int> g_streamk_mode{kStreamKAuto};
 std::atomic<int> g_tail_split{1};
+std::atomic<int> g_edge_last{1};
 std::atomic<uint32_t> g_streamk_epoch{0};
 thread_local int t_last_cuda_error = 0;
 thread_local int64_t t_stall_next = -1;   // one-shot watchdog test hook
-thread_local int64_t t_schedule[6] = {0, 0, 0, 0, 0, 0};
+thread_local int64_t t_schedule[7] = {0, 0, 0, 0, 0, 0, 0};
 
 // Consumes the calling thread's pending stall request, if any.
 uint32_t take_stall() {
@@ -224,14 +225,17 @@ uint32_t next_streamk_epoch() {
   return e;
 }
 
+bool edge_last_enabled() { return g_edge_last.load() != 0; }
+
 void note_schedule(uint32_t clusters, uint32_t cg, uint32_t dp_tiles, uint32_t sk_tiles,
-                   uint32_t sk_unit, uint32_t half_tiles) {
+                   uint32_t sk_unit, uint32_t half_tiles, uint32_t edge_last) {
   t_schedule[0] = clusters;
   t_schedule[1] = cg;
   t_schedule[2] = dp_tiles;
   t_schedule[3] = sk_tiles;
   t_schedule[4] = sk_unit;
   t_schedule[5] = half_tiles;
+  t_schedule[6] = edge_last;
 }
 
 namespace {
@@ -656,6 +660,11 @@ int gemm_set_tail_split(int enable) {
   return g_tail_split.exchange(enable);
 }
 
+int gemm_set_edge_last(int enable) {
+  if (enable != 0 && enable != 1) return GEMM_ERR_INVALID_ARG;
+  return g_edge_last.exchange(enable);
+}
+
 int64_t gemm_tail_split_plan(int64_t tiles, int64_t resident) {
   if (tiles < 0 || resident < 0 || tiles > 0xFFFFFFFFll || resident > 0xFFFFFFFFll)
     return GEMM_ERR_INVALID_ARG;
@@ -684,7 +693,7 @@ int gemm_streamk_plan(int64_t tiles, int64_t resident, int64_t k_tiles, int64_t 
 
 int gemm_last_schedule(int64_t* out) {
   if (out == nullptr) return GEMM_ERR_INVALID_ARG;
-  for (int i = 0; i < 6; ++i) out[i] = t_schedule[i];
+  for (int i = 0; i < 7; ++i) out[i] = t_schedule[i];
   return GEMM_OK;
 }
 

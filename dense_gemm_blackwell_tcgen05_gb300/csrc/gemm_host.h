@@ -125,7 +125,9 @@ struct Maps {
 void note_cuda_error(cudaError_t e);
 // Records the calling thread's last persistent-kernel schedule (gemm_last_schedule).
 void note_schedule(uint32_t clusters, uint32_t cg, uint32_t dp_tiles, uint32_t sk_tiles,
-                   uint32_t sk_unit, uint32_t half_tiles);
+                   uint32_t sk_unit, uint32_t half_tiles, uint32_t edge_last);
+// Whether plain bf16 launches may deal right-edge tiles last (gemm_set_edge_last).
+bool edge_last_enabled();
 
 // Encodes a 2-D tiled tensor map (rows of `inner` elements, pitch in bytes).
 // Returns false when the driver rejects it.

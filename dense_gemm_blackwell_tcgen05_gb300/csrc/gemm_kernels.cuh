@@ -61,6 +61,14 @@ struct GemmArgs {
   // a work item of its own, so a last round that would leave most clusters
   // idle takes about half a tile's time.
   uint32_t half_tiles;
+  // Right-edge tiles last (plain bf16 launches whose last column block holds
+  // at most UMMA_N / 2 live columns): the last column block's tiles come
+  // after all others, and rounds are dealt in alternating directions, so the
+  // cheap edge tiles fill the last round and land on the clusters that took
+  // full tiles last.  edge_half: the edge tiles run as first column halves
+  // (set with edge_last).  0 otherwise.
+  uint32_t edge_last;
+  uint32_t edge_half;
   float* ws_part;             // stream-K partial accumulators, one slot per cluster
   uint32_t* ws_flag;          // per (slot, CTA, epilogue warp) ready flags
   uint32_t epoch;             // this launch's flag value (never 0)
@@ -105,13 +113,45 @@ __device__ __forceinline__ uint64_t sk_bound(uint64_t units, uint32_t c, uint32_
   return units * c / G;
 }
 
+// Block coordinates of tile t: the grouped raster of tile_coords, or, with
+// edge_last (EDGE builds), that raster over all column blocks but the last,
+// followed by the last column block's tiles in row order.
+template <bool EDGE>
+__device__ __forceinline__ void item_coords(const GemmArgs& a, uint32_t t, uint32_t& mb, uint32_t& nb) {
+  if (EDGE && a.edge_last != 0) {
+    const uint32_t nf = a.num_n_blocks - 1;
+    const uint32_t e0 = a.num_m_blocks * nf;
+    if (t >= e0) {
+      mb = t - e0;
+      nb = nf;
+      return;
+    }
+    tile_coords(t, a.num_m_blocks, nf, a.group_m, mb, nb);
+    return;
+  }
+  tile_coords(t, a.num_m_blocks, a.num_n_blocks, a.group_m, mb, nb);
+}
+
 // The wi-th work item of cluster c among G clusters; false past the last.
 // Every role of every CTA calls this with the same arguments, so they all
 // walk the same sequence.  SK = false: a kernel built without stream-K
-// (launched only with sk_tiles == 0).
-template <bool SK = true>
+// (launched only with sk_tiles == 0).  EDGE: a build that honours edge_last.
+template <bool SK = true, bool EDGE = false>
 __device__ __forceinline__ bool work_item(const GemmArgs& a, uint32_t c, uint32_t G, uint32_t KT,
                                           uint32_t wi, WorkItem& w) {
+  if (EDGE && a.edge_last != 0) {
+    // whole tiles only (no tail split, no stream-K): round wi deals tiles
+    // wi G .. wi G + G - 1, to clusters 0 .. G-1 in even rounds and G-1 .. 0
+    // in odd ones; the pair runs an edge tile as a first column half
+    const uint32_t x = wi * G + ((wi & 1u) ? G - 1u - c : c);
+    if (x >= a.dp_tiles) return false;
+    w.tile = x;
+    w.half = (a.edge_half != 0 && x >= a.num_m_blocks * (a.num_n_blocks - 1)) ? 1u : 0u;
+    w.k_begin = 0;
+    w.k_end = KT;
+    w.kind = 0;
+    return true;
+  }
   // data-parallel items: the whole tiles, then two halves of each of the
   // last half_tiles tiles
   const uint32_t n_items = a.dp_tiles + a.half_tiles;
@@ -712,6 +752,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
                    const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
   using C = GemmCfg<CG, KIND, TMA_STORE, EPI2>;
   // the launch's fused-epilogue mode and C-by-TMA flag (none in a plain build)
+  constexpr bool EDGE = PLAIN && KIND == Kind::BF16;   // builds that honour edge_last
   const uint32_t epi_mode = PLAIN ? 0u : args.epi_mode;
   const uint32_t c_tma = PLAIN ? 0u : args.c_tma;
   extern __shared__ uint8_t smem_raw[];
@@ -752,42 +793,37 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
   const uint32_t num_clusters = gridDim.x / CG;
   const Watchdog wd{args.status, args.timeout_ns, abort_flag};
 
-  // ---- set-up: barriers (one thread), TMEM allocation (one warp) ----------
-  if (warp == 0 && lane == 0) {
-    for (uint32_t s = 0; s < C::STAGES; ++s) {
-      mbar_init(full_bar(s), C::FULL_ARRIVALS);  // producer's expect_tx (+ TMA bytes)
-      mbar_init(empty_bar(s), 1);                // MMA issuer's commit
-      if constexpr (C::SF_TILED) mbar_init(sf_full_bar(s), 1);   // producer's expect_tx (+ scale bytes)
+  // ---- set-up: descriptor prefetches and barriers (warp 0, the barriers one
+  // per lane), TMEM allocation (warp 1) ----------------------------------------
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      if (args.half_tiles != 0 || args.edge_half != 0) tma_prefetch_desc(&tmBh);
+      if (c_tma != 0) tma_prefetch_desc(&tmC);
+      if constexpr (TMA_STORE) tma_prefetch_desc(&tmD);
+      if (C::MX && !args.sf_gather) {
+        tma_prefetch_desc(&tmSFA);
+        tma_prefetch_desc(&tmSFB);
+      }
+      *abort_flag = 0u;
     }
-    for (uint32_t g = 0; g < C::RAW_SLOTS; ++g) {
-      mbar_init(raw_full_bar(g), 1);   // this CTA's scale bytes landed (expect_tx)
+    // Arrival counts: the producer's expect_tx (ready barriers), one commit
+    // (free, accumulator-full, drain, scale-slot-free barriers), one arrival
+    // per transfer (fix-up ring, C chunks), and
+    //   t_ready: every CTA's scale-factor warp once per group (tiled scales:
+    //            the copy thread's commit);
+    //   acc_empty: every epilogue warp of the pair.
+    constexpr uint32_t kNumBars = kCBar0 + 4 + (C::SF_TILED ? C::STAGES : 0u);
+    static_assert(kNumBars * 8 <= C::BAR_BYTES && C::FULL_ARRIVALS == 1, "barrier area");
+    for (uint32_t i = lane; i < kNumBars; i += 32) {
+      if (i == kAccBar0 + 5) continue;   // the TMEM address and the abort flag
+      uint32_t count = 1;
+      if (i >= kTBar0 && i < kTBar0 + C::T_SLOTS) count = C::SF_TILED ? 1u : static_cast<uint32_t>(CG);
+      if (i >= kAccBar0 + 2 && i < kAccBar0 + 4) count = 4 * CG * C::EPI_WG;
+      mbar_init(bar0 + 8 * i, count);
     }
-    for (uint32_t g = 0; g < C::T_SLOTS; ++g) {
-      // leader: every CTA's SF warp filled the slot (tiled scales: scale set
-      // g of TMEM written, the copy thread's commit)
-      mbar_init(t_ready_bar(g), C::SF_TILED ? 1 : CG);
-      // MMA issuer's commit after the group's last K-tile (tiled scales: g = 0
-      // is the copy thread's exit drain)
-      mbar_init(t_empty_bar(g), 1);
-    }
-    for (uint32_t b = 0; b < 2; ++b) {
-      mbar_init(accf_bar(b), 1);        // MMA issuer's commit after the last K-tile
-      mbar_init(acce_bar(b), 4 * CG * C::EPI_WG);   // every epilogue warp of the pair
-    }
-    mbar_init(drain_bar, 1);
-    for (uint32_t i = 0; i < C::FIX_TOTAL; ++i) mbar_init(bar0 + 8 * (kFixBar0 + i), 1);
-    for (uint32_t i = 0; i < 4; ++i) mbar_init(bar0 + 8 * (kCBar0 + i), 1);
-    *abort_flag = 0u;
     fence_mbar_init();
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
-    if (args.half_tiles != 0) tma_prefetch_desc(&tmBh);
-    if (c_tma != 0) tma_prefetch_desc(&tmC);
-    if constexpr (TMA_STORE) tma_prefetch_desc(&tmD);
-    if (C::MX && !args.sf_gather) {
-      tma_prefetch_desc(&tmSFA);
-      tma_prefetch_desc(&tmSFB);
-    }
   }
   if (warp == 1) {
     tmem_alloc<CG>(smem_addr(tmem_slot), C::TMEM_COLS);
@@ -808,9 +844,9 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
       uint32_t it = 0;
       bool ok = true;
       WorkItem w;
-      for (uint32_t wi = 0; ok && work_item<!PLAIN>(args, cluster_id, num_clusters, KT, wi, w); ++wi) {
+      for (uint32_t wi = 0; ok && work_item<!PLAIN, EDGE>(args, cluster_id, num_clusters, KT, wi, w); ++wi) {
         uint32_t mb, nb;
-        tile_coords(w.tile, args.num_m_blocks, args.num_n_blocks, args.group_m, mb, nb);
+        item_coords<EDGE>(args, w.tile, mb, nb);
         const int32_t a_row = static_cast<int32_t>(mb * C::UMMA_M + rank * C::BLOCK_M);
         // this CTA's share of the item's B rows: B_ROWS, or half of them
         // for a column half (through the half-height box of tmBh)
@@ -879,7 +915,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
       uint32_t it = 0, j = 0, gi = 0;
       bool issued = false;
       WorkItem w;
-      for (uint32_t wi = 0; work_item<!PLAIN>(args, cluster_id, num_clusters, KT, wi, w); ++wi, ++j) {
+      for (uint32_t wi = 0; work_item<!PLAIN, EDGE>(args, cluster_id, num_clusters, KT, wi, w); ++wi, ++j) {
         const uint32_t b = j % C::ACC_STAGES;
         const uint32_t around = j / C::ACC_STAGES;
         // accumulator b must have been drained by every epilogue warp
@@ -895,7 +931,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
         uint32_t n_mma = item_cols(w, C::UMMA_N);
         if constexpr (KIND == Kind::BF16 && CG == 1) {
           uint32_t mb, nb;
-          tile_coords(w.tile, args.num_m_blocks, args.num_n_blocks, args.group_m, mb, nb);
+          item_coords<EDGE>(args, w.tile, mb, nb);
           const uint32_t n0 = item_n0(w, nb, C::UMMA_N);
           constexpr uint32_t kChunk = TMA_STORE ? C::TS_COLS : 32u;
           const uint32_t live_cols = args.N > n0 ? args.N - n0 : 0u;
@@ -984,7 +1020,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
       uint32_t it = 0;
       bool issued = false, ok = true;
       WorkItem w;
-      for (uint32_t wi = 0; ok && work_item<!PLAIN>(args, cluster_id, num_clusters, KT, wi, w); ++wi) {
+      for (uint32_t wi = 0; ok && work_item<!PLAIN, EDGE>(args, cluster_id, num_clusters, KT, wi, w); ++wi) {
         for (uint32_t kt = w.k_begin; kt < w.k_end; ++kt, ++it) {
           const uint32_t s = it % C::STAGES;
           if (!wait_bounded(sf_full_bar(s), (it / C::STAGES) & 1u, wd, kSiteSfFull)) { ok = false; break; }
@@ -1033,7 +1069,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
     const auto cur_first = [&](GroupCursor& g) {
       g.wi = 0;
       g.q = 0;
-      g.valid = work_item<!PLAIN>(args, cluster_id, num_clusters, KT, 0, g.w);
+      g.valid = work_item<!PLAIN, EDGE>(args, cluster_id, num_clusters, KT, 0, g.w);
     };
     const auto cur_next = [&](GroupCursor& g) {
       if (!g.valid) return;
@@ -1041,7 +1077,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
       if (++g.q < ng) return;
       g.q = 0;
       ++g.wi;
-      g.valid = work_item<!PLAIN>(args, cluster_id, num_clusters, KT, g.wi, g.w);
+      g.valid = work_item<!PLAIN, EDGE>(args, cluster_id, num_clusters, KT, g.wi, g.w);
     };
     const uint64_t pol = l2_policy_evict_last();
     const uint32_t nblk = (args.K + 31u) / 32u;
@@ -1052,7 +1088,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
     // as after the TMA bytes).
     const auto load_group = [&](const GroupCursor& g, uint32_t gi) {
       uint32_t mb, nb;
-      tile_coords(g.w.tile, args.num_m_blocks, args.num_n_blocks, args.group_m, mb, nb);
+      item_coords<EDGE>(args, g.w.tile, mb, nb);
       const uint32_t r = gi % C::RAW_SLOTS;
       const uint32_t slot = raw0 + r * C::RAW_SLOT_BYTES;
       const uint32_t kb0 = (g.w.k_begin / C::SF_GROUP + g.q) * 16;
@@ -1186,13 +1222,13 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
       return true;
     };
     WorkItem w;
-    for (uint32_t wi = 0; ok && work_item<!PLAIN>(args, cluster_id, num_clusters, KT, wi, w); ++wi, ++j) {
+    for (uint32_t wi = 0; ok && work_item<!PLAIN, EDGE>(args, cluster_id, num_clusters, KT, wi, w); ++wi, ++j) {
       const uint32_t b = j % C::ACC_STAGES;
       const uint32_t around = j / C::ACC_STAGES;
       if constexpr (kCTma) {
         if (c_tma != 0 && w.kind != 2) {
           uint32_t mb0, nb0;
-          tile_coords(w.tile, args.num_m_blocks, args.num_n_blocks, args.group_m, mb0, nb0);
+          item_coords<EDGE>(args, w.tile, mb0, nb0);
           const uint32_t r0 = mb0 * C::UMMA_M + rank * C::BLOCK_M + q * 32;
           const uint32_t c0 = item_n0(w, nb0, C::UMMA_N);
           if (r0 < args.M && c0 < args.N) {
@@ -1204,7 +1240,7 @@ __global__ void __launch_bounds__(GemmCfg<CG, KIND, TMA_STORE, EPI2>::kThreads, 
       if (!warp_wait(accf_bar(b), around & 1u, wd, kSiteEpiAccFull, lane)) break;
       tc_fence_after_sync();
       uint32_t mb, nb;
-      tile_coords(w.tile, args.num_m_blocks, args.num_n_blocks, args.group_m, mb, nb);
+      item_coords<EDGE>(args, w.tile, mb, nb);
       const uint32_t row0 = mb * C::UMMA_M + rank * C::BLOCK_M + q * 32;
       const uint32_t col_base = item_n0(w, nb, C::UMMA_N);
       const uint32_t t_addr = tmem_base + ((q * 32u) << 16) + b * C::UMMA_N;

@@ -243,7 +243,22 @@ int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) 
       clusters = items < resident ? items : resident;
     }
   }
-  if (a.half_tiles != 0 &&
+  // Right-edge tiles last (plain bf16 launches whose last column block holds
+  // at most UMMA_N / 2 live columns): those tiles run as first column halves
+  // and end the deal, instead of a tail split.
+  a.edge_last = 0;
+  a.edge_half = 0;
+  if constexpr (KIND == Kind::BF16) {
+    const uint32_t rem = p.N % C::UMMA_N;
+    if (a.sk_tiles == 0 && a.epi_mode == 0 && a.c_tma == 0 && rem != 0 && rem <= C::UMMA_N / 2 &&
+        a.num_n_blocks >= 2 && edge_last_enabled()) {
+      a.edge_last = 1;
+      a.edge_half = 1;
+      a.half_tiles = 0;
+      clusters = tiles < resident ? tiles : resident;
+    }
+  }
+  if ((a.half_tiles != 0 || a.edge_half != 0) &&
       !encode_map_2d(&maps.Bh, dt, p.B, p.K, p.N, p.ldb * C::ELEM, C::BK, C::B_ROWS / 2,
                      CU_TENSOR_MAP_SWIZZLE_128B))
     return GEMM_ERR_LAUNCH;
@@ -263,7 +278,8 @@ int launch_ws_impl(const Problem& p, const LaunchCtx& ctx, cudaStream_t stream) 
   } else {
     cfg.gridDim = dim3(static_cast<unsigned>(clusters));
   }
-  note_schedule(static_cast<uint32_t>(clusters), CG, a.dp_tiles, a.sk_tiles, a.sk_unit, a.half_tiles);
+  note_schedule(static_cast<uint32_t>(clusters), CG, a.dp_tiles, a.sk_tiles, a.sk_unit, a.half_tiles,
+                a.edge_last);
   const auto kern =
       ws_kernel_for<CG, KIND, TMA_STORE, EPI2>(a.sk_tiles == 0 && a.epi_mode == 0 && a.c_tma == 0);
   if (kern == nullptr) return GEMM_ERR_INVALID_ARG;

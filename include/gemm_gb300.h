@@ -340,7 +340,8 @@ int gemm_last_cuda_error(void);
  * out[1] CTAs per cluster, out[2] tiles computed whole (column halves
  * included), out[3] tiles split along K by the stream-K schedule, out[4]
  * K-tiles per stream-K unit, out[5] tiles of the last round cut into two
- * column halves (the tail split below).  `out` holds 6 values.  Returns
+ * column halves (the tail split below), out[6] 1 when right-edge tiles were
+ * dealt last (gemm_set_edge_last below).  `out` holds 7 values.  Returns
  * GEMM_OK, or GEMM_ERR_INVALID_ARG for NULL. */
 int gemm_last_schedule(int64_t* out);
 
@@ -362,6 +363,20 @@ int gemm_last_schedule(int64_t* out);
  * (host only), or GEMM_ERR_INVALID_ARG for negative or > 2^32 - 1 inputs. */
 int gemm_set_tail_split(int enable);
 int64_t gemm_tail_split_plan(int64_t tiles, int64_t resident);
+
+/* Right-edge tiles last (the same ladder level: tile order and tail).  When N
+ * is not a multiple of the tile width and the last column block holds at most
+ * half of it (1 <= N mod 256 <= 128), a plain bf16 launch (gemm_bf16 with no
+ * epilogue, no stream-K split) orders the tiles of that block after all
+ * others, runs each of them as a first column half (MMAs with N = 128), and
+ * deals rounds to clusters in alternating directions: the cheap edge tiles
+ * then fill the last round and land on the clusters that took full tiles
+ * last, where a tail split would have cut full tiles.  No tail split is made
+ * for such a launch.  Each element of D is computed as in a whole tile.
+ * gemm_set_edge_last(1) (the default) enables it process-wide, 0 disables
+ * it; returns the previous setting, or GEMM_ERR_INVALID_ARG for another
+ * value. */
+int gemm_set_edge_last(int enable);
 
 /* Test hook for the device watchdog (no counterpart on the pages: it exists to
  * exercise the failure path without faulting a GPU).  The calling thread's NEXT

@@ -165,7 +165,7 @@ def test_streamk_validation_without_device():
         g.GEMM_ERR_INVALID_ARG
     sched = g.gemm_last_schedule()
     assert set(sched) == {"clusters", "ctas_per_cluster", "dp_tiles", "sk_tiles", "sk_unit",
-                          "half_tiles"}
+                          "half_tiles", "edge_last"}
 
 
 def test_streamk_workspace_query_without_device():

@@ -1,6 +1,9 @@
 """Tail split of the data-parallel schedule: the tiles of a last, partial
 round are cut into two column halves (N = UMMA_N / 2 MMAs) when the halves fit
-in one round.
+in one round.  And its variant for a cheap last column block (right-edge tiles
+last): plain bf16 launches whose last column block holds at most half a tile
+run those tiles as first halves, ordered after all others, with rounds dealt
+in alternating directions.
 
 The halves cover disjoint columns of D and run the same K loop, so each
 element must come out bit for bit as it does from the whole tile: every GPU
@@ -62,13 +65,15 @@ def test_plan_switch_and_validation():
 
 # ------------------------------------------------------------ GPU parity
 
-def _launch(fn, split):
+def _launch(fn, split, edge=False):
     prev = g.gemm_set_tail_split(1 if split else 0)
+    prev_e = g.gemm_set_edge_last(1 if edge else 0)
     try:
         D = fn()
         sched = g.gemm_last_schedule()
     finally:
         g.gemm_set_tail_split(prev)
+        g.gemm_set_edge_last(prev_e)
     return D, sched
 
 
@@ -248,3 +253,76 @@ def test_mxfp8_tiled_split_matches_whole_tiles_and_oracle(case):
     rows, cols = P.sample_positions(M, N, 1500, seed=K, tile_n=128)
     Dr, S = oracle.gemm_mxfp8_entries(A.numpy(), B.numpy(), SFA.numpy(), SFB.numpy(), rows, cols)
     P.check_within_bound(D1.float().numpy()[rows, cols], Dr, S, f"mxfp8 split {case}")
+
+
+# ------------------------------------------------------------ right-edge tiles last
+
+def test_edge_last_switch_validation():
+    prev = g.gemm_set_edge_last(0)
+    try:
+        assert g.gemm_set_edge_last(1) == 0
+        assert g.gemm_set_edge_last(1) == 1
+    finally:
+        g.gemm_set_edge_last(prev)
+    assert g.gemm_set_edge_last(2) == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_set_edge_last(-1) == g.GEMM_ERR_INVALID_ARG
+
+
+# (variant, M, N, K, ldd): plain bf16 launches whose last column block holds
+# 1 <= N mod 256 <= 128 columns, over one or several rounds; the first is the
+# ragged bench workload (4099 x 2053 x 1040, 153 pair tiles, 17 of them edge
+# tiles).
+EDGE_CASES = [
+    ("2cta", 4099, 2053, 1040, 2053),
+    ("2cta", 5000, 1100, 136, 1100),
+    ("2cta_direct", 3000, 2053, 72, 2053),
+    ("1cta", 2560, 1100, 128, 1104),
+    ("1cta_direct", 5000, 1100, 72, 1103),
+    ("auto", 128, 1100, 64, 1100),
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", EDGE_CASES, ids=lambda c: f"{c[0]}-{c[1]}x{c[2]}x{c[3]}-ld{c[4]}")
+def test_edge_last_matches_whole_tiles_and_oracle(case):
+    v, M, N, K, ldd = case
+    A, B = gi.bf16_operands(M, N, K, seed=M + 2 * N + K)
+    D1, s1 = _launch(_bf16(A, B, VARIANT[v], ldd=ldd), split=True, edge=True)
+    D0, s0 = _launch(_bf16(A, B, VARIANT[v], ldd=ldd), split=False, edge=False)
+    assert s1["edge_last"] == 1 and s1["half_tiles"] == 0, s1
+    assert s0["edge_last"] == 0 and s0["half_tiles"] == 0, s0
+    assert s1["dp_tiles"] == s0["dp_tiles"]
+    _assert_same(D1, D0, f"edge-last {case}")
+    rows, cols = P.sample_positions(M, N, 1500, seed=K, tile_n=128)
+    cols[:64] = np.arange(N - 64, N)   # every column of the edge block
+    Dr, S = oracle.gemm_bf16_entries(gi.bf16_codes(A), gi.bf16_codes(B), rows, cols)
+    P.check_within_bound(D1.float().numpy()[rows, cols], Dr, S, f"edge-last {case}")
+    Ai, Bi = _ints(M, N, min(K, 96), seed=K + 3)
+    Di, si = _launch(_bf16(Ai, Bi, VARIANT[v], ldd=ldd), split=True, edge=True)
+    assert si["edge_last"] == 1
+    D_ref, _ = oracle.gemm_bf16(gi.bf16_codes(Ai), gi.bf16_codes(Bi))
+    _assert_oracle_bitwise(Di, D_ref, f"edge-last ints {case}")
+
+
+@pytest.mark.gpu
+def test_edge_last_only_for_plain_launches_with_a_cheap_edge():
+    # more than half a tile of live columns in the last block: the tail split
+    A, B = _ints(2600, 2000, 64, seed=21)
+    _, s = _launch(_bf16(A, B, g.VARIANT_2CTA), split=True, edge=True)
+    assert s["edge_last"] == 0 and s["half_tiles"] > 0, s
+    # N a multiple of the tile width: nothing to move
+    A, B = _ints(2600, 2048, 64, seed=22)
+    _, s = _launch(_bf16(A, B, g.VARIANT_2CTA), split=True, edge=True)
+    assert s["edge_last"] == 0, s
+    # a fused epilogue runs the general build: no edge ordering
+    A, B = _ints(2600, 1100, 64, seed=23)
+    bias = torch.zeros(1100, dtype=torch.float32, device="cuda")
+    epi = g.make_epilogue(1.0, 0.0, None, bias, "none", torch.bfloat16)
+    Df, s = _launch(_bf16(A, B, g.VARIANT_2CTA, epi=epi), split=True, edge=True)
+    assert s["edge_last"] == 0, s
+    D_ref, _ = oracle.gemm_bf16(gi.bf16_codes(A), gi.bf16_codes(B))
+    _assert_oracle_bitwise(Df, D_ref, "fused, edge ordering off")
+    # the MXFP8 kernels never take it
+    Am, SFA, Bm, SFB = gi.mxfp8_operands(700, 1100, 256, seed=24)
+    _, s = _launch(_mx_tiled(Am, SFA, Bm, SFB, g.VARIANT_AUTO), split=True, edge=True)
+    assert s["edge_last"] == 0, s
