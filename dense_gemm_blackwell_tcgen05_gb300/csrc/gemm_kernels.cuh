@@ -10,8 +10,11 @@
 //                        tiles), block-scaled MXFP8 operands with row-major
 //                        scales (128x224 / 256x224) or tiled scales
 //                        (128x256 / 256x256).  A short last round of tiles
-//                        may run as column halves; the fused epilogue can
-//                        bring C in by TMA.
+//                        may run as column halves, or a cheap last column
+//                        block's tiles as halves at the end of the deal; the
+//                        fused epilogue can bring C in by TMA.  A plain build
+//                        (PLAIN) leaves out the stream-K, fused-epilogue and
+//                        C-by-TMA code for launches that need none of it.
 //  * gemm_sync_kernel -- (gemm_sync.cuh) one 128x128 tile per CTA with synchronous thread
 //                        copies into shared memory and one MMA batch per
 //                        K-tile: the first rungs of the optimisation ladder,
