@@ -435,6 +435,11 @@ def step_unit(works):
     return sum(alg_bytes(w) for w in works), "GB/s", 1e9
 
 
+def workload_text(works) -> str:
+    """The config's workload name, the same string in both arms."""
+    return " + ".join(f"{w.name} {w.M}x{w.N}x{w.K} {w.kind}" for w in works)
+
+
 def sample_text(works, plan) -> str:
     return "; ".join(f"first {n} of {w.M * w.N} outputs (row-major) of {w.name} "
                      f"({w.M}x{w.N}x{w.K} {w.kind})" for w, n in zip(works, plan))
@@ -467,7 +472,7 @@ def run_reference(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": " + ".join(w.name for w in works), "parallelism": "none (CPU)"},
+        "config": {"workload": workload_text(works), "parallelism": "none (CPU)"},
         "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
                          "sample": sample_text(works, plan) + " per step"},
         "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -823,7 +828,7 @@ def run_ours(args, rank, world, local):
             "data": "synthetic (seeded; bf16 N(0,1)*0.5, MXFP8 quantised from N(0,1)"
                     + ("; MXFP8 scales passed in the tiled layout" if any(p.tiled for p in probs) else "")
                     + ")",
-            "config": {"workload": " + ".join(f"{w.name} {w.M}x{w.N}x{w.K} {w.kind}" for w in works),
+            "config": {"workload": workload_text(works),
                        "variant": args.variant,
                        "l2": ("512 MiB write before each launch of a workload whose inputs fit "
                               "in L2; its kernels' event time only" if any(flush_each)
