@@ -170,7 +170,8 @@ def test_k_zero(out):
     D = torch.full((M, N), float("nan"), dtype=out_dtype, device="cuda")
     Cd, bd = C.cuda(), bias.cuda()
     e = g.make_epilogue(3.0, -0.5, Cd, bd, "relu", out_dtype)
-    rc = g.gemm_bf16_fused(g.VARIANT_AUTO, A.cuda().data_ptr(), B.cuda().data_ptr(), D.data_ptr(),
+    Ad, Bd = A.cuda(), B.cuda()   # never read with K = 0, but kept alive all the same
+    rc = g.gemm_bf16_fused(g.VARIANT_AUTO, Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(),
                            M, N, 0, 8, 8, N, e, 0)
     assert rc == g.GEMM_OK and g.gemm_last_status(0) == g.GEMM_OK
     D_ref = oracle.epilogue(np.zeros((M, N)), 3.0, -0.5, f64(C), f64(bias), 1)
