@@ -374,6 +374,11 @@ static int bf16_impl(int variant, const void* A, const void* B, void* D, int64_t
   if (ws != nullptr && (base == GEMM_VARIANT_SYNC || !is_device_pointer(ws, ctx.device)))
     return GEMM_ERR_INVALID_ARG;
   bool tma_store = tma_store_ok(D, N, ldd, direct) && !(p.epi_mode & kEpiOutF32);
+  // A fused epilogue on the one-CTA kernel takes its masked-store build: the
+  // library builds no fused TMA-store one-CTA kernel (see launch_ws.cuh).
+  if (p.epi_mode != 0 &&
+      (base == GEMM_VARIANT_1CTA || (base == GEMM_VARIANT_AUTO && M <= 128)))
+    tma_store = false;
   // A launch that splits tiles along K sums the partial tiles in its epilogue
   // warps; the masked-store kernels have two epilogue groups against the
   // TMA-store kernels' one, which measured 11% faster on 1024x1024x16384.

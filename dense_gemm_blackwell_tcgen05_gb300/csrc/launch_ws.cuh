@@ -17,10 +17,14 @@ namespace gb300 {
 // the plain one (PLAIN = true) for bf16 and the tiled-scale MXFP8 kernels,
 // the general one for bf16 and the row-major-scale MXFP8 kernels (the
 // tiled-scale entry point never splits tiles along K or fuses an epilogue).
+// Not the general one-CTA bf16 TMA-store build: the launches that would need
+// it (a fused epilogue on one CTA; a stream-K split) take the masked-store
+// kernel, because that build faulted on one fused shape whose cause is not
+// known.
 template <int CG, Kind KIND, bool TMA_STORE, bool EPI2>
 struct WsBuilds {
   static constexpr bool kPlain = KIND != Kind::MXF8 && !EPI2;
-  static constexpr bool kGeneral = KIND != Kind::MXF8T;
+  static constexpr bool kGeneral = KIND != Kind::MXF8T && !(KIND == Kind::BF16 && CG == 1 && TMA_STORE);
   static_assert(kPlain || kGeneral, "at least one build");
 };
 

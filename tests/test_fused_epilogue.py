@@ -226,8 +226,9 @@ def test_odd_pitches_and_ragged_edges(out):
 
 @pytest.mark.parametrize("v", ["1cta", "2cta"])
 def test_c_by_tma_matches_loaded_c(v):
-    """The TMA-store kernels bring a 16-byte-aligned bf16 C in by TMA, one
-    64-column chunk ahead; the masked-store kernels load it per thread.  The
+    """The pair's TMA-store kernel brings a 16-byte-aligned bf16 C in by TMA,
+    one 64-column chunk ahead; the masked-store kernels load it per thread (a
+    fused epilogue on one CTA always takes the masked-store kernel).  The
     arithmetic after that is the same, so the two agree bit for bit on random
     data (GELU, ragged edges, C pitch other than D's, several chunks and tiles
     per CTA), and both stay within the bound of the oracle."""
