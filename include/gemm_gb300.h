@@ -93,7 +93,8 @@ typedef enum {
                                         MXFP8), except that a stream-K launch that
                                         splits tiles (bf16, or MXFP8 on one CTA)
                                         takes the masked kernel, whose two epilogue
-                                        warpgroups share the partial sums          */
+                                        warpgroups share the partial sums, and so
+                                        does a bf16 fused epilogue on one CTA      */
 } gemm_variant_t;
 
 /*
@@ -192,8 +193,8 @@ typedef struct gemm_epilogue {
 } gemm_epilogue_t;
 
 /* gemm_bf16_variant / gemm_mxfp8_variant with a fused epilogue (variants 0,
- * 1, 2, optionally | GEMM_VARIANT_DIRECT_STORE; an fp32 output always uses
- * the masked-store epilogue).  `epi` NULL means alpha = 1 and nothing else
+ * 1, 2, optionally | GEMM_VARIANT_DIRECT_STORE; an fp32 output, and a bf16
+ * call that runs on one CTA, always use the masked-store epilogue).  `epi` NULL means alpha = 1 and nothing else
  * (the plain entry points).  D holds elements of epi->out_dtype with pitch
  * ldd.  K == 0 gives D = act(alpha * 0 + beta * C + bias).  Errors as the
  * plain entry points, plus GEMM_ERR_INVALID_ARG for an unknown dtype or
